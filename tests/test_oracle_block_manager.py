@@ -1,0 +1,138 @@
+"""Pins for the Python block-manager model (the allocator's oracle)."""
+import json
+import os
+
+import pytest
+
+from oracle.block_manager import BlockManager, OutOfBlocks
+from paged_kv_cache_127_gb300 import synth
+
+G = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "block_tables.json")))
+
+
+def _pool_example():
+    g = G["pool"]
+    order = [b for t in g["tables"] for b in t] + [g["allocated"]]
+    order += [b for b in range(g["num_blocks"]) if b not in order]
+    bm = BlockManager(g["num_blocks"], g["block_size"], order)
+    seqs = []
+    for n in g["lengths"]:
+        s = bm.create()
+        bm.append(s, n)
+        seqs.append(s)
+    return g, bm, seqs
+
+
+def test_three_requests_tables_and_free_count():
+    g, bm, seqs = _pool_example()
+    assert [bm.table(s) for s in seqs] == g["tables"]
+    assert bm.num_free() == g["free_after"]
+
+
+def test_growth_adds_one_block_and_keeps_entries():
+    g, bm, seqs = _pool_example()
+    s = seqs[g["grow_seq"]]
+    before = bm.table(s)
+    slots, pairs = bm.append(s, g["grow_by"])
+    assert bm.length(s) == g["grown_len"]
+    assert bm.table(s) == g["grown_table"]
+    assert bm.table(s)[:len(before)] == before
+    assert len(bm.table(s)) == g["grown_blocks"] and pairs == []
+    # slots of the 10 new tokens: positions 47..56 through [0, 5, 9, 11]
+    assert slots == [9 * 16 + 15] + [11 * 16 + o for o in range(9)]
+
+
+def test_twenty_more_tokens_need_five_blocks():
+    g, bm, seqs = _pool_example()
+    bm.append(seqs[g["grow_seq"]], g["grow_by_alt"])
+    assert len(bm.table(seqs[g["grow_seq"]])) == g["grown_blocks_alt"]
+
+
+def test_full_shared_prefix_needs_no_copy():
+    g = G["full_prefix"]
+    bm = BlockManager(64, g["block_size"])
+    a = bm.create()
+    bm.append(a, g["prefix"])
+    assert len(bm.table(a)) == g["prefix_blocks"]
+    b = bm.fork(a)
+    slots, pairs = bm.append(b, 1)
+    assert len(pairs) == g["cow_pairs_on_next_token"]
+    assert bm.table(b)[:50] == bm.table(a) and len(bm.table(b)) == 51
+    assert bm.refcount(bm.table(b)[-1]) == 1
+    assert all(bm.refcount(x) == 2 for x in bm.table(a))
+
+
+def test_partial_shared_block_is_copied_on_write():
+    g = G["partial_cow"]
+    bm = BlockManager(8, g["block_size"])
+    a = bm.create()
+    bm.append(a, g["shared_tokens"])
+    assert bm.table(a) == g["shared_table"]
+    b = bm.fork(a)
+    slots, pairs = bm.append(b, 1)
+    assert pairs == [tuple(g["copy_pair"])]
+    assert bm.table(b) == g["b_table_after"]
+    assert bm.table(a) == g["a_table_after"]
+    assert {str(k): bm.refcount(k) for k in (0, 1, 2)} == g["refcounts_after"]
+    assert divmod(slots[0], g["block_size"]) == (g["b_new_slot_block"], g["b_new_slot_offset"])
+    # A's next write lands in P1 in place: it is no longer shared
+    slots_a, pairs_a = bm.append(a, 1)
+    assert pairs_a == [] and slots_a == [1 * 16 + 8]
+
+
+def test_refcount_teardown():
+    g = G["refcount_teardown"]
+    bm = BlockManager(4, 16)
+    a = bm.create()
+    bm.append(a, 16)
+    b = bm.fork(a)
+    p0 = bm.table(a)[0]
+    assert bm.refcount(p0) == g["refcount_before"]
+    bm.free_seq(a)
+    assert bm.refcount(p0) == g["refcount_after_a"]
+    assert (p0 in bm.free) == g["freed_after_a"]
+    bm.free_seq(b)
+    assert (p0 in bm.free) == g["freed_after_b"]
+
+
+def test_out_of_blocks_changes_nothing():
+    bm = BlockManager(3, 4)
+    a = bm.create()
+    bm.append(a, 6)
+    b = bm.fork(a)
+    snap = (bm.table(a), bm.table(b), list(bm.free), list(bm.ref))
+    with pytest.raises(OutOfBlocks):
+        bm.append(b, 7)                    # needs a copy + 2 new blocks, only 1 free
+    assert (bm.table(a), bm.table(b), list(bm.free), list(bm.ref)) == snap
+    bm.set_fail_after(0)
+    with pytest.raises(OutOfBlocks):
+        bm.append(a, 3)
+    assert (bm.table(a), bm.table(b), list(bm.free), list(bm.ref)) == snap
+
+
+def test_random_operations_keep_the_invariants():
+    rng = synth.make_rng(21)
+    bm = BlockManager(200, 8, synth.free_order(rng, 200))
+    live = []
+    for step in range(3000):
+        op = rng.integers(0, 10)
+        try:
+            if op == 0 or not live:
+                live.append(bm.create())
+            elif op == 1:
+                live.append(bm.fork(live[rng.integers(len(live))]))
+            elif op == 2:
+                bm.free_seq(live.pop(rng.integers(len(live))))
+            else:
+                bm.append(live[rng.integers(len(live))], int(rng.integers(0, 20)))
+        except OutOfBlocks:
+            pass
+        # refcount = number of tables listing the block; free <=> refcount 0
+        counts = [0] * 200
+        for s in live:
+            t = bm.table(s)
+            assert len(t) == -(-bm.length(s) // 8)
+            for x in t:
+                counts[x] += 1
+        assert counts == bm.ref
+        assert sorted(bm.free) == [x for x in range(200) if counts[x] == 0]
