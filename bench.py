@@ -1,0 +1,440 @@
+"""Benchmark of the paged decode hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = the whole hot path once over one batch: copy-on-write block copies
+(when the step has any), the KV write of one new token per sequence, and
+PagedAttention decode of one query per sequence over its full paged context
+(split-K partitions plus the merge).  Block tables, slots and copy pairs come
+from the library's allocator when the workload is set up.  The default
+workload is the 8B-shaped grouped-query layer: 256 sequences, 32 query heads
+over 8 KV heads, head_dim 128, bf16, 16-token blocks, lognormal lengths
+(median 600, clipped to [1, 4096]).
+
+Printed: one JSON line (rank 0).  `value` is KV-read GB/s over the whole step
+(KV bytes of every sequence's valid tokens / step time), inputs resident in
+HBM; `e2e` is the same metric through the binding with host buffers (pinned
+host -> device copies of the step's inputs and the device -> host copy of the
+output inside the timed region); `roofline` is the decode launch alone
+against the measured HBM copy bandwidth; `cpu_baseline` is the fp64 CPU
+oracle on a bounded sample.  Under torchrun each rank runs its own workload
+replica (different seed) -- the path has no cross-GPU exchange -- and the
+timing is the max over ranks.
+
+`--impl reference` times the CPU oracle (the only other implementation of
+this path) on the host cores, on the same workload, metric and units.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged-decode KV-read GB/s (% of GB300 HBM peak); decode query-tokens/s/layer"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 126 * 2**20
+KERNEL_SOURCES = ("pa_decode.cuh", "pa_device.cuh", "pa_cache_ops.cu", "pa_api.cu")
+
+
+# --------------------------------------------------------------------------- distributed helpers
+def dist_env():
+    """(rank, local_rank, world_size) from the torchrun environment (1-process default)."""
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def dist_init(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def reduce_scalar(dist, value: float, op: str, device=None) -> float:
+    """max / sum of a scalar over all ranks (identity with one process)."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if (device is not None and dist.get_backend() == "nccl") else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- peaks, clocks, profiles
+def measured_hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_127_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """ncu DRAM bytes per decode launch, if the summary matches the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"decode_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)\s+sources:\s*([0-9a-f]+)", text)
+    if not m or m.group(2) != kernel_source_hash():
+        return None
+    return int(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while it runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"pa_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- oracle timing
+def time_oracle(step, seq_ids):
+    """Run the fp64 CPU oracle (KV write then decode) for the given sequences; return seconds."""
+    import oracle
+    kc, vc = step.k_cache, step.v_cache
+    t0 = time.perf_counter()
+    oracle.write_kv(step.k_new[seq_ids], step.v_new[seq_ids], step.slots[seq_ids], kc, vc, step.dtype)
+    oracle.decode(step.q[seq_ids], kc, vc, step.tables[seq_ids], step.lens[seq_ids], step.scale, step.dtype)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(step, budget_s: float = 15.0):
+    """The oracle as it stands, single-threaded, on a bounded sample of sequences."""
+    rng = np.random.default_rng(12345)
+    order = rng.permutation(step.num_seqs)
+    done, secs, nbytes = [], 0.0, 0
+    per_tok = step.kv_bytes_per_token()
+    for s in order:
+        secs += time_oracle(step, np.array([s]))
+        done.append(int(s))
+        nbytes += int(step.lens[s]) * per_tok
+        if secs >= budget_s:
+            break
+    tokens = int(step.lens[done].sum())
+    return {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{len(done)} of {step.num_seqs} sequences ({tokens} context tokens), KV write + fp64 "
+                      f"decode, single thread, {secs:.1f} s",
+            "seconds": secs}
+
+
+# --------------------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+
+    from paged_kv_cache_127_gb300 import binding as pa
+    from paged_kv_cache_127_gb300 import workloads
+
+    rank, local_rank, world = dist_env()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    dist = dist_init(world, "nccl")
+
+    step = workloads.build_step(args.workload, seed=rank, binding=pa)
+    dims = step.dims(pa)
+    S, Hq, D = step.num_seqs, step.num_q_heads, step.head_dim
+
+    def bf(x):
+        if step.dtype == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(x))
+
+    # host (pinned) copies of the step's inputs, for the end-to-end leg
+    h_q, h_k, h_v = bf(step.q).pin_memory(), bf(step.k_new).pin_memory(), bf(step.v_new).pin_memory()
+    h_slots = torch.from_numpy(step.slots).pin_memory()
+    h_tables = torch.from_numpy(step.tables).pin_memory()
+    h_lens = torch.from_numpy(step.lens).pin_memory()
+    h_pairs = torch.from_numpy(np.ascontiguousarray(step.pairs)).pin_memory()
+    h_out = torch.empty((S, Hq, D), dtype=torch.float32).pin_memory()
+
+    d_q, d_k, d_v = h_q.to(device), h_k.to(device), h_v.to(device)
+    d_slots, d_tables, d_lens = h_slots.to(device), h_tables.to(device), h_lens.to(device)
+    d_pairs = h_pairs.to(device)
+    d_kc, d_vc = bf(step.k_cache).to(device), bf(step.v_cache).to(device)
+    d_out = torch.empty((S, Hq, D), dtype=torch.float32, device=device)
+    ws_bytes = pa.pa_decode_workspace_bytes(dims)
+    d_ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    npairs = int(step.pairs.shape[0])
+    # copy-on-write pairs apply once: after the first step the copies are in place and
+    # re-running them would copy identical bytes; they stay in the step for fidelity.
+    launches_per_step = 2 + (1 if ws_bytes else 0) + (1 if npairs else 0)
+
+    dec_ev = []
+
+    def device_step(record=False):
+        if npairs:
+            pa.pa_copy_blocks(dims, d_kc, d_vc, d_pairs, stream)
+        pa.pa_write_kv(dims, d_k, d_v, d_slots, d_kc, d_vc, stream)
+        if record:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        pa.pa_decode(dims, d_q, d_kc, d_vc, d_tables, d_lens, step.scale, d_out, d_ws, stream)
+        if record:
+            e1.record(stream)
+            dec_ev.append((e0, e1))
+
+    pa.pa_device_errors(clear=True)
+    sampler = ClockSampler(device.index).start() if rank == 0 else None
+    for _ in range(args.warmup):
+        device_step()
+    torch.cuda.synchronize(device)
+    assert pa.pa_device_errors(clear=True) == 0, "device error flags set during warm-up"
+
+    # ---- device-resident timing
+    barrier(dist, device)
+    torch.cuda.synchronize(device)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        device_step(record=True)
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(dist, device)
+    ms_local = t0.elapsed_time(t1)
+    dec_ms = float(np.mean([a.elapsed_time(b) for a, b in dec_ev]))
+    ms_total = reduce_scalar(dist, ms_local, "max", device)
+
+    # ---- end to end through the binding with host buffers
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    for _ in range(3):
+        d_q.copy_(h_q, non_blocking=True)
+        device_step()
+        h_out.copy_(d_out, non_blocking=True)
+    barrier(dist, device)
+    torch.cuda.synchronize(device)
+    w0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        d_q.copy_(h_q, non_blocking=True)
+        d_k.copy_(h_k, non_blocking=True)
+        d_v.copy_(h_v, non_blocking=True)
+        d_slots.copy_(h_slots, non_blocking=True)
+        d_tables.copy_(h_tables, non_blocking=True)
+        d_lens.copy_(h_lens, non_blocking=True)
+        if npairs:
+            d_pairs.copy_(h_pairs, non_blocking=True)
+        device_step()
+        h_out.copy_(d_out, non_blocking=True)
+        stream.synchronize()
+    e2e_s = time.perf_counter() - w0
+    barrier(dist, device)
+    e2e_s = reduce_scalar(dist, e2e_s, "max", device)
+    clocks = sampler.stop() if sampler else None
+    assert pa.pa_device_errors(clear=True) == 0, "device error flags set during the timed steps"
+    assert torch.isfinite(d_out).all().item()
+
+    kv_bytes = step.kv_bytes_logical()
+    kv_all = reduce_scalar(dist, kv_bytes, "sum", device)
+    seqs_all = reduce_scalar(dist, S, "sum", device)
+    step_s = ms_total / 1e3 / args.steps
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slots, h_tables, h_lens))
+    h2d += h_pairs.numel() * h_pairs.element_size() if npairs else 0
+    d2h = h_out.numel() * h_out.element_size()
+
+    if rank != 0:
+        return None
+    peak, peak_kind = measured_hbm_peak()
+    achieved = kv_bytes / (dec_ms / 1e3) / 1e9
+    value = kv_all / step_s / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_total / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": step.dtype,
+        "data": "synthetic (seeded; shapes and length distributions of the workload)",
+        "config": {
+            "workload": args.workload,
+            "num_seqs": S, "num_q_heads": Hq, "num_kv_heads": step.num_kv_heads, "head_dim": D,
+            "block_size": step.block_size, "partition_size": step.partition_size,
+            "num_blocks": step.num_blocks, "context_tokens": int(step.lens.sum()),
+            "max_context": int(step.lens.max()), "cow_pairs": npairs,
+            "kv_bytes_per_step": kv_bytes,
+            "l2": f"inputs larger than L2 ({kv_bytes / 2**20:.0f} MiB of KV read per step vs "
+                  f"{L2_BYTES / 2**20:.0f} MiB L2); no flush",
+            "parallelism": f"replicas x{world} (one workload per GPU, no collective on the data path)",
+        },
+        "q_tok_per_s_per_layer": round(seqs_all / step_s, 1),
+        "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "pa_decode (partition kernel + merge), events around each launch",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": profiled_traffic(args.workload),
+            "decode_ms": round(dec_ms, 5),
+        },
+        "e2e": {"value": round(kv_all * e2e_steps / e2e_s / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_s * 1e3 / e2e_steps, 5), "steps": e2e_steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = {k: v for k, v in cpu_baseline(step).items() if k != "seconds"}
+    return line
+
+
+# --------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    """Time the CPU oracle on host cores: each step one bounded sample of the workload."""
+    rank, _, world = dist_env()
+    if rank != 0:
+        return None
+    from paged_kv_cache_127_gb300 import workloads
+
+    try:
+        from paged_kv_cache_127_gb300 import binding as pa
+    except ImportError:
+        from paged_kv_cache_127_gb300 import build as pa_build
+        pa_build.build()
+        from paged_kv_cache_127_gb300 import binding as pa
+    step = workloads.build_step(args.workload, seed=0, binding=pa)
+    rng = np.random.default_rng(7)
+    order = rng.permutation(step.num_seqs)
+    # size each step so that the whole run stays within ~2 minutes
+    calib = time_oracle(step, order[:1])
+    per_seq = max(calib, 1e-4)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    k = int(max(1, min(step.num_seqs, budget / per_seq)))
+    per_tok = step.kv_bytes_per_token()
+    pos = 0
+
+    def one():
+        nonlocal pos
+        ids = np.array([order[(pos + i) % step.num_seqs] for i in range(k)])
+        pos += k
+        return time_oracle(step, ids), int(step.lens[ids].sum()) * per_tok
+
+    for _ in range(args.warmup):
+        one()
+    secs, nbytes = 0.0, 0
+    for _ in range(args.steps):
+        s, b = one()
+        secs += s
+        nbytes += b
+    value = nbytes / secs / 1e9
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; same workload as the GPU arm)",
+        "config": {"workload": args.workload, "num_seqs": step.num_seqs, "block_size": step.block_size,
+                   "sequences_per_step": k},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{k} sequence(s) per step, KV write + fp64 decode, single thread"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description="paged decode benchmark")
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", default="gqa8b_b16")
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if dist_env()[2] > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

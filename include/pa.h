@@ -1,0 +1,280 @@
+/*
+ * pa.h -- C ABI of libpa.so, a GB300 (sm_103a) paged KV cache with
+ * PagedAttention decode.
+ *
+ * The KV cache of every sequence lives in fixed-size physical blocks of B
+ * token slots, scattered over one shared pool and reached through the
+ * sequence's block table: token position pos is stored at offset pos % B of
+ * physical block table[pos / B].  ("PagedAttention: Virtual Memory for the KV
+ * Cache", section "A block table preserves token order"; "Paged Attention and
+ * vLLM", section "Block Table and Logical-to-Physical Mapping".)
+ *
+ * Conventions for every call below
+ * --------------------------------
+ *  - Device pointers are owned by the caller (for instance torch tensors),
+ *    row-major and contiguous, and must be 16-byte aligned.  The GPU entry
+ *    points allocate no device memory; the split-K scratch of pa_decode is
+ *    passed in as `workspace`.
+ *  - GPU calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL is the legacy default stream).  The returned status covers only
+ *    what the host can check (dimensions, dtypes, alignment, supported
+ *    shapes, launch errors).
+ *  - Bad indices met on the device (a block-table entry outside [0, N), a
+ *    context length outside [0, max_blocks_per_seq * B], a slot >= N * B, a
+ *    copy pair outside [0, N)) never fault: the offending item is skipped and
+ *    a sticky bit is set in a per-device error word read by pa_device_errors.
+ *  - Cache layout: k_cache and v_cache are each [N, Hkv, B, D] in kv_dtype;
+ *    one (block, kv head) row set is B * D contiguous elements.
+ *  - Supported shapes: head_dim D in {64, 128}; block_size B in {16, 32};
+ *    group G = Hq / Hkv in {1, 2, 4, 8}; kv_dtype f32, f16 or bf16.  Other
+ *    valid shapes return PA_ERR_UNSUPPORTED.
+ *  - Host allocator calls (pa_pool_*, pa_seq_*) touch no GPU and are not
+ *    thread-safe: one pool is used from one thread at a time.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID = 1,      /* bad argument: null or misaligned pointer, bad sizes */
+    PA_ERR_UNSUPPORTED = 2,  /* valid but not compiled: D, B, G or dtype combination */
+    PA_ERR_OOM = 3,          /* allocator: not enough free blocks; nothing changed */
+    PA_ERR_BAD_INDEX = 4,    /* allocator: unknown sequence id or block id */
+    PA_ERR_CUDA = 5          /* a CUDA runtime call failed (no device, launch error) */
+} pa_status;
+
+typedef enum pa_dtype { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
+
+/* Shapes shared by the GPU calls. */
+typedef struct pa_dims {
+    int32_t num_seqs;            /* S: sequences (one decode query each)             */
+    int32_t num_q_heads;         /* Hq                                               */
+    int32_t num_kv_heads;        /* Hkv; Hq % Hkv == 0, query head h reads KV head   */
+                                 /*      h / (Hq / Hkv)                              */
+    int32_t head_dim;            /* D                                                */
+    int32_t block_size;          /* B: token slots per physical block                */
+    int32_t num_blocks;          /* N: physical blocks in the pool                   */
+    int32_t max_blocks_per_seq;  /* columns of block_tables                          */
+    int32_t partition_size;      /* context tokens per split-K partition; a multiple */
+                                 /* of B, at most 256 * B; 0 selects 512             */
+    int32_t kv_dtype;            /* pa_dtype of q, k, v, k_cache and v_cache         */
+} pa_dims;
+
+/* Bits of the per-device error word (see pa_device_errors). */
+#define PA_DEVERR_BAD_BLOCK 1u   /* block-table entry outside [0, N): block skipped   */
+#define PA_DEVERR_BAD_LEN 2u     /* context length < 0 or > max_blocks_per_seq * B:  */
+                                 /* clamped into range                               */
+#define PA_DEVERR_BAD_SLOT 4u    /* pa_write_kv slot >= N * B: token skipped          */
+#define PA_DEVERR_BAD_PAIR 8u    /* pa_copy_blocks id outside [0, N): pair skipped    */
+#define PA_DEVERR_TIMEOUT 16u    /* a bounded in-kernel wait gave up; outputs of the  */
+                                 /* affected work item were not written              */
+
+/* ------------------------------------------------------------------ GPU calls */
+
+/*
+ * pa_decode_workspace_bytes -- bytes of device scratch pa_decode needs for the
+ * split-K partial results: S * Hq * P * (D + 2) floats, P = ceil(max_blocks_per_seq
+ * * B / partition_size), rounded up to 256 bytes.  Returns 0 when one partition
+ * covers every possible context (then workspace may be NULL), and 0 for
+ * invalid dims.
+ */
+PA_API size_t pa_decode_workspace_bytes(const pa_dims *dims);
+
+/*
+ * pa_decode -- PagedAttention decode: for every sequence s and query head h,
+ *
+ *     out[s, h, :] = softmax(scale * q[s, h, :] . K_s^T) . V_s
+ *
+ * where K_s, V_s are the context_lens[s] keys/values of s read through its
+ * block table, in token order, without building a contiguous copy.
+ * ("Paged Attention and vLLM", "Block Table and Logical-to-Physical Mapping",
+ * the a_t equation; section "Paged Attention CUDA Kernel" for the per-partition
+ * (m_b, l_b, v_b^acc) terms and their log-sum-exp merge, used here as split-K
+ * over context partitions of partition_size tokens.)
+ *
+ *   q             [S, Hq, D] kv_dtype, device
+ *   k_cache,
+ *   v_cache       [N, Hkv, B, D] kv_dtype, device
+ *   block_tables  int32 [S, max_blocks_per_seq], device; entries past
+ *                 ceil(context_lens[s] / B) are never read
+ *   context_lens  int32 [S], device; 0 gives an all-zero output row
+ *   scale         logit scale (1/sqrt(D) for standard attention)
+ *   out           float32 [S, Hq, D], device, written
+ *   workspace     device scratch of >= pa_decode_workspace_bytes(dims) bytes
+ *                 (may be NULL when that is 0); contents need no initialisation
+ *                 and are garbage afterwards; concurrent calls need separate
+ *                 workspaces
+ * Returns PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED or PA_ERR_CUDA.
+ */
+PA_API int32_t pa_decode(const pa_dims *dims, const void *q, const void *k_cache,
+                  const void *v_cache, const int32_t *block_tables,
+                  const int32_t *context_lens, float scale, float *out,
+                  void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * pa_write_kv -- the KV write (reshape-and-cache): store each new token's key
+ * and value rows in its slot, for every KV head:
+ *
+ *     k_cache[slot / B, h, slot % B, :] = k[t, h, :]   (and the same for v)
+ *
+ * ("PagedAttention: Virtual Memory for the KV Cache", "Sharing a prefix and
+ * copying a partial block": the engine writes the new entry into the block the
+ * table now points at.)  The copy is bit-exact.
+ *
+ *   k, v          [num_tokens, Hkv, D] kv_dtype, device
+ *   slot_mapping  int64 [num_tokens], device; slot = physical block * B +
+ *                 offset; a negative slot skips the token (padding)
+ *   k_cache,
+ *   v_cache       [N, Hkv, B, D] kv_dtype, device, updated in place
+ * Distinct tokens must have distinct slots.  Only num_kv_heads, head_dim,
+ * block_size, num_blocks and kv_dtype of dims are used.
+ */
+PA_API int32_t pa_write_kv(const pa_dims *dims, const void *k, const void *v,
+                    const int64_t *slot_mapping, int32_t num_tokens,
+                    void *k_cache, void *v_cache, void *stream);
+
+/*
+ * pa_copy_blocks -- copy-on-write block copy: for each pair (src, dst) copy
+ * the whole physical block src -> dst (all Hkv heads, all B slots, keys and
+ * values), bit-exact.  ("PagedAttention: Virtual Memory for the KV Cache",
+ * "Sharing a prefix and copying a partial block"; "Paged Attention and vLLM",
+ * "Continuous Batching and Scheduler", the copy-on-write rule.)
+ *
+ *   src_dst_pairs  int64 [num_pairs, 2], device
+ * Precondition: every dst is distinct and no dst is also a src (the allocator
+ * only emits such pairs); otherwise the result is unspecified.  Only
+ * num_kv_heads, head_dim, block_size, num_blocks and kv_dtype of dims are used.
+ */
+PA_API int32_t pa_copy_blocks(const pa_dims *dims, void *k_cache, void *v_cache,
+                       const int64_t *src_dst_pairs, int32_t num_pairs, void *stream);
+
+/*
+ * pa_device_errors -- read (and, if clear != 0, reset) the sticky PA_DEVERR_*
+ * bits of the current device.  Synchronises with the device.
+ */
+PA_API int32_t pa_device_errors(uint32_t *flags, int32_t clear);
+
+/* Library version string, e.g. "pa 0.1.0 sm_103a". */
+PA_API const char *pa_version(void);
+
+/* ------------------------------------------------------- host block allocator
+ *
+ * A pool of N physical blocks of B slots with a FIFO free list, a reference
+ * count per block, per-sequence block tables, prefix sharing by fork and
+ * copy-on-write of a partially filled shared last block.  ("PagedAttention:
+ * Virtual Memory for the KV Cache", sections "Growing a request" and "Sharing a
+ * prefix and copying a partial block"; "KV Cache Optimization and Management",
+ * "PagedAttention: borrowing virtual memory" and answer A6.)
+ */
+typedef struct pa_pool pa_pool;
+
+typedef struct pa_pool_stats {
+    int32_t num_blocks;
+    int32_t block_size;
+    int32_t free_blocks;
+    int32_t used_blocks;      /* refcount >= 1                                   */
+    int32_t shared_blocks;    /* refcount >= 2                                   */
+    int32_t live_seqs;
+    int64_t cow_copies;       /* copy-on-write pairs emitted since creation      */
+    int64_t tokens;           /* sum of live sequence lengths                    */
+    int64_t table_slots;      /* B * sum of live table lengths (per-seq view)    */
+    int64_t padded_slots;     /* table_slots - tokens                            */
+} pa_pool_stats;
+
+/*
+ * Create a pool of num_blocks blocks of block_size slots.  free_order (host,
+ * nullable) is a permutation of 0..num_blocks-1 giving the order in which free
+ * blocks are handed out; NULL means ascending ids.  Returns NULL on bad
+ * arguments.  Destroy with pa_pool_destroy.
+ */
+PA_API pa_pool *pa_pool_create(int32_t num_blocks, int32_t block_size, const int32_t *free_order);
+PA_API void pa_pool_destroy(pa_pool *pool);
+
+/* New empty sequence; returns its id (>= 0; ids are never reused) or -PA_ERR_INVALID. */
+PA_API int32_t pa_seq_create(pa_pool *pool);
+
+/*
+ * Fork: a new sequence sharing all of parent's blocks (each block's refcount
+ * + 1) and its length.  Sharing is only valid when the prefix was computed
+ * from the same model state, positions and inputs; the library does not check
+ * that.  Returns the new id or -PA_ERR_BAD_INDEX.
+ */
+PA_API int32_t pa_seq_fork(pa_pool *pool, int32_t parent);
+
+/*
+ * Append n_tokens tokens to sequence seq and return their slots.
+ *  - If the next token falls in a partially filled last block that is shared
+ *    (refcount > 1), that block is first copied: a fresh block p' is taken,
+ *    the pair (p, p') is written to cow_pairs_out[0..1], p's count drops by
+ *    one and the table now points at p'.  *n_cow is set to 1, else 0.  The
+ *    caller must run pa_copy_blocks on the pair before writing the new tokens.
+ *    A full shared block is never copied: growth takes a new private block.
+ *  - A new block is taken from the free list whenever a token starts a block.
+ *  - slots_out[i] = table[pos / B] * B + pos % B for pos = len .. len+n-1.
+ *  The call is atomic: when the blocks it needs (copy plus growth) are not all
+ *  available it returns PA_ERR_OOM and changes nothing.  Within one call the
+ *  copy block is taken before the growth blocks.
+ *  slots_out: host int64[n_tokens] (may be NULL if n_tokens == 0);
+ *  cow_pairs_out: host int64[2]; n_cow: host int32.
+ */
+PA_API int32_t pa_seq_append(pa_pool *pool, int32_t seq, int32_t n_tokens, int64_t *slots_out,
+                      int64_t *cow_pairs_out, int32_t *n_cow);
+
+/*
+ * Batched append: append tokens_each tokens to each of n distinct sequences
+ * seqs[0..n-1], in that order, with the same rules as pa_seq_append.
+ * slots_out: int64[n * tokens_each] (row i for seqs[i]); cow_pairs_out:
+ * int64[2 * n]; *n_cow receives the number of pairs written.  All-or-nothing:
+ * PA_ERR_OOM leaves the pool unchanged.  Duplicate ids give PA_ERR_INVALID.
+ */
+PA_API int32_t pa_seq_append_batch(pa_pool *pool, const int32_t *seqs, int32_t n, int32_t tokens_each,
+                            int64_t *slots_out, int64_t *cow_pairs_out, int32_t *n_cow);
+
+/* Release a sequence: each of its blocks' counts drops by one; blocks reaching
+ * zero go to the back of the free list, in table order. */
+PA_API int32_t pa_seq_free(pa_pool *pool, int32_t seq);
+
+/* Copy up to cap table entries of seq into out; returns the table length or
+ * -PA_ERR_BAD_INDEX. */
+PA_API int32_t pa_seq_table(const pa_pool *pool, int32_t seq, int32_t *out, int32_t cap);
+
+/* Length (stored tokens) of seq, or -PA_ERR_BAD_INDEX. */
+PA_API int32_t pa_seq_len(const pa_pool *pool, int32_t seq);
+
+/*
+ * Export device-ready tables for n sequences: tables_out int32[n, max_blocks]
+ * (row i = table of seqs[i], padded with `pad`) and lens_out int32[n].
+ * PA_ERR_INVALID if a table is longer than max_blocks.
+ */
+PA_API int32_t pa_pool_export(const pa_pool *pool, const int32_t *seqs, int32_t n, int32_t max_blocks,
+                       int32_t pad, int32_t *tables_out, int32_t *lens_out);
+
+PA_API int32_t pa_pool_num_free(const pa_pool *pool);
+PA_API int32_t pa_block_refcount(const pa_pool *pool, int32_t block);   /* -PA_ERR_BAD_INDEX if bad id */
+PA_API int32_t pa_pool_get_stats(const pa_pool *pool, pa_pool_stats *out);
+
+/*
+ * Fault injection for tests: let only n more block allocations succeed; any
+ * operation needing more fails with PA_ERR_OOM and changes nothing.  n < 0
+ * removes the limit.
+ */
+PA_API int32_t pa_pool_set_fail_after(pa_pool *pool, int32_t n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -1,0 +1,335 @@
+"""Thin ctypes binding over libpa.so, with the names of the C ABI (include/pa.h).
+
+Argument marshalling only: every GPU step runs in the library's CUDA kernels.
+The GPU calls take torch CUDA tensors (PyTorch supplies device memory and
+streams) and check their shapes, dtypes, devices and contiguity against the
+``pa_dims`` they are given, because the C ABI itself sees only pointers.
+Importing this module fails with ImportError when the library has not been
+built -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libpa.so")
+
+PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_OOM, PA_ERR_BAD_INDEX, PA_ERR_CUDA = range(6)
+PA_F32, PA_F16, PA_BF16 = 0, 1, 2
+DTYPE_CODES = {"f32": PA_F32, "f16": PA_F16, "bf16": PA_BF16}
+STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_OOM",
+                4: "PA_ERR_BAD_INDEX", 5: "PA_ERR_CUDA"}
+PA_DEVERR_BAD_BLOCK, PA_DEVERR_BAD_LEN, PA_DEVERR_BAD_SLOT, PA_DEVERR_BAD_PAIR, PA_DEVERR_TIMEOUT = (
+    1, 2, 4, 8, 16)
+
+
+class PaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+
+
+class pa_dims(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+                ("max_blocks_per_seq", ctypes.c_int32), ("partition_size", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32)]
+
+
+class pa_pool_stats(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("free_blocks", ctypes.c_int32), ("used_blocks", ctypes.c_int32),
+                ("shared_blocks", ctypes.c_int32), ("live_seqs", ctypes.c_int32),
+                ("cow_copies", ctypes.c_int64), ("tokens", ctypes.c_int64),
+                ("table_slots", ctypes.c_int64), ("padded_slots", ctypes.c_int64)]
+
+
+_vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+_SIGNATURES = {
+    "pa_decode_workspace_bytes": (_sz, [_vp]),
+    "pa_decode": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _sz, _vp]),
+    "pa_write_kv": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp]),
+    "pa_copy_blocks": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp]),
+    "pa_device_errors": (_i32, [_vp, _i32]),
+    "pa_version": (ctypes.c_char_p, []),
+    "pa_pool_create": (_vp, [_i32, _i32, _vp]),
+    "pa_pool_destroy": (None, [_vp]),
+    "pa_seq_create": (_i32, [_vp]),
+    "pa_seq_fork": (_i32, [_vp, _i32]),
+    "pa_seq_append": (_i32, [_vp, _i32, _i32, _vp, _vp, _vp]),
+    "pa_seq_append_batch": (_i32, [_vp, _vp, _i32, _i32, _vp, _vp, _vp]),
+    "pa_seq_free": (_i32, [_vp, _i32]),
+    "pa_seq_table": (_i32, [_vp, _i32, _vp, _i32]),
+    "pa_seq_len": (_i32, [_vp, _i32]),
+    "pa_pool_export": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp]),
+    "pa_pool_num_free": (_i32, [_vp]),
+    "pa_block_refcount": (_i32, [_vp, _i32]),
+    "pa_pool_get_stats": (_i32, [_vp, _vp]),
+    "pa_pool_set_fail_after": (_i32, [_vp, _i32]),
+}
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built; run `python -m paged_kv_cache_127_gb300.build` "
+                          "(or __graft_entry__.build()) first -- there is no non-CUDA fallback")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+def _check(status: int, what: str) -> None:
+    if status != PA_OK:
+        raise PaError(status, what)
+
+
+def _np_ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def make_dims(num_seqs=0, num_q_heads=1, num_kv_heads=1, head_dim=128, block_size=16, num_blocks=1,
+              max_blocks_per_seq=1, partition_size=0, kv_dtype="bf16") -> pa_dims:
+    code = DTYPE_CODES[kv_dtype] if isinstance(kv_dtype, str) else int(kv_dtype)
+    return pa_dims(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                   max_blocks_per_seq, partition_size, code)
+
+
+# ------------------------------------------------------------------ GPU calls
+def _torch():
+    import torch
+    return torch
+
+
+def _torch_dtype(code: int):
+    t = _torch()
+    return {PA_F32: t.float32, PA_F16: t.float16, PA_BF16: t.bfloat16}[code]
+
+
+def _expect(t, name, shape, dtype, device):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream_ptr(stream, device):
+    t = _torch()
+    s = t.cuda.current_stream(device) if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def pa_decode_workspace_bytes(dims: pa_dims) -> int:
+    return int(lib.pa_decode_workspace_bytes(ctypes.byref(dims)))
+
+
+def pa_decode(dims: pa_dims, q, k_cache, v_cache, block_tables, context_lens, scale: float, out,
+              workspace=None, stream=None) -> None:
+    """out[s, h] = softmax(scale * q[s, h] . K_s^T) . V_s over each sequence's paged context."""
+    t = _torch()
+    d, kv = dims, _torch_dtype(dims.kv_dtype)
+    dev = q.device
+    _expect(q, "q", (d.num_seqs, d.num_q_heads, d.head_dim), kv, dev)
+    cache_shape = (d.num_blocks, d.num_kv_heads, d.block_size, d.head_dim)
+    _expect(k_cache, "k_cache", cache_shape, kv, dev)
+    _expect(v_cache, "v_cache", cache_shape, kv, dev)
+    _expect(block_tables, "block_tables", (d.num_seqs, d.max_blocks_per_seq), t.int32, dev)
+    _expect(context_lens, "context_lens", (d.num_seqs,), t.int32, dev)
+    _expect(out, "out", (d.num_seqs, d.num_q_heads, d.head_dim), t.float32, dev)
+    need = pa_decode_workspace_bytes(dims)
+    ws_ptr, ws_bytes = None, 0
+    if need:
+        if workspace is None:
+            raise ValueError(f"pa_decode needs a workspace of {need} bytes")
+        if not workspace.is_cuda or not workspace.is_contiguous() or workspace.device != dev:
+            raise ValueError("workspace must be a contiguous CUDA tensor on the same device")
+        ws_bytes = workspace.numel() * workspace.element_size()
+        ws_ptr = ctypes.c_void_p(workspace.data_ptr())
+    st = lib.pa_decode(ctypes.byref(dims), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                       block_tables.data_ptr(), context_lens.data_ptr(), float(scale), out.data_ptr(),
+                       ws_ptr, ws_bytes, _stream_ptr(stream, dev))
+    _check(st, "pa_decode")
+
+
+def pa_write_kv(dims: pa_dims, k, v, slot_mapping, k_cache, v_cache, stream=None) -> None:
+    """k_cache[slot // B, h, slot % B] = k[t, h] (and v) for every slot >= 0."""
+    t = _torch()
+    d, kv = dims, _torch_dtype(dims.kv_dtype)
+    dev = k.device
+    T = int(slot_mapping.shape[0])
+    _expect(k, "k", (T, d.num_kv_heads, d.head_dim), kv, dev)
+    _expect(v, "v", (T, d.num_kv_heads, d.head_dim), kv, dev)
+    _expect(slot_mapping, "slot_mapping", (T,), t.int64, dev)
+    cache_shape = (d.num_blocks, d.num_kv_heads, d.block_size, d.head_dim)
+    _expect(k_cache, "k_cache", cache_shape, kv, dev)
+    _expect(v_cache, "v_cache", cache_shape, kv, dev)
+    st = lib.pa_write_kv(ctypes.byref(dims), k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), T,
+                         k_cache.data_ptr(), v_cache.data_ptr(), _stream_ptr(stream, dev))
+    _check(st, "pa_write_kv")
+
+
+def pa_copy_blocks(dims: pa_dims, k_cache, v_cache, src_dst_pairs, stream=None) -> None:
+    """Copy whole blocks src -> dst in both caches for each row of src_dst_pairs [P, 2]."""
+    t = _torch()
+    d, kv = dims, _torch_dtype(dims.kv_dtype)
+    dev = k_cache.device
+    P = int(src_dst_pairs.shape[0])
+    cache_shape = (d.num_blocks, d.num_kv_heads, d.block_size, d.head_dim)
+    _expect(k_cache, "k_cache", cache_shape, kv, dev)
+    _expect(v_cache, "v_cache", cache_shape, kv, dev)
+    _expect(src_dst_pairs, "src_dst_pairs", (P, 2), t.int64, dev)
+    st = lib.pa_copy_blocks(ctypes.byref(dims), k_cache.data_ptr(), v_cache.data_ptr(),
+                            src_dst_pairs.data_ptr(), P, _stream_ptr(stream, dev))
+    _check(st, "pa_copy_blocks")
+
+
+def pa_device_errors(clear: bool = True) -> int:
+    flags = ctypes.c_uint32(0)
+    _check(lib.pa_device_errors(ctypes.byref(flags), 1 if clear else 0), "pa_device_errors")
+    return int(flags.value)
+
+
+def pa_version() -> str:
+    return lib.pa_version().decode()
+
+
+# ------------------------------------------------------------------ host allocator
+def pa_pool_create(num_blocks: int, block_size: int, free_order=None) -> int:
+    order = None
+    if free_order is not None:
+        order = np.ascontiguousarray(free_order, dtype=np.int32)
+        if order.shape != (num_blocks,):
+            raise ValueError("free_order must hold num_blocks ids")
+    h = lib.pa_pool_create(num_blocks, block_size, None if order is None else _np_ptr(order))
+    if not h:
+        raise PaError(PA_ERR_INVALID, "pa_pool_create")
+    return h
+
+
+def pa_pool_destroy(pool) -> None:
+    lib.pa_pool_destroy(pool)
+
+
+def pa_seq_create(pool) -> int:
+    r = lib.pa_seq_create(pool)
+    if r < 0:
+        raise PaError(-r, "pa_seq_create")
+    return r
+
+
+def pa_seq_fork(pool, parent: int) -> int:
+    r = lib.pa_seq_fork(pool, parent)
+    if r < 0:
+        raise PaError(-r, "pa_seq_fork")
+    return r
+
+
+def pa_seq_append(pool, seq: int, n_tokens: int):
+    """Returns (slots int64[n_tokens], cow_pairs int64[k, 2]) with k in {0, 1}."""
+    slots = np.empty(max(n_tokens, 1), dtype=np.int64)
+    pair = np.empty(2, dtype=np.int64)
+    ncow = ctypes.c_int32(0)
+    _check(lib.pa_seq_append(pool, seq, n_tokens, _np_ptr(slots), _np_ptr(pair), ctypes.byref(ncow)),
+           "pa_seq_append")
+    return slots[:n_tokens], pair.reshape(1, 2)[:ncow.value]
+
+
+def pa_seq_append_batch(pool, seqs, tokens_each: int):
+    """Returns (slots int64[n, tokens_each], cow_pairs int64[k, 2])."""
+    seqs = np.ascontiguousarray(seqs, dtype=np.int32)
+    n = seqs.shape[0]
+    slots = np.empty((max(n, 1), max(tokens_each, 1)), dtype=np.int64)
+    pairs = np.empty((max(n, 1), 2), dtype=np.int64)
+    ncow = ctypes.c_int32(0)
+    _check(lib.pa_seq_append_batch(pool, _np_ptr(seqs), n, tokens_each, _np_ptr(slots), _np_ptr(pairs),
+                                   ctypes.byref(ncow)), "pa_seq_append_batch")
+    return slots[:n, :tokens_each].copy(), pairs[:ncow.value].copy()
+
+
+def pa_seq_free(pool, seq: int) -> None:
+    _check(lib.pa_seq_free(pool, seq), "pa_seq_free")
+
+
+def pa_seq_table(pool, seq: int) -> np.ndarray:
+    n = lib.pa_seq_table(pool, seq, None, 0)
+    if n < 0:
+        raise PaError(-n, "pa_seq_table")
+    out = np.empty(max(n, 1), dtype=np.int32)
+    lib.pa_seq_table(pool, seq, _np_ptr(out), n)
+    return out[:n]
+
+
+def pa_seq_len(pool, seq: int) -> int:
+    r = lib.pa_seq_len(pool, seq)
+    if r < 0:
+        raise PaError(-r, "pa_seq_len")
+    return r
+
+
+def pa_pool_export(pool, seqs, max_blocks: int, pad: int = -1):
+    """Returns (tables int32[n, max_blocks], lens int32[n]) for the given sequences."""
+    seqs = np.ascontiguousarray(seqs, dtype=np.int32)
+    n = seqs.shape[0]
+    tables = np.empty((max(n, 1), max_blocks), dtype=np.int32)
+    lens = np.empty(max(n, 1), dtype=np.int32)
+    _check(lib.pa_pool_export(pool, _np_ptr(seqs), n, max_blocks, pad, _np_ptr(tables), _np_ptr(lens)),
+           "pa_pool_export")
+    return tables[:n].copy(), lens[:n].copy()
+
+
+def pa_pool_num_free(pool) -> int:
+    return int(lib.pa_pool_num_free(pool))
+
+
+def pa_block_refcount(pool, block: int) -> int:
+    r = lib.pa_block_refcount(pool, block)
+    if r < 0:
+        raise PaError(-r, "pa_block_refcount")
+    return r
+
+
+def pa_pool_get_stats(pool) -> dict:
+    st = pa_pool_stats()
+    _check(lib.pa_pool_get_stats(pool, ctypes.byref(st)), "pa_pool_get_stats")
+    return {name: getattr(st, name) for name, _ in pa_pool_stats._fields_}
+
+
+def pa_pool_set_fail_after(pool, n) -> None:
+    _check(lib.pa_pool_set_fail_after(pool, -1 if n is None else int(n)), "pa_pool_set_fail_after")
+
+
+class Pool:
+    """Owning wrapper: ``with Pool(n, B) as p: ...`` destroys the pool on exit."""
+
+    def __init__(self, num_blocks: int, block_size: int, free_order=None):
+        self.handle = pa_pool_create(num_blocks, block_size, free_order)
+        self.block_size = block_size
+        self.num_blocks = num_blocks
+
+    def close(self):
+        if self.handle:
+            pa_pool_destroy(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        self.close()

@@ -1,0 +1,142 @@
+// pa_cache_ops.cu -- the two companion kernels of paged decode, plus the
+// cross-partition merge of the split-K decode.
+//
+//  - write_kv (reshape-and-cache): each new token's K and V rows go to its slot,
+//    k_cache[slot / B, h, slot % B, :] = k[t, h, :].  ("PagedAttention: Virtual
+//    Memory for the KV Cache", "Sharing a prefix and copying a partial block":
+//    the engine writes the new entry into the block its table points at.)
+//  - copy_blocks: copy-on-write copy of whole physical blocks, src -> dst, in
+//    both caches (same section; "Paged Attention and vLLM", "Continuous
+//    Batching and Scheduler", the copy-on-write rule).
+//  - merge: o = sum_b 2^(m_b - m*) acc_b / sum_b 2^(m_b - m*) l_b with
+//    m* = max_b m_b, over the partitions of one (sequence, query head)
+//    ("Paged Attention and vLLM", "Paged Attention CUDA Kernel", merge
+//    equation; m is kept in log2 units, so the weights are powers of two).
+//
+// The copies move 16-byte vectors; every row is a multiple of 16 bytes.
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+__global__ void write_kv_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+                                const int64_t *__restrict__ slots, int Hkv, int row_chunks, int B,
+                                int N, uint4 *__restrict__ kc, uint4 *__restrict__ vc,
+                                unsigned int *err) {
+    const int t = blockIdx.x;
+    const int64_t slot = slots[t];
+    if (slot < 0) return;
+    if (slot >= (int64_t)N * B) {
+        if (threadIdx.x == 0) set_error(err, PA_DEVERR_BAD_SLOT);
+        return;
+    }
+    const int64_t blk = slot / B;
+    const int64_t off = slot % B;
+    const int per_cache = Hkv * row_chunks;
+    for (int c = threadIdx.x; c < 2 * per_cache; c += blockDim.x) {
+        const bool is_v = c >= per_cache;
+        const int cc = is_v ? c - per_cache : c;
+        const int h = cc / row_chunks;
+        const int w = cc - h * row_chunks;
+        const size_t src = ((size_t)t * Hkv + h) * row_chunks + w;
+        const size_t dst = (((size_t)blk * Hkv + h) * B + off) * row_chunks + w;
+        if (is_v)
+            vc[dst] = v[src];
+        else
+            kc[dst] = k[src];
+    }
+}
+
+__global__ void copy_blocks_kernel(uint4 *kc, uint4 *vc, const int64_t *__restrict__ pairs,
+                                   int64_t chunks, int N, unsigned int *err) {
+    const int p = blockIdx.x;
+    const int64_t src = pairs[2 * p];
+    const int64_t dst = pairs[2 * p + 1];
+    if (src < 0 || src >= N || dst < 0 || dst >= N) {
+        if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) set_error(err, PA_DEVERR_BAD_PAIR);
+        return;
+    }
+    uint4 *base = blockIdx.y ? vc : kc;
+    const uint4 *from = base + src * chunks;
+    uint4 *to = base + dst * chunks;
+    for (int64_t i = threadIdx.x + (int64_t)blockIdx.z * blockDim.x; i < chunks;
+         i += (int64_t)blockDim.x * gridDim.z)
+        to[i] = from[i];
+}
+
+// One warp per (sequence, query head); lane i owns D/32 consecutive outputs.
+template <int D>
+__global__ void decode_merge_kernel(const DecodeArgs a) {
+    constexpr int kPer = D / 32;
+    const int gw = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    if (gw >= a.S * a.Hq) return;
+    const int s = gw / a.Hq;
+    int len = a.context_lens[s];
+    const int cap = a.max_blocks * a.B;
+    len = len < 0 ? 0 : (len > cap ? cap : len);
+    const int np = (len + a.partition_size - 1) / a.partition_size;
+    if (np <= 1) return;  // finished in place by the partition kernel
+    const size_t r0 = (size_t)gw * a.max_parts;
+    const float *ml = a.ws_ml + 2 * r0;
+    const float *acc = a.ws_acc + r0 * D;
+    float M = -INFINITY;
+    for (int p = lane; p < np; p += 32) M = fmaxf(M, ml[2 * p]);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float L = 0.f;
+    float o[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) o[i] = 0.f;
+    if (M != -INFINITY) {
+        for (int p = 0; p < np; ++p) {
+            const float w = ex2(ml[2 * p] - M);
+            L += w * ml[2 * p + 1];
+            const float *x = acc + (size_t)p * D + lane * kPer;
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) o[i] += w * x[i];
+        }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    float *dst = a.out + (size_t)gw * D + lane * kPer;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) dst[i] = o[i] * inv;
+}
+
+cudaError_t launch_decode_merge(const DecodeArgs &a, cudaStream_t st) {
+    const int warps = a.S * a.Hq;
+    const int per_block = 8;
+    const dim3 grid((unsigned)((warps + per_block - 1) / per_block));
+    if (a.D == 64)
+        decode_merge_kernel<64><<<grid, per_block * 32, 0, st>>>(a);
+    else if (a.D == 128)
+        decode_merge_kernel<128><<<grid, per_block * 32, 0, st>>>(a);
+    else
+        return cudaErrorNotSupported;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_write_kv(const void *k, const void *v, const int64_t *slots, int T, int Hkv,
+                            int row_bytes, int B, int N, void *k_cache, void *v_cache,
+                            unsigned int *err, cudaStream_t st) {
+    if (T == 0) return cudaSuccess;
+    write_kv_kernel<<<T, 128, 0, st>>>(static_cast<const uint4 *>(k), static_cast<const uint4 *>(v),
+                                       slots, Hkv, row_bytes / 16, B, N, static_cast<uint4 *>(k_cache),
+                                       static_cast<uint4 *>(v_cache), err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, int P,
+                               int64_t block_bytes, int N, unsigned int *err, cudaStream_t st) {
+    if (P == 0) return cudaSuccess;
+    const int64_t chunks = block_bytes / 16;
+    const int threads = 256;
+    int z = (int)((chunks + threads * 8 - 1) / (threads * 8));  // ~8 vectors per thread
+    if (z < 1) z = 1;
+    if (z > 64) z = 64;
+    copy_blocks_kernel<<<dim3((unsigned)P, 2, (unsigned)z), threads, 0, st>>>(
+        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), pairs, chunks, N, err);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,44 @@
+// pa_internal.h -- host-side interface between the C-ABI entry points
+// (pa_api.cu) and the per-dtype kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace pa {
+
+// Everything a decode launch needs, already validated by the entry point.
+struct DecodeArgs {
+    const void *q;
+    const void *k_cache;
+    const void *v_cache;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    float *out;
+    float *ws_ml;    // [S, Hq, P, 2]  (m in log2 units, l)
+    float *ws_acc;   // [S, Hq, P, D]
+    unsigned int *err;
+    int S, Hq, Hkv, D, B, N, max_blocks, partition_size, max_parts;
+    float scale;
+};
+
+// Tokens per partition upper bound (table slice staged in shared memory).
+constexpr int kMaxPartitionBlocks = 256;
+
+// Per-dtype launchers; return cudaSuccess, cudaErrorNotSupported for a shape
+// that is not compiled, or the launch error.
+cudaError_t launch_decode_f32(const DecodeArgs &a, cudaStream_t st);
+cudaError_t launch_decode_f16(const DecodeArgs &a, cudaStream_t st);
+cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t st);
+
+// Cross-partition merge (dtype independent).
+cudaError_t launch_decode_merge(const DecodeArgs &a, cudaStream_t st);
+
+cudaError_t launch_write_kv(const void *k, const void *v, const int64_t *slots, int T, int Hkv,
+                            int row_bytes, int B, int N, void *k_cache, void *v_cache,
+                            unsigned int *err, cudaStream_t st);
+
+cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, int P,
+                               int64_t block_bytes, int N, unsigned int *err, cudaStream_t st);
+
+}  // namespace pa

@@ -1,0 +1,109 @@
+"""The C-ABI library loads on a CPU-only host and exports what include/pa.h declares.
+
+No call here reaches the GPU: only symbol lookup, the version string, the
+workspace-size arithmetic and host-side argument validation.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from paged_kv_cache_127_gb300 import build as pa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pa.h")
+
+
+@pytest.fixture(scope="module")
+def pa():
+    pa_build.build()
+    from paged_kv_cache_127_gb300 import binding
+    return binding
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^PA_API [^;]*?\b(pa_\w+)\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for must in ("pa_decode", "pa_write_kv", "pa_copy_blocks", "pa_decode_workspace_bytes",
+                 "pa_pool_create", "pa_seq_append", "pa_seq_fork", "pa_seq_free"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(pa):
+    out = subprocess.run(["nm", "-D", "--defined-only", pa.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT (pa_\w+)$", out, flags=re.M))
+    declared = set(_declared())
+    assert declared <= exported, f"missing: {sorted(declared - exported)}"
+    assert exported <= declared, f"exported but undeclared: {sorted(exported - declared)}"
+    for name in declared:
+        assert getattr(pa.lib, name)
+
+
+def test_binding_covers_every_symbol(pa):
+    for name in _declared():
+        assert name in pa._SIGNATURES
+        assert hasattr(pa, name)
+
+
+def test_version(pa):
+    assert "sm_103a" in pa.pa_version()
+
+
+def test_workspace_bytes(pa):
+    d = pa.make_dims(num_seqs=256, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+                     num_blocks=1000, max_blocks_per_seq=256, partition_size=512, kv_dtype="bf16")
+    parts = (256 * 16 + 511) // 512
+    expect = 256 * 32 * parts * (128 + 2) * 4
+    assert pa.pa_decode_workspace_bytes(d) == (expect + 255) // 256 * 256
+    d.max_blocks_per_seq = 32            # one partition covers every context
+    assert pa.pa_decode_workspace_bytes(d) == 0
+    d.num_q_heads = 30                   # Hq not a multiple of Hkv: invalid -> 0
+    assert pa.pa_decode_workspace_bytes(d) == 0
+
+
+def _decode_status(pa, **over):
+    kw = dict(num_seqs=2, num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16, num_blocks=8,
+              max_blocks_per_seq=4, partition_size=0, kv_dtype="bf16")
+    kw.update(over)
+    d = pa.make_dims(**kw)
+    fake = ctypes.c_void_p(0x10000)      # never dereferenced: validation fails first
+    return pa.lib.pa_decode(ctypes.byref(d), fake, fake, fake, fake, fake, 1.0, fake, None, 0, None)
+
+
+def test_decode_rejects_bad_arguments_on_the_host(pa):
+    assert _decode_status(pa, num_q_heads=7) == pa.PA_ERR_INVALID
+    assert _decode_status(pa, head_dim=96) == pa.PA_ERR_UNSUPPORTED
+    assert _decode_status(pa, block_size=8) == pa.PA_ERR_UNSUPPORTED
+    assert _decode_status(pa, num_q_heads=32, num_kv_heads=2) == pa.PA_ERR_UNSUPPORTED   # G = 16
+    assert _decode_status(pa, partition_size=24) == pa.PA_ERR_INVALID                   # not a multiple of B
+    assert _decode_status(pa, kv_dtype=7) == pa.PA_ERR_INVALID
+    assert _decode_status(pa, num_blocks=0) == pa.PA_ERR_INVALID
+    # needs a workspace (2 partitions of 32 tokens) but none is given
+    assert _decode_status(pa, partition_size=32) == pa.PA_ERR_INVALID
+    d = pa.make_dims(num_seqs=1, num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
+                     num_blocks=8, max_blocks_per_seq=4)
+    assert pa.lib.pa_decode(ctypes.byref(d), None, None, None, None, None, 1.0, None, None, 0,
+                            None) == pa.PA_ERR_INVALID
+    odd = ctypes.c_void_p(0x10004)       # not 16-byte aligned
+    ok = ctypes.c_void_p(0x10000)
+    assert pa.lib.pa_decode(ctypes.byref(d), odd, ok, ok, ok, ok, 1.0, ok, None, 0,
+                            None) == pa.PA_ERR_INVALID
+
+
+def test_write_and_copy_reject_bad_arguments_on_the_host(pa):
+    d = pa.make_dims(num_kv_heads=2, head_dim=128, block_size=16, num_blocks=8, kv_dtype="f16")
+    ok = ctypes.c_void_p(0x10000)
+    assert pa.lib.pa_write_kv(ctypes.byref(d), ok, ok, ok, -1, ok, ok, None) == pa.PA_ERR_INVALID
+    assert pa.lib.pa_write_kv(ctypes.byref(d), ok, ok, ok, 0, ok, ok, None) == pa.PA_OK   # no-op
+    assert pa.lib.pa_write_kv(ctypes.byref(d), None, ok, ok, 3, ok, ok, None) == pa.PA_ERR_INVALID
+    assert pa.lib.pa_copy_blocks(ctypes.byref(d), ok, ok, ok, -2, None) == pa.PA_ERR_INVALID
+    assert pa.lib.pa_copy_blocks(ctypes.byref(d), ok, ok, ok, 0, None) == pa.PA_OK        # no-op
+    bad = pa.make_dims(num_kv_heads=2, head_dim=4, block_size=16, num_blocks=8, kv_dtype="f16")
+    assert pa.lib.pa_copy_blocks(ctypes.byref(bad), ok, ok, ok, 1, None) == pa.PA_ERR_UNSUPPORTED

@@ -1,0 +1,75 @@
+"""Host-side pieces of bench.py: the multi-rank timing reduction over gloo
+(world size 2, CPU only) and the CPU-oracle reference arm on the tiny workload."""
+import io
+import json
+import os
+import socket
+import sys
+from contextlib import redirect_stdout
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      LOCAL_RANK=str(rank), WORLD_SIZE=str(world))
+    sys.path.insert(0, ROOT)
+    import bench
+    r, lr, w = bench.dist_env()
+    dist = bench.dist_init(w, "gloo")
+    bench.barrier(dist)
+    # each rank times its own replica; the job is as slow as its slowest rank and
+    # its throughput counts every rank's bytes
+    mx = bench.reduce_scalar(dist, 10.0 + rank, "max")
+    sm = bench.reduce_scalar(dist, 100 * (rank + 1), "sum")
+    bench.barrier(dist)
+    dist.destroy_process_group()
+    q.put((r, lr, w, mx, sm))
+
+
+def test_two_rank_timing_reduction_over_gloo():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    assert got == [(0, 0, 2, 11.0, 300.0), (1, 1, 2, 11.0, 300.0)]
+
+
+def test_single_process_helpers_are_identity(monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    for k in ("RANK", "LOCAL_RANK", "WORLD_SIZE"):
+        monkeypatch.delenv(k, raising=False)
+    assert bench.dist_env() == (0, 0, 1)
+    assert bench.dist_init(1, "gloo") is None
+    assert bench.reduce_scalar(None, 3.5, "max") == 3.5
+
+
+def test_reference_arm_runs_the_oracle_on_cpu(monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    for k in ("RANK", "LOCAL_RANK", "WORLD_SIZE"):
+        monkeypatch.delenv(k, raising=False)
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "3", "--warmup", "3"])
+    line = json.loads(buf.getvalue().strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["metric"] == bench.METRIC
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
