@@ -53,7 +53,9 @@ typedef enum pa_status {
     PA_ERR_UNSUPPORTED = 2,  /* valid but not compiled: D, B, G or dtype combination */
     PA_ERR_OOM = 3,          /* allocator: not enough free blocks; nothing changed */
     PA_ERR_BAD_INDEX = 4,    /* allocator: unknown sequence id or block id */
-    PA_ERR_CUDA = 5          /* a CUDA runtime call failed (no device, launch error) */
+    PA_ERR_CUDA = 5,         /* a CUDA runtime call failed (no device, launch error) */
+    PA_ERR_TOO_LARGE = 6     /* pa_decode_noalloc: the problem needs more scratch than */
+                             /* the library's fixed buffer holds                      */
 } pa_status;
 
 typedef enum pa_dtype { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
@@ -123,6 +125,35 @@ PA_API int32_t pa_decode(const pa_dims *dims, const void *q, const void *k_cache
                   const void *v_cache, const int32_t *block_tables,
                   const int32_t *context_lens, float scale, float *out,
                   void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * pa_decode_noalloc -- pa_decode for callers that cannot allocate device
+ * memory.  The pages have no counterpart to this call.
+ *
+ * Some callers cannot provide the split-K workspace: code running inside a
+ * memory pool or arena that forbids further device allocations, plugin hosts
+ * that own every allocation, or code paths where a cudaMalloc would
+ * synchronise the device at a bad moment.  This call computes exactly what
+ * pa_decode computes, with the same arguments except the workspace: its
+ * scratch is a fixed buffer of PA_NOALLOC_SCRATCH_BYTES bytes built into the
+ * library, held on every GPU that loads the library until the process exits.
+ * It allocates nothing.
+ *
+ *  - The first call on each device looks up that buffer's device address
+ *    (cudaGetSymbolAddress, with the device current) and caches it; make that
+ *    first call before any stream capture on the device.
+ *  - Returns PA_ERR_TOO_LARGE, doing nothing, when pa_decode_workspace_bytes
+ *    (dims) exceeds PA_NOALLOC_SCRATCH_BYTES; use pa_decode with a workspace
+ *    then.  Other statuses as for pa_decode.
+ *  - All calls share the one buffer.  Calls whose GPU work overlaps (different
+ *    streams, or different host threads, without ordering between them) race
+ *    on it and give wrong results; order them on one stream.  Nothing carries
+ *    over between calls: each call initialises what it reads.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (64u << 20) /* 64 MiB */
+PA_API int32_t pa_decode_noalloc(const pa_dims *dims, const void *q, const void *k_cache,
+                                 const void *v_cache, const int32_t *block_tables,
+                                 const int32_t *context_lens, float scale, float *out, void *stream);
 
 /*
  * pa_write_kv -- the KV write (reshape-and-cache): store each new token's key

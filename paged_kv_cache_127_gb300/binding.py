@@ -16,11 +16,12 @@ import numpy as np
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libpa.so")
 
-PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_OOM, PA_ERR_BAD_INDEX, PA_ERR_CUDA = range(6)
+PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_OOM, PA_ERR_BAD_INDEX, PA_ERR_CUDA, PA_ERR_TOO_LARGE = range(7)
+PA_NOALLOC_SCRATCH_BYTES = 64 << 20
 PA_F32, PA_F16, PA_BF16 = 0, 1, 2
 DTYPE_CODES = {"f32": PA_F32, "f16": PA_F16, "bf16": PA_BF16}
 STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_OOM",
-                4: "PA_ERR_BAD_INDEX", 5: "PA_ERR_CUDA"}
+                4: "PA_ERR_BAD_INDEX", 5: "PA_ERR_CUDA", 6: "PA_ERR_TOO_LARGE"}
 PA_DEVERR_BAD_BLOCK, PA_DEVERR_BAD_LEN, PA_DEVERR_BAD_SLOT, PA_DEVERR_BAD_PAIR, PA_DEVERR_TIMEOUT = (
     1, 2, 4, 8, 16)
 
@@ -51,6 +52,7 @@ _vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c
 _SIGNATURES = {
     "pa_decode_workspace_bytes": (_sz, [_vp]),
     "pa_decode": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _sz, _vp]),
+    "pa_decode_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
     "pa_write_kv": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp]),
     "pa_copy_blocks": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp]),
     "pa_device_errors": (_i32, [_vp, _i32]),
@@ -163,6 +165,32 @@ def pa_decode(dims: pa_dims, q, k_cache, v_cache, block_tables, context_lens, sc
                        block_tables.data_ptr(), context_lens.data_ptr(), float(scale), out.data_ptr(),
                        ws_ptr, ws_bytes, _stream_ptr(stream, dev))
     _check(st, "pa_decode")
+
+
+def pa_decode_noalloc(dims: pa_dims, q, k_cache, v_cache, block_tables, context_lens, scale: float, out,
+                      stream=None) -> None:
+    """pa_decode without a caller workspace, for callers that cannot allocate device memory.
+
+    The scratch is a fixed PA_NOALLOC_SCRATCH_BYTES buffer inside the library,
+    shared by every call: calls whose GPU work overlaps race on it, so keep them
+    on one stream.  The first call on a device looks the buffer up; make it
+    before any stream capture.  Raises PaError(PA_ERR_TOO_LARGE) when the
+    problem needs more scratch than that buffer holds.
+    """
+    t = _torch()
+    d, kv = dims, _torch_dtype(dims.kv_dtype)
+    dev = q.device
+    _expect(q, "q", (d.num_seqs, d.num_q_heads, d.head_dim), kv, dev)
+    cache_shape = (d.num_blocks, d.num_kv_heads, d.block_size, d.head_dim)
+    _expect(k_cache, "k_cache", cache_shape, kv, dev)
+    _expect(v_cache, "v_cache", cache_shape, kv, dev)
+    _expect(block_tables, "block_tables", (d.num_seqs, d.max_blocks_per_seq), t.int32, dev)
+    _expect(context_lens, "context_lens", (d.num_seqs,), t.int32, dev)
+    _expect(out, "out", (d.num_seqs, d.num_q_heads, d.head_dim), t.float32, dev)
+    st = lib.pa_decode_noalloc(ctypes.byref(dims), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                               block_tables.data_ptr(), context_lens.data_ptr(), float(scale), out.data_ptr(),
+                               _stream_ptr(stream, dev))
+    _check(st, "pa_decode_noalloc")
 
 
 def pa_write_kv(dims: pa_dims, k, v, slot_mapping, k_cache, v_cache, stream=None) -> None:
