@@ -87,11 +87,11 @@ typedef struct pa_dims {
 /* ------------------------------------------------------------------ GPU calls */
 
 /*
- * pa_decode_workspace_bytes -- bytes of device scratch pa_decode needs for the
- * split-K partial results: S * Hq * P * (D + 2) floats, P = ceil(max_blocks_per_seq
- * * B / partition_size), rounded up to 256 bytes.  Returns 0 when one partition
- * covers every possible context (then workspace may be NULL), and 0 for
- * invalid dims.
+ * pa_decode_workspace_bytes -- bytes of device scratch pa_decode needs: a
+ * work list and counters (S * Hkv + S * P * 2 ints), plus, when one sequence
+ * can span several partitions (P > 1), the split-K partials: S * Hq * P *
+ * (D + 2) floats; P = ceil(max_blocks_per_seq * B / partition_size).  Each part
+ * is rounded up to 256 bytes.  Returns 0 for S == 0 and for invalid dims.
  */
 PA_API size_t pa_decode_workspace_bytes(const pa_dims *dims);
 
@@ -115,10 +115,10 @@ PA_API size_t pa_decode_workspace_bytes(const pa_dims *dims);
  *   context_lens  int32 [S], device; 0 gives an all-zero output row
  *   scale         logit scale (1/sqrt(D) for standard attention)
  *   out           float32 [S, Hq, D], device, written
- *   workspace     device scratch of >= pa_decode_workspace_bytes(dims) bytes
- *                 (may be NULL when that is 0); contents need no initialisation
- *                 and are garbage afterwards; concurrent calls need separate
- *                 workspaces
+ *   workspace     device scratch of >= pa_decode_workspace_bytes(dims) bytes,
+ *                 256-byte aligned; its contents need no initialisation (the
+ *                 call resets what it uses) and are garbage afterwards;
+ *                 concurrent calls need separate workspaces
  * Returns PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED or PA_ERR_CUDA.
  */
 PA_API int32_t pa_decode(const pa_dims *dims, const void *q, const void *k_cache,

@@ -64,6 +64,8 @@ int32_t check_decode_dims(const pa_dims *d, int32_t *max_parts) {
         return PA_ERR_UNSUPPORTED;
     const int64_t cap = (int64_t)d->max_blocks_per_seq * d->block_size;
     if (cap > INT32_MAX) return PA_ERR_INVALID;
+    // cache rows (N * Hkv * B) are addressed with 32-bit coordinates
+    if ((int64_t)d->num_blocks * d->num_kv_heads * d->block_size > INT32_MAX) return PA_ERR_INVALID;
     const int64_t parts = (cap + pt - 1) / pt;
     if (parts > 65535) return PA_ERR_INVALID;
     if ((int64_t)d->num_seqs * d->num_kv_heads > INT32_MAX) return PA_ERR_INVALID;
@@ -71,11 +73,69 @@ int32_t check_decode_dims(const pa_dims *d, int32_t *max_parts) {
     return PA_OK;
 }
 
+// Workspace layout, each part 256-byte aligned:
+//   header    2 ints: work items, claim counter
+//   counters  int [S, Hkv]: partitions finished per (sequence, KV head)
+//   list      int2 [S * P]: (sequence, partition) work items, largest first
+//   acc       float [S, Hq, P, D]: split-K partial sums          (only if P > 1)
+//   ml        float [S, Hq, P, 2]: partial (max in log2 units, sum) (only if P > 1)
+struct WsLayout {
+    size_t cnt, list, acc, ml, total;
+};
+
+WsLayout workspace_layout(const pa_dims *d, int32_t max_parts) {
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    const size_t S = (size_t)d->num_seqs;
+    WsLayout L{};
+    size_t off = 256;
+    L.cnt = off;
+    off += up(S * d->num_kv_heads * sizeof(int));
+    L.list = off;
+    off += up(S * max_parts * 2 * sizeof(int));
+    L.acc = off;
+    off += max_parts > 1 ? up(S * d->num_q_heads * max_parts * d->head_dim * sizeof(float)) : 0;
+    L.ml = off;
+    off += max_parts > 1 ? up(S * d->num_q_heads * max_parts * 2 * sizeof(float)) : 0;
+    L.total = off;
+    return L;
+}
+
 size_t workspace_bytes_for(const pa_dims *d, int32_t max_parts) {
-    if (max_parts <= 1) return 0;
-    const size_t rows = (size_t)d->num_seqs * d->num_q_heads * max_parts;
-    const size_t bytes = rows * (size_t)(d->head_dim + 2) * sizeof(float);
-    return (bytes + 255) & ~(size_t)255;
+    return d->num_seqs > 0 ? workspace_layout(d, max_parts).total : 0;
+}
+
+// Tensor maps of the two caches, re-encoded only when the cache or its shape
+// changes (per host thread).
+struct TmapEntry {
+    const void *ptr = nullptr;
+    long long rows = 0;
+    int D = 0, B = 0;
+    bool bf16 = false;
+    CUtensorMap map;
+};
+
+cudaError_t cache_tensor_map(const void *ptr, bool bf16, int D, int B, long long rows, CUtensorMap *out) {
+    thread_local TmapEntry cache[4];
+    thread_local int next = 0;
+    for (auto &e : cache)
+        if (e.ptr == ptr && e.rows == rows && e.D == D && e.B == B && e.bf16 == bf16) {
+            *out = e.map;
+            return cudaSuccess;
+        }
+    TmapEntry &e = cache[next];
+    next = (next + 1) % 4;
+    cudaError_t rc = pa::make_cache_tensor_map(&e.map, ptr, bf16, D, B, rows);
+    if (rc != cudaSuccess) {
+        e.ptr = nullptr;
+        return rc;
+    }
+    e.ptr = ptr;
+    e.rows = rows;
+    e.D = D;
+    e.B = B;
+    e.bf16 = bf16;
+    *out = e.map;
+    return cudaSuccess;
 }
 
 int32_t to_status(cudaError_t e) {
@@ -106,7 +166,8 @@ int32_t pa_decode(const pa_dims *dims, const void *q, const void *k_cache, const
         !aligned(block_tables, 4) || !aligned(context_lens, 4))
         return PA_ERR_INVALID;
     const size_t need = workspace_bytes_for(dims, parts);
-    if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16))) return PA_ERR_INVALID;
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return PA_ERR_INVALID;
+    const WsLayout L = workspace_layout(dims, parts);
 
     pa::DecodeArgs a{};
     a.q = q;
@@ -115,9 +176,12 @@ int32_t pa_decode(const pa_dims *dims, const void *q, const void *k_cache, const
     a.block_tables = block_tables;
     a.context_lens = context_lens;
     a.out = out;
-    const size_t acc_floats = (size_t)dims->num_seqs * dims->num_q_heads * parts * dims->head_dim;
-    a.ws_acc = need ? static_cast<float *>(workspace) : nullptr;
-    a.ws_ml = need ? static_cast<float *>(workspace) + acc_floats : nullptr;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    a.plan_hdr = reinterpret_cast<int *>(ws);
+    a.plan_cnt = reinterpret_cast<int *>(ws + L.cnt);
+    a.plan_list = reinterpret_cast<int2 *>(ws + L.list);
+    a.ws_acc = parts > 1 ? reinterpret_cast<float *>(ws + L.acc) : nullptr;
+    a.ws_ml = parts > 1 ? reinterpret_cast<float *>(ws + L.ml) : nullptr;
     a.err = error_word();
     if (!a.err) return PA_ERR_CUDA;
     a.S = dims->num_seqs;
@@ -133,17 +197,27 @@ int32_t pa_decode(const pa_dims *dims, const void *q, const void *k_cache, const
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    switch (dims->kv_dtype) {
-        case PA_F32: e = pa::launch_decode_f32(a, st); break;
-        case PA_F16: e = pa::launch_decode_f16(a, st); break;
-        default: e = pa::launch_decode_bf16(a, st); break;
-    }
-    if (e != cudaSuccess) return to_status(e);
-    if (parts > 1) {
-        e = pa::launch_decode_merge(a, st);
+    if (dims->kv_dtype == PA_F32) {
+        // fp32 caches: CUDA-core kernel, then the merge kernel for split-K
+        e = pa::launch_decode_f32(a, st);
         if (e != cudaSuccess) return to_status(e);
+        if (parts > 1) {
+            e = pa::launch_decode_merge(a, st);
+            if (e != cudaSuccess) return to_status(e);
+        }
+        return PA_OK;
     }
-    return PA_OK;
+    // f16 / bf16 caches: work list, then the persistent tensor-core kernel
+    const bool bf16 = dims->kv_dtype == PA_BF16;
+    const long long rows = (long long)dims->num_blocks * dims->num_kv_heads * dims->block_size;
+    CUtensorMap tmk, tmv;
+    e = cache_tensor_map(k_cache, bf16, dims->head_dim, dims->block_size, rows, &tmk);
+    if (e == cudaSuccess) e = cache_tensor_map(v_cache, bf16, dims->head_dim, dims->block_size, rows, &tmv);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+    e = pa::launch_decode_plan(a, st);
+    if (e != cudaSuccess) return to_status(e);
+    e = bf16 ? pa::launch_decode_mma_bf16(a, tmk, tmv, st) : pa::launch_decode_mma_f16(a, tmk, tmv, st);
+    return to_status(e);
 }
 
 int32_t pa_write_kv(const pa_dims *dims, const void *k, const void *v, const int64_t *slot_mapping,

@@ -51,9 +51,6 @@ namespace pa {
 
 constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
 
-// Polls of a bounded mbarrier wait before the kernel reports a timeout.
-constexpr uint32_t kWaitLimit = 1u << 22;
-
 template <typename T, int D, int B, int G>
 struct DecodeCfg {
     static constexpr int kEB = Elem<T>::kBytes;

@@ -1,7 +1,10 @@
-// pa_decode_bf16.cu -- decode kernel instantiations for bf16 KV caches (kept in a
-// translation unit of their own so the three dtypes compile in parallel).
-#include "pa_decode.cuh"
+// pa_decode_bf16.cu -- tensor-core decode instantiations for bf16 KV caches
+// (a translation unit of its own so the dtypes compile in parallel).
+#include "pa_decode_mma.cuh"
 
 namespace pa {
-cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t st) { return dispatch_decode<__nv_bfloat16>(a, st); }
+cudaError_t launch_decode_mma_bf16(const DecodeArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                                 cudaStream_t st) {
+    return dispatch_decode_mma<__nv_bfloat16>(a, tmk, tmv, st);
+}
 }  // namespace pa

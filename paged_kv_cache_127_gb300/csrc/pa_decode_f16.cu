@@ -1,7 +1,10 @@
-// pa_decode_f16.cu -- decode kernel instantiations for f16 KV caches (kept in a
-// translation unit of their own so the three dtypes compile in parallel).
-#include "pa_decode.cuh"
+// pa_decode_f16.cu -- tensor-core decode instantiations for f16 KV caches
+// (a translation unit of its own so the dtypes compile in parallel).
+#include "pa_decode_mma.cuh"
 
 namespace pa {
-cudaError_t launch_decode_f16(const DecodeArgs &a, cudaStream_t st) { return dispatch_decode<__half>(a, st); }
+cudaError_t launch_decode_mma_f16(const DecodeArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                                 cudaStream_t st) {
+    return dispatch_decode_mma<__half>(a, tmk, tmv, st);
+}
 }  // namespace pa

@@ -11,6 +11,9 @@
 
 namespace pa {
 
+// Polls of a bounded mbarrier wait before a kernel reports a timeout.
+constexpr uint32_t kWaitLimit = 1u << 22;
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

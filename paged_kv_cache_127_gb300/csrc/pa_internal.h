@@ -2,6 +2,7 @@
 // (pa_api.cu) and the per-dtype kernel translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -17,6 +18,9 @@ struct DecodeArgs {
     float *out;
     float *ws_ml;    // [S, Hq, P, 2]  (m in log2 units, l)
     float *ws_acc;   // [S, Hq, P, D]
+    int *plan_hdr;   // [0] work items, [1] claim counter
+    int *plan_cnt;   // [S, Hkv] partitions finished (split-K merge)
+    int2 *plan_list; // (sequence, partition) per item, largest first
     unsigned int *err;
     int S, Hq, Hkv, D, B, N, max_blocks, partition_size, max_parts;
     float scale;
@@ -25,14 +29,27 @@ struct DecodeArgs {
 // Tokens per partition upper bound (table slice staged in shared memory).
 constexpr int kMaxPartitionBlocks = 256;
 
-// Per-dtype launchers; return cudaSuccess, cudaErrorNotSupported for a shape
-// that is not compiled, or the launch error.
+// Launchers return cudaSuccess, cudaErrorNotSupported for a shape that is not
+// compiled, or the launch error.
+// CUDA-core decode (fp32 caches).
 cudaError_t launch_decode_f32(const DecodeArgs &a, cudaStream_t st);
-cudaError_t launch_decode_f16(const DecodeArgs &a, cudaStream_t st);
-cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t st);
 
-// Cross-partition merge (dtype independent).
+// Cross-partition merge (dtype independent; f32 path).
 cudaError_t launch_decode_merge(const DecodeArgs &a, cudaStream_t st);
+
+// Work list for the tensor-core decode (f16 / bf16 path).
+cudaError_t launch_decode_plan(const DecodeArgs &a, cudaStream_t st);
+
+// Tensor-core decode: f16 / bf16 caches, K and V read through 2-D tensor maps
+// ([N*Hkv*B rows, D columns], 64x B boxes, 128-byte swizzle).
+cudaError_t launch_decode_mma_f16(const DecodeArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                                  cudaStream_t st);
+cudaError_t launch_decode_mma_bf16(const DecodeArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                                   cudaStream_t st);
+
+// Encode the tensor map of one cache ([N*Hkv*B, D] 16-bit rows).
+cudaError_t make_cache_tensor_map(CUtensorMap *map, const void *cache, bool bf16, int D, int B,
+                                  long long rows);
 
 cudaError_t launch_write_kv(const void *k, const void *v, const int64_t *slots, int T, int Hkv,
                             int row_bytes, int B, int N, void *k_cache, void *v_cache,

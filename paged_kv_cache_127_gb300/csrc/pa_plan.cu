@@ -1,0 +1,73 @@
+// pa_plan.cu -- work list for the tensor-core decode.
+//
+// One CTA lists every (sequence, partition) pair of the batch, largest
+// partition first (a counting sort on the partition's block count), so the
+// persistent decode kernel hands out big items before small ones and its
+// tail is short.  It also resets the claim counter and the per-(sequence,
+// KV head) merge counters, writes the all-zero output rows of empty contexts,
+// and flags context lengths outside [0, max_blocks * B].
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+__global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeArgs a) {
+    __shared__ int hist[kMaxPartitionBlocks + 1];
+    __shared__ int start[kMaxPartitionBlocks + 1];
+    // let the decode kernel start its set-up; it waits for this grid before
+    // reading anything written here
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int tid = threadIdx.x;
+    const int Pt = a.partition_size;
+    const int B = a.B;
+    const int cap = a.max_blocks * B;
+    const int maxpb = Pt / B;
+    for (int i = tid; i <= maxpb; i += blockDim.x) hist[i] = 0;
+    for (int i = tid; i < a.S * a.Hkv; i += blockDim.x) a.plan_cnt[i] = 0;
+    if (tid == 0) a.plan_hdr[1] = 0;
+    __syncthreads();
+    for (int s = tid; s < a.S; s += blockDim.x) {
+        int len = a.context_lens[s];
+        if (len < 0 || len > cap) {
+            set_error(a.err, PA_DEVERR_BAD_LEN);
+            len = len < 0 ? 0 : cap;
+        }
+        if (len == 0) {
+            float4 *row = reinterpret_cast<float4 *>(a.out + (size_t)s * a.Hq * a.D);
+            for (int i = 0; i < a.Hq * a.D / 4; ++i) row[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            continue;
+        }
+        const int np = (len + Pt - 1) / Pt;
+        for (int p = 0; p < np; ++p) {
+            const int nt = min(Pt, len - p * Pt);
+            atomicAdd(&hist[(nt + B - 1) / B], 1);
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int acc = 0;
+        for (int z = maxpb; z >= 1; --z) {
+            start[z] = acc;
+            acc += hist[z];
+        }
+        a.plan_hdr[0] = acc * a.Hkv;
+    }
+    __syncthreads();
+    for (int s = tid; s < a.S; s += blockDim.x) {
+        int len = a.context_lens[s];
+        len = len < 0 ? 0 : (len > cap ? cap : len);
+        const int np = (len + Pt - 1) / Pt;
+        for (int p = 0; p < np; ++p) {
+            const int nt = min(Pt, len - p * Pt);
+            const int pos = atomicAdd(&start[(nt + B - 1) / B], 1);
+            a.plan_list[pos] = make_int2(s, p);
+        }
+    }
+}
+
+cudaError_t launch_decode_plan(const DecodeArgs &a, cudaStream_t st) {
+    decode_plan_kernel<<<1, 1024, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -57,13 +57,20 @@ def test_version(pa):
 
 
 def test_workspace_bytes(pa):
-    d = pa.make_dims(num_seqs=256, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+    def up(x):
+        return (x + 255) // 256 * 256
+
+    S, Hq, Hkv, D = 256, 32, 8, 128
+    d = pa.make_dims(num_seqs=S, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, block_size=16,
                      num_blocks=1000, max_blocks_per_seq=256, partition_size=512, kv_dtype="bf16")
-    parts = (256 * 16 + 511) // 512
-    expect = 256 * 32 * parts * (128 + 2) * 4
-    assert pa.pa_decode_workspace_bytes(d) == (expect + 255) // 256 * 256
-    d.max_blocks_per_seq = 32            # one partition covers every context
+    P = (256 * 16 + 511) // 512
+    expect = 256 + up(S * Hkv * 4) + up(S * P * 8) + up(S * Hq * P * D * 4) + up(S * Hq * P * 2 * 4)
+    assert pa.pa_decode_workspace_bytes(d) == expect
+    d.max_blocks_per_seq = 32            # one partition covers every context: no partials
+    assert pa.pa_decode_workspace_bytes(d) == 256 + up(S * Hkv * 4) + up(S * 8)
+    d.num_seqs = 0
     assert pa.pa_decode_workspace_bytes(d) == 0
+    d.num_seqs = S
     d.num_q_heads = 30                   # Hq not a multiple of Hkv: invalid -> 0
     assert pa.pa_decode_workspace_bytes(d) == 0
 
@@ -85,8 +92,9 @@ def test_decode_rejects_bad_arguments_on_the_host(pa):
     assert _decode_status(pa, partition_size=24) == pa.PA_ERR_INVALID                   # not a multiple of B
     assert _decode_status(pa, kv_dtype=7) == pa.PA_ERR_INVALID
     assert _decode_status(pa, num_blocks=0) == pa.PA_ERR_INVALID
-    # needs a workspace (2 partitions of 32 tokens) but none is given
+    # needs a workspace but none is given
     assert _decode_status(pa, partition_size=32) == pa.PA_ERR_INVALID
+    assert _decode_status(pa) == pa.PA_ERR_INVALID
     d = pa.make_dims(num_seqs=1, num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
                      num_blocks=8, max_blocks_per_seq=4)
     assert pa.lib.pa_decode(ctypes.byref(d), None, None, None, None, None, 1.0, None, None, 0,
