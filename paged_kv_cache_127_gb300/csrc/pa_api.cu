@@ -76,7 +76,7 @@ int32_t check_decode_dims(const pa_dims *d, int32_t *max_parts) {
 // Workspace layout, each part 256-byte aligned:
 //   header    2 ints: work items, claim counter
 //   counters  int [S, Hkv]: partitions finished per (sequence, KV head)
-//   list      int2 [S * P]: (sequence, partition) work items, largest first
+//   list      int4 [S * P]: (sequence, partition, tokens, partitions) work items, largest first
 //   acc       float [S, Hq, P, D]: split-K partial sums          (only if P > 1)
 //   ml        float [S, Hq, P, 2]: partial (max in log2 units, sum) (only if P > 1)
 struct WsLayout {
@@ -91,7 +91,7 @@ WsLayout workspace_layout(const pa_dims *d, int32_t max_parts) {
     L.cnt = off;
     off += up(S * d->num_kv_heads * sizeof(int));
     L.list = off;
-    off += up(S * max_parts * 2 * sizeof(int));
+    off += up(S * max_parts * 4 * sizeof(int));
     L.acc = off;
     off += max_parts > 1 ? up(S * d->num_q_heads * max_parts * d->head_dim * sizeof(float)) : 0;
     L.ml = off;
@@ -109,22 +109,22 @@ size_t workspace_bytes_for(const pa_dims *d, int32_t max_parts) {
 struct TmapEntry {
     const void *ptr = nullptr;
     long long rows = 0;
-    int D = 0, B = 0;
+    int D = 0;
     bool bf16 = false;
     CUtensorMap map;
 };
 
-cudaError_t cache_tensor_map(const void *ptr, bool bf16, int D, int B, long long rows, CUtensorMap *out) {
+cudaError_t cache_tensor_map(const void *ptr, bool bf16, int D, long long rows, CUtensorMap *out) {
     thread_local TmapEntry cache[4];
     thread_local int next = 0;
     for (auto &e : cache)
-        if (e.ptr == ptr && e.rows == rows && e.D == D && e.B == B && e.bf16 == bf16) {
+        if (e.ptr == ptr && e.rows == rows && e.D == D && e.bf16 == bf16) {
             *out = e.map;
             return cudaSuccess;
         }
     TmapEntry &e = cache[next];
     next = (next + 1) % 4;
-    cudaError_t rc = pa::make_cache_tensor_map(&e.map, ptr, bf16, D, B, rows);
+    cudaError_t rc = pa::make_cache_tensor_map(&e.map, ptr, bf16, D, rows);
     if (rc != cudaSuccess) {
         e.ptr = nullptr;
         return rc;
@@ -132,7 +132,6 @@ cudaError_t cache_tensor_map(const void *ptr, bool bf16, int D, int B, long long
     e.ptr = ptr;
     e.rows = rows;
     e.D = D;
-    e.B = B;
     e.bf16 = bf16;
     *out = e.map;
     return cudaSuccess;
@@ -179,7 +178,7 @@ int32_t pa_decode(const pa_dims *dims, const void *q, const void *k_cache, const
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     a.plan_hdr = reinterpret_cast<int *>(ws);
     a.plan_cnt = reinterpret_cast<int *>(ws + L.cnt);
-    a.plan_list = reinterpret_cast<int2 *>(ws + L.list);
+    a.plan_list = reinterpret_cast<int4 *>(ws + L.list);
     a.ws_acc = parts > 1 ? reinterpret_cast<float *>(ws + L.acc) : nullptr;
     a.ws_ml = parts > 1 ? reinterpret_cast<float *>(ws + L.ml) : nullptr;
     a.err = error_word();
@@ -211,8 +210,8 @@ int32_t pa_decode(const pa_dims *dims, const void *q, const void *k_cache, const
     const bool bf16 = dims->kv_dtype == PA_BF16;
     const long long rows = (long long)dims->num_blocks * dims->num_kv_heads * dims->block_size;
     CUtensorMap tmk, tmv;
-    e = cache_tensor_map(k_cache, bf16, dims->head_dim, dims->block_size, rows, &tmk);
-    if (e == cudaSuccess) e = cache_tensor_map(v_cache, bf16, dims->head_dim, dims->block_size, rows, &tmv);
+    e = cache_tensor_map(k_cache, bf16, dims->head_dim, rows, &tmk);
+    if (e == cudaSuccess) e = cache_tensor_map(v_cache, bf16, dims->head_dim, rows, &tmv);
     if (e != cudaSuccess) return PA_ERR_CUDA;
     e = pa::launch_decode_plan(a, st);
     if (e != cudaSuccess) return to_status(e);

@@ -23,6 +23,9 @@ __global__ void write_kv_kernel(const uint4 *__restrict__ k, const uint4 *__rest
                                 const int64_t *__restrict__ slots, int Hkv, int row_chunks, int B,
                                 int N, uint4 *__restrict__ kc, uint4 *__restrict__ vc,
                                 unsigned int *err) {
+    // a following kernel launched as a programmatic dependent may start its
+    // set-up now; it waits for this grid before it reads the caches
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int t = blockIdx.x;
     const int64_t slot = slots[t];
     if (slot < 0) return;
@@ -49,6 +52,7 @@ __global__ void write_kv_kernel(const uint4 *__restrict__ k, const uint4 *__rest
 
 __global__ void copy_blocks_kernel(uint4 *kc, uint4 *vc, const int64_t *__restrict__ pairs,
                                    int64_t chunks, int N, unsigned int *err) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int p = blockIdx.x;
     const int64_t src = pairs[2 * p];
     const int64_t dst = pairs[2 * p + 1];

@@ -119,39 +119,43 @@ struct Mma16<__half> {
 };
 
 // ------------------------------------------------------------------ configuration
-template <int D, int B>
+// A stage holds one 16-token chunk of one (physical block, KV head): its K rows
+// and its V rows, each split into 128-byte-wide swizzled sub-tiles.  A 32-slot
+// block is two chunks.
+template <int D>
 struct MmaCfg {
     static constexpr int kKS = D / 16;          // k-steps of q.k
     static constexpr int kNT = D / 8;           // 8-wide n-tiles of p.v
     static constexpr int kSub = D / 64;         // 128-byte swizzled sub-tiles per row
-    static constexpr int kSubBytes = B * 128;   // one sub-tile of one (block, head)
-    static constexpr int kTileBytes = kSub * kSubBytes;  // K (or V) rows of one (block, head)
+    static constexpr int kSubBytes = kChunkRows * 128;  // one sub-tile of a 16-token chunk
+    static constexpr int kTileBytes = kSub * kSubBytes;  // K (or V) rows of a chunk
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kChunks = B / 16;
-    static constexpr int kWarps = 4;
-    static constexpr int kStagesRaw = (48 * 1024) / kStageBytes;
-    static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
+    static constexpr int kWarps = 8;
+    static constexpr int kStages = (192 * 1024) / (kWarps * kStageBytes);
     static constexpr int kThreads = kWarps * 32;
     static constexpr int kTblCap = kMaxPartitionBlocks;  // table entries per item slot
     static constexpr size_t kBarsOff = (size_t)kWarps * kStages * kStageBytes;
     static constexpr size_t kTblOff = kBarsOff + (size_t)kWarps * kStages * 8;
     static constexpr size_t kSmem = kTblOff + (size_t)kWarps * 2 * kTblCap * 4 + 1024;  // + alignment slack
     static_assert(D == 64 || D == 128, "head_dim");
-    static_assert(B % 16 == 0, "block size");
-    static_assert(kSubBytes % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
+    static_assert(kChunkRows == 16, "one chunk is one m16n8k16 k-extent of tokens");
+    static_assert(kStages >= 2, "stages");
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
 
+// One work item: partition p of sequence s, for one KV head.  ntok tokens from
+// p * partition_size; np = partitions of the sequence.
 struct WorkItem {
-    int s, kvh, p, np, tok0, ntok, nblk;
+    int s, kvh, p, np, ntok, nchunk;
 };
 
 template <typename T, int D, int B>
-__global__ void __launch_bounds__(MmaCfg<D, B>::kThreads, 1)
+__global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
     decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv) {
-    using C = MmaCfg<D, B>;
+    using C = MmaCfg<D>;
     using M = Mma16<T>;
+    constexpr int kCPB = B / 16;  // chunks per block
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;  // 1024-aligned: the 128-byte swizzle repeats every 1 KB
@@ -160,7 +164,6 @@ __global__ void __launch_bounds__(MmaCfg<D, B>::kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int G = a.Hq / a.Hkv;
     const int Pt = a.partition_size;
-    const int cap = a.max_blocks * B;
 
     const uint32_t st0 = base + (uint32_t)(warp * C::kStages * C::kStageBytes);
     const uint32_t bar0 = base + (uint32_t)C::kBarsOff + (uint32_t)(warp * C::kStages * 8);
@@ -187,44 +190,67 @@ __global__ void __launch_bounds__(MmaCfg<D, B>::kThreads, 1)
     const uint32_t vx = (uint32_t)((lm >> 1) ^ lr);   // and for V reads
     const float sl = a.scale * 1.4426950408889634f;   // logits in log2 units
 
-    auto claim = [&](WorkItem &it, int32_t *tb) -> bool {
-        int idx = 0;
-        if (lane == 0) idx = atomicAdd(a.plan_hdr + 1, 1);
-        idx = __shfl_sync(0xffffffffu, idx, 0);
+    // Claims are pipelined: the counter is bumped one item ahead, so the atomic's
+    // latency is hidden behind the current item's work.
+    int ticket = 0;
+    if (lane == 0) ticket = atomicAdd(a.plan_hdr + 1, 1);
+    // Turn the pending ticket into a work item: its plan entry, its block-table
+    // slice (into tb) and its query fragments (into qf); then take the next ticket.
+    auto claim = [&](WorkItem &it, int32_t *tb, uint32_t (&qf)[C::kKS][2]) -> bool {
+        const int idx = __shfl_sync(0xffffffffu, ticket, 0);
+        if (lane == 0) ticket = atomicAdd(a.plan_hdr + 1, 1);
         if (idx >= n_items) return false;
-        const int2 e = a.plan_list[idx / a.Hkv];
+        const int4 e = a.plan_list[idx / a.Hkv];
         it.s = e.x;
         it.p = e.y;
+        it.ntok = e.z;
+        it.np = e.w;
         it.kvh = idx % a.Hkv;
-        int len = a.context_lens[it.s];
-        len = len < 0 ? 0 : (len > cap ? cap : len);
-        it.np = (len + Pt - 1) / Pt;
-        it.tok0 = it.p * Pt;
-        it.ntok = min(len, it.tok0 + Pt) - it.tok0;
-        it.nblk = (it.ntok + B - 1) / B;
-        const int32_t *row = a.block_tables + (size_t)it.s * a.max_blocks + it.tok0 / B;
-        for (int i = lane; i < it.nblk; i += 32) {
-            int pb = row[i];
-            if (pb < 0 || pb >= a.N) {
-                set_error(a.err, PA_DEVERR_BAD_BLOCK);
-                pb = -1;
+        it.nchunk = (it.ntok + 15) >> 4;
+        const int nblk = (it.ntok + B - 1) / B;
+        const int32_t *row = a.block_tables + (size_t)it.s * a.max_blocks + (size_t)it.p * (Pt / B);
+        int pbv[(kMaxPartitionBlocks + 31) / 32];
+#pragma unroll
+        for (int k = 0; k < (kMaxPartitionBlocks + 31) / 32; ++k) {
+            const int i = lane + 32 * k;
+            pbv[k] = i < nblk ? row[i] : 0;
+            if (32 * (k + 1) >= nblk) break;
+        }
+        const int h = it.kvh * G + g;
+        const uint16_t *qrow = static_cast<const uint16_t *>(a.q) + ((size_t)it.s * a.Hq + h) * D;
+#pragma unroll
+        for (int ks = 0; ks < C::kKS; ++ks) {
+            qf[ks][0] = g < G ? *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + c2) : 0u;
+            qf[ks][1] = g < G ? *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + c2) : 0u;
+        }
+#pragma unroll
+        for (int k = 0; k < (kMaxPartitionBlocks + 31) / 32; ++k) {
+            const int i = lane + 32 * k;
+            if (i < nblk) {
+                int pb = pbv[k];
+                if (pb < 0 || pb >= a.N) {
+                    set_error(a.err, PA_DEVERR_BAD_BLOCK);
+                    pb = -1;
+                }
+                tb[i] = pb;
             }
-            tb[i] = pb;
+            if (32 * (k + 1) >= nblk) break;
         }
         __syncwarp();
         return true;
     };
 
     int iss = 0, cons = 0;
-    auto issue_block = [&](int pb, int kvh) {
+    auto issue_chunk = [&](const int32_t *tb, int ci, int kvh) {
         const int slot = iss % C::kStages;
         const uint32_t bar = bar0 + 8 * slot;
         if (lane == 0) {
+            const int pb = tb[ci / kCPB];
             if (pb < 0) {
                 mbar_arrive(bar);  // bad table entry: complete the phase without data
             } else {
                 const uint32_t dst = st0 + (uint32_t)(slot * C::kStageBytes);
-                const int y = (pb * a.Hkv + kvh) * B;
+                const int y = (pb * a.Hkv + kvh) * B + (ci % kCPB) * 16;
                 mbar_arrive_expect_tx(bar, C::kStageBytes);
 #pragma unroll
                 for (int sb = 0; sb < C::kSub; ++sb) {
@@ -237,15 +263,16 @@ __global__ void __launch_bounds__(MmaCfg<D, B>::kThreads, 1)
     };
 
     WorkItem cur, nxt;
+    uint32_t qa[C::kKS][2], qn[C::kKS][2];
     int cs = 0;  // table slot of cur
-    if (!claim(cur, tbl)) return;
-    bool has_nxt = claim(nxt, tbl + C::kTblCap);
-    int iss_sel = 0, iss_j = 0;  // issue cursor: item (0 = cur, 1 = nxt) and block within it
+    if (!claim(cur, tbl, qa)) return;
+    bool has_nxt = claim(nxt, tbl + C::kTblCap, qn);
+    int iss_sel = 0, iss_j = 0;  // issue cursor: item (0 = cur, 1 = nxt) and chunk within it
     auto top_up = [&]() {
         while (iss - cons < C::kStages) {
             if (iss_sel == 0) {
-                if (iss_j < cur.nblk) {
-                    issue_block(tbl[cs * C::kTblCap + iss_j], cur.kvh);
+                if (iss_j < cur.nchunk) {
+                    issue_chunk(tbl + cs * C::kTblCap, iss_j, cur.kvh);
                     ++iss_j;
                     continue;
                 }
@@ -253,8 +280,8 @@ __global__ void __launch_bounds__(MmaCfg<D, B>::kThreads, 1)
                 iss_sel = 1;
                 iss_j = 0;
             }
-            if (iss_j < nxt.nblk) {
-                issue_block(tbl[(cs ^ 1) * C::kTblCap + iss_j], nxt.kvh);
+            if (iss_j < nxt.nchunk) {
+                issue_chunk(tbl + (cs ^ 1) * C::kTblCap, iss_j, nxt.kvh);
                 ++iss_j;
                 continue;
             }
@@ -263,23 +290,13 @@ __global__ void __launch_bounds__(MmaCfg<D, B>::kThreads, 1)
     };
 
     while (true) {
-        // ---- per item: query fragments (A of q.k), running softmax state
-        uint32_t qa[C::kKS][2];
-        {
-            const int h = cur.kvh * G + g;
-            const uint16_t *qrow = static_cast<const uint16_t *>(a.q) + ((size_t)cur.s * a.Hq + h) * D;
-#pragma unroll
-            for (int ks = 0; ks < C::kKS; ++ks) {
-                qa[ks][0] = g < G ? *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + c2) : 0u;
-                qa[ks][1] = g < G ? *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + c2) : 0u;
-            }
-        }
         float o[C::kNT][4];
 #pragma unroll
         for (int nt = 0; nt < C::kNT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
         float m_run = -INFINITY, l_run = 0.f;
+        const int32_t *ctb = tbl + cs * C::kTblCap;
 
-        for (int j = 0; j < cur.nblk; ++j) {
+        for (int j = 0; j < cur.nchunk; ++j) {
             top_up();
             const int slot = cons % C::kStages;
             const uint32_t parity = (uint32_t)(cons / C::kStages) & 1u;
@@ -290,52 +307,52 @@ __global__ void __launch_bounds__(MmaCfg<D, B>::kThreads, 1)
                     mbar_wait_bounded(bar0 + 8 * (k % C::kStages), (uint32_t)(k / C::kStages) & 1u, kWaitLimit);
                 return;
             }
-            const int pb = tbl[cs * C::kTblCap + j];
-            const int nv = pb < 0 ? 0 : min(B, cur.ntok - j * B);
+            const int nv = ctb[j / kCPB] < 0 ? 0 : min(16, cur.ntok - j * 16);
             const uint32_t kst = st0 + (uint32_t)(slot * C::kStageBytes);
             const uint32_t vst = kst + C::kTileBytes;
-            if (nv > 0 && nv < B) {
-                // tail block: zero the V rows past the context (whole 128-byte rows,
-                // so the swizzle does not matter)
-                const int nz = (B - nv) * C::kSub * 8;
-                for (int i = lane; i < nz; i += 32) {
-                    const int chunk = i & 7;
-                    const int rowi = i >> 3;
-                    const int sb = rowi / (B - nv);
-                    const int r = nv + rowi % (B - nv);
-                    const uint32_t addr = vst + sb * C::kSubBytes + r * 128 + chunk * 16;
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+            if (nv > 0) {
+                if (nv < 16) {
+                    // tail chunk: zero the V rows past the context (whole 128-byte rows,
+                    // so the swizzle does not matter)
+                    const int nz = (16 - nv) * C::kSub * 8;
+                    for (int i = lane; i < nz; i += 32) {
+                        const int chunk = i & 7;
+                        const int rowi = i >> 3;
+                        const int sb = rowi / (16 - nv);
+                        const int r = nv + rowi % (16 - nv);
+                        const uint32_t addr = vst + sb * C::kSubBytes + r * 128 + chunk * 16;
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
-            }
+                // ---- S = Q K^T for 16 tokens (two n-tiles of 8), two accumulators
+                // per n-tile (even / odd k-steps) to halve the MMA dependency chain
+                float sc[2][2][4];
 #pragma unroll
-            for (int c = 0; c < C::kChunks; ++c) {
-                if (c * 16 >= nv) break;
-                // ---- S = Q K^T for 16 tokens (two n-tiles of 8)
-                float sc[2][4];
+                for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+                    for (int hh = 0; hh < 2; ++hh) sc[nt][hh][0] = sc[nt][hh][1] = sc[nt][hh][2] = sc[nt][hh][3] = 0.f;
 #pragma unroll
                 for (int ks2 = 0; ks2 < C::kKS / 2; ++ks2) {
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt) {
                         const uint32_t addr = kst + (uint32_t)((ks2 >> 1) * C::kSubBytes) +
-                                              (uint32_t)((c * 16 + nt * 8 + lr) * 128) +
+                                              (uint32_t)((nt * 8 + lr) * 128) +
                                               (((uint32_t)(4 * (ks2 & 1)) ^ kx) << 4);
                         uint32_t b0, b1, b2, b3;
                         ldsm_x4(addr, b0, b1, b2, b3);
-                        M::mma(sc[nt], qa[2 * ks2][0], 0u, qa[2 * ks2][1], 0u, b0, b1);
-                        M::mma(sc[nt], qa[2 * ks2 + 1][0], 0u, qa[2 * ks2 + 1][1], 0u, b2, b3);
+                        M::mma(sc[nt][0], qa[2 * ks2][0], 0u, qa[2 * ks2][1], 0u, b0, b1);
+                        M::mma(sc[nt][1], qa[2 * ks2 + 1][0], 0u, qa[2 * ks2 + 1][1], 0u, b2, b3);
                     }
                 }
                 // ---- online softmax on this lane's row g, tokens c2, c2+1, 8+c2, 9+c2
-                float x[4] = {sc[0][0] * sl, sc[0][1] * sl, sc[1][0] * sl, sc[1][1] * sl};
-                if (c * 16 + 16 > nv) {
-                    const int t0 = c * 16 + c2;
-                    if (t0 >= nv) x[0] = -INFINITY;
-                    if (t0 + 1 >= nv) x[1] = -INFINITY;
-                    if (t0 + 8 >= nv) x[2] = -INFINITY;
-                    if (t0 + 9 >= nv) x[3] = -INFINITY;
+                float x[4] = {(sc[0][0][0] + sc[0][1][0]) * sl, (sc[0][0][1] + sc[0][1][1]) * sl,
+                              (sc[1][0][0] + sc[1][1][0]) * sl, (sc[1][0][1] + sc[1][1][1]) * sl};
+                if (nv < 16) {
+                    if (c2 >= nv) x[0] = -INFINITY;
+                    if (c2 + 1 >= nv) x[1] = -INFINITY;
+                    if (c2 + 8 >= nv) x[2] = -INFINITY;
+                    if (c2 + 9 >= nv) x[3] = -INFINITY;
                 }
                 float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
@@ -368,7 +385,7 @@ __global__ void __launch_bounds__(MmaCfg<D, B>::kThreads, 1)
 #pragma unroll
                 for (int ntp = 0; ntp < C::kNT / 2; ++ntp) {
                     const uint32_t addr = vst + (uint32_t)((ntp >> 2) * C::kSubBytes) +
-                                          (uint32_t)((c * 16 + (lm & 1) * 8 + lr) * 128) +
+                                          (uint32_t)(((lm & 1) * 8 + lr) * 128) +
                                           (((uint32_t)(2 * (ntp & 3)) ^ vx) << 4);
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4_t(addr, b0, b1, b2, b3);
@@ -454,18 +471,23 @@ __global__ void __launch_bounds__(MmaCfg<D, B>::kThreads, 1)
         if (!has_nxt) break;
         cur = nxt;
         cs ^= 1;
+#pragma unroll
+        for (int ks = 0; ks < C::kKS; ++ks) {
+            qa[ks][0] = qn[ks][0];
+            qa[ks][1] = qn[ks][1];
+        }
         if (iss_sel == 1)
             iss_sel = 0;  // the cursor was already streaming the new current item
         else
             iss_j = 0;
-        has_nxt = claim(nxt, tbl + (cs ^ 1) * C::kTblCap);
+        has_nxt = claim(nxt, tbl + (cs ^ 1) * C::kTblCap, qn);
     }
 }
 
 template <typename T, int D, int B>
 cudaError_t launch_decode_mma_t(const DecodeArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                 cudaStream_t st) {
-    using C = MmaCfg<D, B>;
+    using C = MmaCfg<D>;
     static bool configured[64] = {};
     static int grid_for[64] = {};
     int dev = 0;

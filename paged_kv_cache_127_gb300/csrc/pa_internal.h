@@ -20,7 +20,7 @@ struct DecodeArgs {
     float *ws_acc;   // [S, Hq, P, D]
     int *plan_hdr;   // [0] work items, [1] claim counter
     int *plan_cnt;   // [S, Hkv] partitions finished (split-K merge)
-    int2 *plan_list; // (sequence, partition) per item, largest first
+    int4 *plan_list; // (sequence, partition, tokens, partitions of the sequence) per item, largest first
     unsigned int *err;
     int S, Hq, Hkv, D, B, N, max_blocks, partition_size, max_parts;
     float scale;
@@ -28,6 +28,10 @@ struct DecodeArgs {
 
 // Tokens per partition upper bound (table slice staged in shared memory).
 constexpr int kMaxPartitionBlocks = 256;
+
+// Token rows per tensor-core decode stage: one TMA box is this many rows of one
+// (physical block, KV head); a block of B slots is B / kChunkRows boxes.
+constexpr int kChunkRows = 16;
 
 // Launchers return cudaSuccess, cudaErrorNotSupported for a shape that is not
 // compiled, or the launch error.
@@ -47,9 +51,9 @@ cudaError_t launch_decode_mma_f16(const DecodeArgs &a, const CUtensorMap &tmk, c
 cudaError_t launch_decode_mma_bf16(const DecodeArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                    cudaStream_t st);
 
-// Encode the tensor map of one cache ([N*Hkv*B, D] 16-bit rows).
-cudaError_t make_cache_tensor_map(CUtensorMap *map, const void *cache, bool bf16, int D, int B,
-                                  long long rows);
+// Encode the tensor map of one cache ([N*Hkv*B, D] 16-bit rows; boxes of
+// 64 columns by kChunkRows rows).
+cudaError_t make_cache_tensor_map(CUtensorMap *map, const void *cache, bool bf16, int D, long long rows);
 
 cudaError_t launch_write_kv(const void *k, const void *v, const int64_t *slots, int T, int Hkv,
                             int row_bytes, int B, int N, void *k_cache, void *v_cache,

@@ -1,6 +1,7 @@
 // pa_plan.cu -- work list for the tensor-core decode.
 //
-// One CTA lists every (sequence, partition) pair of the batch, largest
+// One CTA lists every (sequence, partition) pair of the batch -- with the
+// partition's token count and the sequence's partition count -- largest
 // partition first (a counting sort on the partition's block count), so the
 // persistent decode kernel hands out big items before small ones and its
 // tail is short.  It also resets the claim counter and the per-(sequence,
@@ -14,9 +15,11 @@ namespace pa {
 __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeArgs a) {
     __shared__ int hist[kMaxPartitionBlocks + 1];
     __shared__ int start[kMaxPartitionBlocks + 1];
-    // let the decode kernel start its set-up; it waits for this grid before
-    // reading anything written here
+    // Let the decode kernel start its set-up (it waits for this grid before
+    // reading anything written here), then wait for the work before this one
+    // in the stream: the workspace and context_lens are only touched after it.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int tid = threadIdx.x;
     const int Pt = a.partition_size;
     const int B = a.B;
@@ -60,14 +63,24 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeArgs a) {
         for (int p = 0; p < np; ++p) {
             const int nt = min(Pt, len - p * Pt);
             const int pos = atomicAdd(&start[(nt + B - 1) / B], 1);
-            a.plan_list[pos] = make_int2(s, p);
+            a.plan_list[pos] = make_int4(s, p, nt, np);
         }
     }
 }
 
 cudaError_t launch_decode_plan(const DecodeArgs &a, cudaStream_t st) {
-    decode_plan_kernel<<<1, 1024, 0, st>>>(a);
-    return cudaGetLastError();
+    // launched as a programmatic dependent: its launch overlaps the tail of the
+    // previous kernel in the stream, and it waits for that kernel before work
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(1024);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_plan_kernel, a);
 }
 
 }  // namespace pa

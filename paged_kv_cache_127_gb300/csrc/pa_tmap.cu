@@ -1,10 +1,11 @@
 // pa_tmap.cu -- tensor maps (TMA descriptors) for the KV caches.
 //
 // A cache [N, Hkv, B, D] of 16-bit elements is described as a 2-D tensor of
-// N*Hkv*B rows by D columns.  A box is 64 columns (128 bytes) by B rows -- the
-// K (or V) rows of one (physical block, KV head), or half of them when D is
-// 128 -- written to shared memory with the 128-byte swizzle so that ldmatrix
-// reads of 8 rows hit 8 different bank groups.
+// N*Hkv*B rows by D columns.  A box is 64 columns (128 bytes) by kChunkRows
+// (16) rows -- 16 token rows of one (physical block, KV head), or the left or
+// right half of them when D is 128 -- written to shared memory with the
+// 128-byte swizzle so that ldmatrix reads of 8 rows hit 8 different bank
+// groups.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -29,12 +30,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 }  // namespace
 
-cudaError_t make_cache_tensor_map(CUtensorMap *map, const void *cache, bool bf16, int D, int B, long long rows) {
+cudaError_t make_cache_tensor_map(CUtensorMap *map, const void *cache, bool bf16, int D, long long rows) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    const cuuint32_t box[2] = {64u, (cuuint32_t)B};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)kChunkRows};
     const cuuint32_t estr[2] = {1u, 1u};
     CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
                      const_cast<void *>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
