@@ -207,6 +207,8 @@ def run_ours(args):
     dist = dist_init(world, "nccl")
 
     step = workloads.build_step(args.workload, seed=rank, binding=pa)
+    if args.partition_size:
+        step.partition_size = args.partition_size
     dims = step.dims(pa)
     S, Hq, D = step.num_seqs, step.num_q_heads, step.head_dim
 
@@ -424,6 +426,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--partition-size", type=int, default=0,
+                    help="context tokens per split-K partition (default: the workload's, 512)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -108,30 +108,34 @@ size_t workspace_bytes_for(const pa_dims *d, int32_t max_parts) {
 // changes (per host thread).
 struct TmapEntry {
     const void *ptr = nullptr;
-    long long rows = 0;
-    int D = 0;
+    long long block_heads = 0;
+    int D = 0, B = 0, hg = 0;
     bool bf16 = false;
     CUtensorMap map;
 };
 
-cudaError_t cache_tensor_map(const void *ptr, bool bf16, int D, long long rows, CUtensorMap *out) {
+cudaError_t cache_tensor_map(const void *ptr, bool bf16, int D, int B, long long block_heads, int hg,
+                             CUtensorMap *out) {
     thread_local TmapEntry cache[4];
     thread_local int next = 0;
     for (auto &e : cache)
-        if (e.ptr == ptr && e.rows == rows && e.D == D && e.bf16 == bf16) {
+        if (e.ptr == ptr && e.block_heads == block_heads && e.D == D && e.B == B && e.hg == hg &&
+            e.bf16 == bf16) {
             *out = e.map;
             return cudaSuccess;
         }
     TmapEntry &e = cache[next];
     next = (next + 1) % 4;
-    cudaError_t rc = pa::make_cache_tensor_map(&e.map, ptr, bf16, D, rows);
+    cudaError_t rc = pa::make_cache_tensor_map(&e.map, ptr, bf16, D, B, block_heads, hg);
     if (rc != cudaSuccess) {
         e.ptr = nullptr;
         return rc;
     }
     e.ptr = ptr;
-    e.rows = rows;
+    e.block_heads = block_heads;
     e.D = D;
+    e.B = B;
+    e.hg = hg;
     e.bf16 = bf16;
     *out = e.map;
     return cudaSuccess;
@@ -192,6 +196,7 @@ int32_t pa_decode(const pa_dims *dims, const void *q, const void *k_cache, const
     a.max_blocks = dims->max_blocks_per_seq;
     a.partition_size = effective_partition(dims);
     a.max_parts = parts;
+    a.head_group = pa::decode_head_group(dims->num_kv_heads);
     a.scale = scale;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -208,10 +213,11 @@ int32_t pa_decode(const pa_dims *dims, const void *q, const void *k_cache, const
     }
     // f16 / bf16 caches: work list, then the persistent tensor-core kernel
     const bool bf16 = dims->kv_dtype == PA_BF16;
-    const long long rows = (long long)dims->num_blocks * dims->num_kv_heads * dims->block_size;
+    const long long block_heads = (long long)dims->num_blocks * dims->num_kv_heads;
     CUtensorMap tmk, tmv;
-    e = cache_tensor_map(k_cache, bf16, dims->head_dim, rows, &tmk);
-    if (e == cudaSuccess) e = cache_tensor_map(v_cache, bf16, dims->head_dim, rows, &tmv);
+    e = cache_tensor_map(k_cache, bf16, dims->head_dim, dims->block_size, block_heads, a.head_group, &tmk);
+    if (e == cudaSuccess)
+        e = cache_tensor_map(v_cache, bf16, dims->head_dim, dims->block_size, block_heads, a.head_group, &tmv);
     if (e != cudaSuccess) return PA_ERR_CUDA;
     e = pa::launch_decode_plan(a, st);
     if (e != cudaSuccess) return to_status(e);

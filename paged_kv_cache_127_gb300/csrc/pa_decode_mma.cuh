@@ -9,15 +9,16 @@
 //
 // over the context_lens[s] tokens of s, gathered through its block table.
 //
-// Work: a work item is one (sequence, KV head, context partition).  A small
-// plan kernel lists the items, largest first, in the workspace.  Every warp of
-// this persistent kernel is an independent decode engine: it claims items
-// from a global counter, keeps the next item's block-table slice in shared
-// memory, and streams the item's KV tiles through its own ring of shared-
-// memory stages.  Lane 0 fills a stage with TMA tensor copies
-// (cp.async.bulk.tensor, 128-byte swizzle): the K rows and the V rows of one
-// (physical block, KV head).  The ring runs across item boundaries, so HBM
-// stays busy while a warp finishes an item.
+// Work: a work item is one (sequence, context partition, group of HG KV heads).
+// A small plan kernel lists the (sequence, partition) pairs, largest first, in
+// the workspace.  The kernel is persistent: each CTA claims items from a global
+// counter and gives warp w the item's KV head g0 + w.  Warp 0's lane 0 is also
+// the producer: it streams the item's 16-token chunks into a ring of
+// shared-memory stages with TMA tensor copies (cp.async.bulk.tensor, 128-byte
+// swizzle) -- one 3-D box covers 16 rows of all HG heads, so a copy is 8 KB
+// rather than one head's 2 KB -- and runs ahead across item boundaries.  Full
+// barriers (transaction counts) signal data; empty barriers (one arrival per
+// warp) return stages to the producer.
 //
 // Per 16-token chunk, with G = Hq / Hkv query heads sharing the KV head:
 //   S = Q K^T   mma.m16n8k16, A = the G query rows (padded to 16 with zeros),
@@ -46,12 +47,28 @@
 namespace pa {
 
 // ------------------------------------------------------------------ PTX wrappers
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+// 3-D TMA tensor load into shared memory, completing on `bar`, with an L2
+// cache policy (the KV stream is read once per decode: evict-first).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, uint32_t bar,
+                                            uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-        "[%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+        "{%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
         : "memory");
+}
+
+// Non-blocking probe of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
@@ -118,42 +135,104 @@ struct Mma16<__half> {
     }
 };
 
-// ------------------------------------------------------------------ configuration
-// A stage holds one 16-token chunk of one (physical block, KV head): its K rows
-// and its V rows, each split into 128-byte-wide swizzled sub-tiles.  A 32-slot
-// block is two chunks.
+// ------------------------------------------------------------------ split-K merge
+// o = sum_b 2^(m_b - m*) acc_b / sum_b 2^(m_b - m*) l_b over the np partitions
+// of (s, kvh), for each of its G query heads ("Paged Attention and vLLM",
+// "Paged Attention CUDA Kernel", the merge equation; m in log2 units).  One warp;
+// the partials are read through L2 (they were written by other SMs), several
+// partitions per round trip.
 template <int D>
+__device__ __forceinline__ void merge_partitions(const DecodeArgs &a, int s, int kvh, int G, int np, int lane) {
+    constexpr int kPer = D / 32;
+    constexpr int kU = 4;  // partitions loaded per round trip
+    for (int gg = 0; gg < G; ++gg) {
+        const size_t r0 = ((size_t)s * a.Hq + kvh * G + gg) * a.max_parts;
+        float Mx = -INFINITY;
+        for (int pp = lane; pp < np; pp += 32) Mx = fmaxf(Mx, __ldcg(a.ws_ml + 2 * (r0 + pp)));
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, off));
+        float L = 0.f, acc[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
+        if (Mx != -INFINITY) {
+            for (int p0 = 0; p0 < np; p0 += kU) {
+                float2 ml[kU];
+                float v[kU][kPer];
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int pp = p0 + u;
+                    ml[u] = pp < np ? __ldcg(reinterpret_cast<const float2 *>(a.ws_ml + 2 * (r0 + pp)))
+                                    : make_float2(-INFINITY, 0.f);
+                    const float *src = a.ws_acc + (r0 + (pp < np ? pp : p0)) * D + lane * kPer;
+                    if constexpr (kPer == 4) {
+                        const float4 x = __ldcg(reinterpret_cast<const float4 *>(src));
+                        v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+                    } else {
+                        const float2 x = __ldcg(reinterpret_cast<const float2 *>(src));
+                        v[u][0] = x.x; v[u][1] = x.y;
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const float w = ex2(ml[u].x - Mx);  // 0 for the padding partitions
+                    L += w * ml[u].y;
+#pragma unroll
+                    for (int i = 0; i < kPer; ++i) acc[i] += w * v[u][i];
+                }
+            }
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        float *dst = a.out + ((size_t)s * a.Hq + kvh * G + gg) * D + lane * kPer;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) dst[i] = acc[i] * inv;
+    }
+}
+
+// ------------------------------------------------------------------ configuration
+// A CTA owns HG consecutive KV heads of one (sequence, partition) work item --
+// one warp per head.  A stage holds one 16-token chunk of the item for all HG
+// heads: K rows then V rows, each split into 128-byte-wide halves of D; one TMA
+// box is one half for the HG heads (HG x 16 rows x 128 bytes, 8 KB at HG = 4),
+// written with the 128-byte swizzle.  Bigger boxes than one head's 2 KB keep
+// the bulk-copy engine at HBM speed.
+#ifndef PA_MMA_STAGE_BUDGET
+#define PA_MMA_STAGE_BUDGET (96 * 1024)
+#endif
+
+template <int D, int HG>
 struct MmaCfg {
-    static constexpr int kKS = D / 16;          // k-steps of q.k
-    static constexpr int kNT = D / 8;           // 8-wide n-tiles of p.v
-    static constexpr int kSub = D / 64;         // 128-byte swizzled sub-tiles per row
-    static constexpr int kSubBytes = kChunkRows * 128;  // one sub-tile of a 16-token chunk
-    static constexpr int kTileBytes = kSub * kSubBytes;  // K (or V) rows of a chunk
+    static constexpr int kKS = D / 16;                   // k-steps of q.k
+    static constexpr int kNT = D / 8;                    // 8-wide n-tiles of p.v
+    static constexpr int kSub = D / 64;                  // 128-byte halves of a row
+    static constexpr int kHeadSub = kChunkRows * 128;    // one head's half-rows of a chunk
+    static constexpr int kBoxBytes = HG * kHeadSub;      // one TMA box: that, for HG heads
+    static constexpr int kTileBytes = kSub * kBoxBytes;  // K (or V) of a chunk, all HG heads
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kWarps = 8;
-    static constexpr int kStages = (192 * 1024) / (kWarps * kStageBytes);
+    static constexpr int kWarps = HG;
     static constexpr int kThreads = kWarps * 32;
+    static constexpr int kStagesRaw = PA_MMA_STAGE_BUDGET / kStageBytes;
+    static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
+    static constexpr int kSlots = 3;                     // work items in flight per CTA
     static constexpr int kTblCap = kMaxPartitionBlocks;  // table entries per item slot
-    static constexpr size_t kBarsOff = (size_t)kWarps * kStages * kStageBytes;
-    static constexpr size_t kTblOff = kBarsOff + (size_t)kWarps * kStages * 8;
-    static constexpr size_t kSmem = kTblOff + (size_t)kWarps * 2 * kTblCap * 4 + 1024;  // + alignment slack
+    // shared-memory layout from a 1024-aligned base
+    static constexpr size_t kFullOff = (size_t)kStages * kStageBytes;
+    static constexpr size_t kEmptyOff = kFullOff + 8 * kStages;
+    static constexpr size_t kItemFullOff = kEmptyOff + 8 * kStages;
+    static constexpr size_t kItemEmptyOff = kItemFullOff + 8 * kSlots;
+    static constexpr size_t kInfoOff = kItemEmptyOff + 8 * kSlots;   // kSlots x int4 (s, p, ntok, np) + int4 (g0, ...)
+    static constexpr size_t kTblOff = kInfoOff + 32 * kSlots;
+    static constexpr size_t kSmem = kTblOff + (size_t)kSlots * kTblCap * 4 + 1024;  // + alignment slack
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(kChunkRows == 16, "one chunk is one m16n8k16 k-extent of tokens");
-    static_assert(kStages >= 2, "stages");
+    static_assert(kHeadSub % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
 
-// One work item: partition p of sequence s, for one KV head.  ntok tokens from
-// p * partition_size; np = partitions of the sequence.
-struct WorkItem {
-    int s, kvh, p, np, ntok, nchunk;
-};
-
-template <typename T, int D, int B>
-__global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
+template <typename T, int D, int B, int HG>
+__global__ void __launch_bounds__(MmaCfg<D, HG>::kThreads, 2)
     decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv) {
-    using C = MmaCfg<D>;
+    using C = MmaCfg<D, HG>;
     using M = Mma16<T>;
     constexpr int kCPB = B / 16;  // chunks per block
     extern __shared__ unsigned char smem_raw[];
@@ -164,20 +243,29 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int G = a.Hq / a.Hkv;
     const int Pt = a.partition_size;
+    const int ngroups = a.Hkv / HG;
 
-    const uint32_t st0 = base + (uint32_t)(warp * C::kStages * C::kStageBytes);
-    const uint32_t bar0 = base + (uint32_t)C::kBarsOff + (uint32_t)(warp * C::kStages * 8);
-    int32_t *tbl = reinterpret_cast<int32_t *>(basep + C::kTblOff) + warp * 2 * C::kTblCap;
+    const uint32_t full0 = base + (uint32_t)C::kFullOff;
+    const uint32_t empty0 = base + (uint32_t)C::kEmptyOff;
+    const uint32_t ifull0 = base + (uint32_t)C::kItemFullOff;
+    const uint32_t iempty0 = base + (uint32_t)C::kItemEmptyOff;
+    int4 *info = reinterpret_cast<int4 *>(basep + C::kInfoOff);     // [slot * 2]: (s, p, ntok, np), (g0, nchunk, valid, -)
+    int32_t *tbl = reinterpret_cast<int32_t *>(basep + C::kTblOff);  // [slot][kTblCap]
 
-    if (lane == 0) {
-        for (int i = 0; i < C::kStages; ++i) mbar_init(bar0 + 8 * i, 1);
-        fence_mbar_init();
-        if (warp == 0) {
-            prefetch_tmap(&tmk);
-            prefetch_tmap(&tmv);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::kStages; ++i) {
+            mbar_init(full0 + 8 * i, 1);
+            mbar_init(empty0 + 8 * i, C::kWarps);
         }
+        for (int i = 0; i < C::kSlots; ++i) {
+            mbar_init(ifull0 + 8 * i, 1);
+            mbar_init(iempty0 + 8 * i, C::kWarps);
+        }
+        fence_mbar_init();
+        prefetch_tmap(&tmk);
+        prefetch_tmap(&tmv);
     }
-    __syncwarp();
+    __syncthreads();
     griddep_wait();  // the plan kernel's work list must be complete (no-op without PDL)
     const int n_items = a.plan_hdr[0];
 
@@ -189,138 +277,156 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
     const uint32_t kx = (uint32_t)(lm ^ lr);          // swizzled chunk bits for K reads
     const uint32_t vx = (uint32_t)((lm >> 1) ^ lr);   // and for V reads
     const float sl = a.scale * 1.4426950408889634f;   // logits in log2 units
+    const uint64_t pol = policy_evict_first();
 
-    // Claims are pipelined: the counter is bumped one item ahead, so the atomic's
-    // latency is hidden behind the current item's work.
+    // ------------------------------------------------------------ producer (warp 0)
+    // Warp 0 claims work items (one ticket ahead, hiding the atomic), fills the
+    // item slots, and lane 0 issues the TMA loads, running up to kStages chunks
+    // ahead of warp 0's own consumption and across item boundaries.
     int ticket = 0;
-    if (lane == 0) ticket = atomicAdd(a.plan_hdr + 1, 1);
-    // Turn the pending ticket into a work item: its plan entry, its block-table
-    // slice (into tb) and its query fragments (into qf); then take the next ticket.
-    auto claim = [&](WorkItem &it, int32_t *tb, uint32_t (&qf)[C::kKS][2]) -> bool {
+    if (warp == 0 && lane == 0) ticket = atomicAdd(a.plan_hdr + 1, 1);
+    int p_item = 0;    // item sequence number the issue cursor is in
+    int p_chunk = 0;   // next chunk of it
+    int p_claimed = 0; // items claimed (slots filled) so far
+    int iss = 0;       // chunks issued
+    bool p_done = false;
+
+    auto claim_into_slot = [&](int seq) {  // warp 0, uniform
+        const int slot = seq % C::kSlots;
+        if (seq >= C::kSlots)  // all warps must be done with the item that used this slot
+            mbar_wait_bounded(iempty0 + 8 * slot, (uint32_t)((seq / C::kSlots) - 1) & 1u, kWaitLimit);
         const int idx = __shfl_sync(0xffffffffu, ticket, 0);
         if (lane == 0) ticket = atomicAdd(a.plan_hdr + 1, 1);
-        if (idx >= n_items) return false;
-        const int4 e = a.plan_list[idx / a.Hkv];
-        it.s = e.x;
-        it.p = e.y;
-        it.ntok = e.z;
-        it.np = e.w;
-        it.kvh = idx % a.Hkv;
-        it.nchunk = (it.ntok + 15) >> 4;
-        const int nblk = (it.ntok + B - 1) / B;
-        const int32_t *row = a.block_tables + (size_t)it.s * a.max_blocks + (size_t)it.p * (Pt / B);
-        int pbv[(kMaxPartitionBlocks + 31) / 32];
-#pragma unroll
-        for (int k = 0; k < (kMaxPartitionBlocks + 31) / 32; ++k) {
-            const int i = lane + 32 * k;
-            pbv[k] = i < nblk ? row[i] : 0;
-            if (32 * (k + 1) >= nblk) break;
-        }
-        const int h = it.kvh * G + g;
-        const uint16_t *qrow = static_cast<const uint16_t *>(a.q) + ((size_t)it.s * a.Hq + h) * D;
-#pragma unroll
-        for (int ks = 0; ks < C::kKS; ++ks) {
-            qf[ks][0] = g < G ? *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + c2) : 0u;
-            qf[ks][1] = g < G ? *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + c2) : 0u;
-        }
-#pragma unroll
-        for (int k = 0; k < (kMaxPartitionBlocks + 31) / 32; ++k) {
-            const int i = lane + 32 * k;
-            if (i < nblk) {
-                int pb = pbv[k];
+        int4 e0 = make_int4(0, 0, 0, 0), e1 = make_int4(0, 0, 0, 0);
+        if (idx < n_items) {
+            const int4 e = a.plan_list[idx / ngroups];
+            e0 = e;
+            const int nchunk = (e.z + 15) >> 4;
+            e1 = make_int4((idx % ngroups) * HG, nchunk, 1, 0);
+            const int nblk = (e.z + B - 1) / B;
+            const int32_t *row = a.block_tables + (size_t)e.x * a.max_blocks + (size_t)e.y * (Pt / B);
+            int32_t *tb = tbl + slot * C::kTblCap;
+            for (int i = lane; i < nblk; i += 32) {
+                int pb = row[i];
                 if (pb < 0 || pb >= a.N) {
                     set_error(a.err, PA_DEVERR_BAD_BLOCK);
                     pb = -1;
                 }
                 tb[i] = pb;
             }
-            if (32 * (k + 1) >= nblk) break;
+        }
+        if (lane == 0) {
+            info[2 * slot] = e0;
+            info[2 * slot + 1] = e1;
         }
         __syncwarp();
-        return true;
+        if (lane == 0) mbar_arrive(ifull0 + 8 * slot);  // release: info and table visible
+        p_claimed = seq + 1;
+        return idx < n_items;
     };
 
-    int iss = 0, cons = 0;
-    auto issue_chunk = [&](const int32_t *tb, int ci, int kvh) {
-        const int slot = iss % C::kStages;
-        const uint32_t bar = bar0 + 8 * slot;
-        if (lane == 0) {
-            const int pb = tb[ci / kCPB];
-            if (pb < 0) {
-                mbar_arrive(bar);  // bad table entry: complete the phase without data
-            } else {
-                const uint32_t dst = st0 + (uint32_t)(slot * C::kStageBytes);
-                const int y = (pb * a.Hkv + kvh) * B + (ci % kCPB) * 16;
-                mbar_arrive_expect_tx(bar, C::kStageBytes);
-#pragma unroll
-                for (int sb = 0; sb < C::kSub; ++sb) {
-                    tma_load_2d(dst + sb * C::kSubBytes, &tmk, sb * 64, y, bar);
-                    tma_load_2d(dst + C::kTileBytes + sb * C::kSubBytes, &tmv, sb * 64, y, bar);
+    int cons = 0;  // chunks consumed by this warp
+    int seq = 0;   // item this warp is working on (same sequence of items in every warp)
+    // Issue chunks while fewer than kStages are ahead of warp 0's consumption.
+    // The cursor never enters an item whose slot is still held by warp 0's
+    // current item (claiming it would wait on warp 0 itself).
+    auto top_up = [&]() {  // warp 0, uniform
+        while (!p_done && iss - cons < C::kStages) {
+            const int slot = p_item % C::kSlots;
+            if (p_item >= p_claimed) {
+                if (p_item >= seq + C::kSlots) break;
+                if (!claim_into_slot(p_item)) {
+                    p_done = true;
+                    break;
                 }
             }
-        }
-        ++iss;
-    };
-
-    WorkItem cur, nxt;
-    uint32_t qa[C::kKS][2], qn[C::kKS][2];
-    int cs = 0;  // table slot of cur
-    if (!claim(cur, tbl, qa)) return;
-    bool has_nxt = claim(nxt, tbl + C::kTblCap, qn);
-    int iss_sel = 0, iss_j = 0;  // issue cursor: item (0 = cur, 1 = nxt) and chunk within it
-    auto top_up = [&]() {
-        while (iss - cons < C::kStages) {
-            if (iss_sel == 0) {
-                if (iss_j < cur.nchunk) {
-                    issue_chunk(tbl + cs * C::kTblCap, iss_j, cur.kvh);
-                    ++iss_j;
-                    continue;
-                }
-                if (!has_nxt) break;
-                iss_sel = 1;
-                iss_j = 0;
-            }
-            if (iss_j < nxt.nchunk) {
-                issue_chunk(tbl + (cs ^ 1) * C::kTblCap, iss_j, nxt.kvh);
-                ++iss_j;
+            const int4 e1 = info[2 * slot + 1];
+            if (p_chunk >= e1.y) {  // item exhausted: move on
+                ++p_item;
+                p_chunk = 0;
                 continue;
             }
-            break;
+            const int st = iss % C::kStages;
+            if (iss >= C::kStages)  // every warp has released this stage's previous chunk
+                mbar_wait_bounded(empty0 + 8 * st, (uint32_t)((iss / C::kStages) - 1) & 1u, kWaitLimit);
+            if (lane == 0) {
+                const uint32_t bar = full0 + 8 * st;
+                const int pb = tbl[slot * C::kTblCap + p_chunk / kCPB];
+                if (pb < 0) {
+                    mbar_arrive(bar);  // bad table entry: complete the phase without data
+                } else {
+                    const uint32_t dst = base + (uint32_t)(st * C::kStageBytes);
+                    const int y = (p_chunk % kCPB) * kChunkRows;
+                    const int z = pb * a.Hkv + e1.x;
+                    mbar_arrive_expect_tx(bar, C::kStageBytes);
+#pragma unroll
+                    for (int sb = 0; sb < C::kSub; ++sb) {
+                        tma_load_3d(dst + sb * C::kBoxBytes, &tmk, sb * 64, y, z, bar, pol);
+                        tma_load_3d(dst + C::kTileBytes + sb * C::kBoxBytes, &tmv, sb * 64, y, z, bar, pol);
+                    }
+                }
+            }
+            ++iss;
+            ++p_chunk;
         }
     };
 
-    while (true) {
+    // ------------------------------------------------------------ consumers (all warps)
+    uint32_t qa[C::kKS][2];
+    for (;; ++seq) {
+        const int slot = seq % C::kSlots;
+        if (warp == 0 && !p_done && seq >= p_claimed) {
+            if (!claim_into_slot(seq)) p_done = true;
+        }
+        if (!mbar_wait_bounded(ifull0 + 8 * slot, (uint32_t)(seq / C::kSlots) & 1u, kWaitLimit)) {
+            if (lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
+            break;
+        }
+        const int4 e0 = info[2 * slot];
+        const int4 e1 = info[2 * slot + 1];
+        if (!e1.z) break;  // no more work
+        const int s = e0.x, p = e0.y, ntok = e0.z, np = e0.w;
+        const int kvh = e1.x + warp;
+        const int nchunk = e1.y;
+        const int32_t *ctb = tbl + slot * C::kTblCap;
+        {
+            const int h = kvh * G + g;
+            const uint16_t *qrow = static_cast<const uint16_t *>(a.q) + ((size_t)s * a.Hq + h) * D;
+#pragma unroll
+            for (int ks = 0; ks < C::kKS; ++ks) {
+                qa[ks][0] = g < G ? *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + c2) : 0u;
+                qa[ks][1] = g < G ? *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + c2) : 0u;
+            }
+        }
         float o[C::kNT][4];
 #pragma unroll
         for (int nt = 0; nt < C::kNT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
         float m_run = -INFINITY, l_run = 0.f;
-        const int32_t *ctb = tbl + cs * C::kTblCap;
+        bool timed_out = false;
 
-        for (int j = 0; j < cur.nchunk; ++j) {
-            top_up();
-            const int slot = cons % C::kStages;
+        for (int j = 0; j < nchunk; ++j) {
+            if (warp == 0) top_up();
+            const int st = cons % C::kStages;
             const uint32_t parity = (uint32_t)(cons / C::kStages) & 1u;
-            const bool got = mbar_wait_bounded(bar0 + 8 * slot, parity, kWaitLimit);
-            if (!__all_sync(0xffffffffu, got)) {
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(full0 + 8 * st, parity, kWaitLimit))) {
                 if (lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
-                for (int k = cons + 1; k < iss; ++k)  // drain this warp's copies in flight
-                    mbar_wait_bounded(bar0 + 8 * (k % C::kStages), (uint32_t)(k / C::kStages) & 1u, kWaitLimit);
-                return;
+                timed_out = true;
+                break;
             }
-            const int nv = ctb[j / kCPB] < 0 ? 0 : min(16, cur.ntok - j * 16);
-            const uint32_t kst = st0 + (uint32_t)(slot * C::kStageBytes);
+            const int nv = ctb[j / kCPB] < 0 ? 0 : min(16, ntok - j * 16);
+            const uint32_t kst = base + (uint32_t)(st * C::kStageBytes) + (uint32_t)(warp * C::kHeadSub);
             const uint32_t vst = kst + C::kTileBytes;
             if (nv > 0) {
                 if (nv < 16) {
-                    // tail chunk: zero the V rows past the context (whole 128-byte rows,
-                    // so the swizzle does not matter)
+                    // tail chunk: zero this head's V rows past the context (whole
+                    // 128-byte rows, so the swizzle does not matter)
                     const int nz = (16 - nv) * C::kSub * 8;
                     for (int i = lane; i < nz; i += 32) {
                         const int chunk = i & 7;
                         const int rowi = i >> 3;
                         const int sb = rowi / (16 - nv);
                         const int r = nv + rowi % (16 - nv);
-                        const uint32_t addr = vst + sb * C::kSubBytes + r * 128 + chunk * 16;
+                        const uint32_t addr = vst + sb * C::kBoxBytes + r * 128 + chunk * 16;
                         asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
                     }
                     __syncwarp();
@@ -336,7 +442,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
                 for (int ks2 = 0; ks2 < C::kKS / 2; ++ks2) {
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt) {
-                        const uint32_t addr = kst + (uint32_t)((ks2 >> 1) * C::kSubBytes) +
+                        const uint32_t addr = kst + (uint32_t)((ks2 >> 1) * C::kBoxBytes) +
                                               (uint32_t)((nt * 8 + lr) * 128) +
                                               (((uint32_t)(4 * (ks2 & 1)) ^ kx) << 4);
                         uint32_t b0, b1, b2, b3;
@@ -370,21 +476,21 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
                     }
                     m_run = mn;
                 }
-                float p[4];
+                float pr[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) p[i] = ex2(x[i] - m_run);
-                l_run += (p[0] + p[1]) + (p[2] + p[3]);
+                for (int i = 0; i < 4; ++i) pr[i] = ex2(x[i] - m_run);
+                l_run += (pr[0] + pr[1]) + (pr[2] + pr[3]);
                 // P = P_hi + P_lo, both 16-bit: rows 0-7 of A carry P_hi, rows 8-15 P_lo
-                const uint32_t h01 = M::pack(p[0], p[1]);
-                const uint32_t h23 = M::pack(p[2], p[3]);
+                const uint32_t h01 = M::pack(pr[0], pr[1]);
+                const uint32_t h23 = M::pack(pr[2], pr[3]);
                 const float2 f01 = M::unpack(h01);
                 const float2 f23 = M::unpack(h23);
-                const uint32_t l01 = M::pack(p[0] - f01.x, p[1] - f01.y);
-                const uint32_t l23 = M::pack(p[2] - f23.x, p[3] - f23.y);
+                const uint32_t l01 = M::pack(pr[0] - f01.x, pr[1] - f01.y);
+                const uint32_t l23 = M::pack(pr[2] - f23.x, pr[3] - f23.y);
                 // ---- O += P V
 #pragma unroll
                 for (int ntp = 0; ntp < C::kNT / 2; ++ntp) {
-                    const uint32_t addr = vst + (uint32_t)((ntp >> 2) * C::kSubBytes) +
+                    const uint32_t addr = vst + (uint32_t)((ntp >> 2) * C::kBoxBytes) +
                                           (uint32_t)(((lm & 1) * 8 + lr) * 128) +
                                           (((uint32_t)(2 * (ntp & 3)) ^ vx) << 4);
                     uint32_t b0, b1, b2, b3;
@@ -393,22 +499,24 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
                     M::mma(o[2 * ntp + 1], h01, l01, h23, l23, b2, b3);
                 }
             }
-            // the stage is consumed: order these generic shared-memory accesses
-            // before the next bulk copy into it, then let lane 0 reuse it
+            // release the stage: order these generic shared-memory accesses before
+            // the next bulk copy into it, then count this warp out
             fence_proxy_async_smem();
             __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * st);
             ++cons;
         }
+        if (timed_out) break;
 
-        // ---- finish the item
+        // ---- finish this warp's head of the item
         float lt = l_run;
         lt += __shfl_xor_sync(0xffffffffu, lt, 1);
         lt += __shfl_xor_sync(0xffffffffu, lt, 2);
-        const int h = cur.kvh * G + g;
-        if (cur.np == 1) {
+        const int h = kvh * G + g;
+        if (np == 1) {
             if (g < G) {
                 const float inv = lt > 0.f ? 1.f / lt : 0.f;
-                float *orow = a.out + ((size_t)cur.s * a.Hq + h) * D;
+                float *orow = a.out + ((size_t)s * a.Hq + h) * D;
 #pragma unroll
                 for (int nt = 0; nt < C::kNT; ++nt)
                     *reinterpret_cast<float2 *>(orow + nt * 8 + c2) =
@@ -416,7 +524,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
             }
         } else {
             if (g < G) {
-                const size_t r = ((size_t)cur.s * a.Hq + h) * a.max_parts + cur.p;
+                const size_t r = ((size_t)s * a.Hq + h) * a.max_parts + p;
                 float *acc = a.ws_acc + r * D;
 #pragma unroll
                 for (int nt = 0; nt < C::kNT; ++nt)
@@ -427,67 +535,28 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 1)
             __threadfence();
             __syncwarp();
             int done = 0;
-            if (lane == 0) done = atomicAdd(a.plan_cnt + (size_t)cur.s * a.Hkv + cur.kvh, 1);
+            if (lane == 0) done = atomicAdd(a.plan_cnt + (size_t)s * a.Hkv + kvh, 1);
             done = __shfl_sync(0xffffffffu, done, 0);
-            if (done == cur.np - 1) {  // last partition of this (sequence, KV head): merge
+            if (done == np - 1) {  // last partition of this (sequence, KV head): merge
                 __threadfence();
-                constexpr int kPer = D / 32;
-                for (int gg = 0; gg < G; ++gg) {
-                    const size_t r0 = ((size_t)cur.s * a.Hq + cur.kvh * G + gg) * a.max_parts;
-                    float Mx = -INFINITY;
-                    for (int pp = lane; pp < cur.np; pp += 32) Mx = fmaxf(Mx, __ldcg(a.ws_ml + 2 * (r0 + pp)));
-#pragma unroll
-                    for (int off = 16; off >= 1; off >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, off));
-                    float L = 0.f, acc[kPer];
-#pragma unroll
-                    for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
-                    if (Mx != -INFINITY) {
-                        for (int pp = 0; pp < cur.np; ++pp) {
-                            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.ws_ml + 2 * (r0 + pp)));
-                            const float w = ex2(ml.x - Mx);
-                            L += w * ml.y;
-                            const float *src = a.ws_acc + (r0 + pp) * D + lane * kPer;
-                            if constexpr (kPer == 4) {
-                                const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
-                                acc[0] += w * v.x;
-                                acc[1] += w * v.y;
-                                acc[2] += w * v.z;
-                                acc[3] += w * v.w;
-                            } else {
-                                const float2 v = __ldcg(reinterpret_cast<const float2 *>(src));
-                                acc[0] += w * v.x;
-                                acc[1] += w * v.y;
-                            }
-                        }
-                    }
-                    const float inv = L > 0.f ? 1.f / L : 0.f;
-                    float *dst = a.out + ((size_t)cur.s * a.Hq + cur.kvh * G + gg) * D + lane * kPer;
-#pragma unroll
-                    for (int i = 0; i < kPer; ++i) dst[i] = acc[i] * inv;
-                }
+                merge_partitions<D>(a, s, kvh, G, np, lane);
             }
         }
-
-        if (!has_nxt) break;
-        cur = nxt;
-        cs ^= 1;
-#pragma unroll
-        for (int ks = 0; ks < C::kKS; ++ks) {
-            qa[ks][0] = qn[ks][0];
-            qa[ks][1] = qn[ks][1];
-        }
-        if (iss_sel == 1)
-            iss_sel = 0;  // the cursor was already streaming the new current item
-        else
-            iss_j = 0;
-        has_nxt = claim(nxt, tbl + (cs ^ 1) * C::kTblCap, qn);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(iempty0 + 8 * slot);  // this warp is done with the item slot
+    }
+    // Drain: warp 0 waits for any copies it issued that were never consumed
+    // (only after a timeout) before the CTA's shared memory is released.
+    if (warp == 0) {
+        for (int k = cons; k < iss; ++k)
+            mbar_wait_bounded(full0 + 8 * (k % C::kStages), (uint32_t)(k / C::kStages) & 1u, kWaitLimit);
     }
 }
 
-template <typename T, int D, int B>
+template <typename T, int D, int B, int HG>
 cudaError_t launch_decode_mma_t(const DecodeArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                 cudaStream_t st) {
-    using C = MmaCfg<D>;
+    using C = MmaCfg<D, HG>;
     static bool configured[64] = {};
     static int grid_for[64] = {};
     int dev = 0;
@@ -495,13 +564,13 @@ cudaError_t launch_decode_mma_t(const DecodeArgs &a, const CUtensorMap &tmk, con
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        e = cudaFuncSetAttribute(decode_mma_kernel<T, D, B>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(decode_mma_kernel<T, D, B, HG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)C::kSmem);
         if (e != cudaSuccess) return e;
         int sms = 0, per_sm = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_mma_kernel<T, D, B>, C::kThreads,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_mma_kernel<T, D, B, HG>, C::kThreads,
                                                           C::kSmem);
         if (e != cudaSuccess) return e;
         grid_for[dev] = sms * (per_sm > 0 ? per_sm : 1);
@@ -517,16 +586,26 @@ cudaError_t launch_decode_mma_t(const DecodeArgs &a, const CUtensorMap &tmk, con
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_mma_kernel<T, D, B>, a, tmk, tmv);
+    return cudaLaunchKernelEx(&cfg, decode_mma_kernel<T, D, B, HG>, a, tmk, tmv);
+}
+
+template <typename T, int D, int B>
+cudaError_t dispatch_decode_mma_hg(const DecodeArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                                   cudaStream_t st) {
+    switch (a.head_group) {
+        case 4: return launch_decode_mma_t<T, D, B, 4>(a, tmk, tmv, st);
+        case 2: return launch_decode_mma_t<T, D, B, 2>(a, tmk, tmv, st);
+        default: return launch_decode_mma_t<T, D, B, 1>(a, tmk, tmv, st);
+    }
 }
 
 template <typename T>
 cudaError_t dispatch_decode_mma(const DecodeArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                 cudaStream_t st) {
-    if (a.D == 64 && a.B == 16) return launch_decode_mma_t<T, 64, 16>(a, tmk, tmv, st);
-    if (a.D == 64 && a.B == 32) return launch_decode_mma_t<T, 64, 32>(a, tmk, tmv, st);
-    if (a.D == 128 && a.B == 16) return launch_decode_mma_t<T, 128, 16>(a, tmk, tmv, st);
-    if (a.D == 128 && a.B == 32) return launch_decode_mma_t<T, 128, 32>(a, tmk, tmv, st);
+    if (a.D == 64 && a.B == 16) return dispatch_decode_mma_hg<T, 64, 16>(a, tmk, tmv, st);
+    if (a.D == 64 && a.B == 32) return dispatch_decode_mma_hg<T, 64, 32>(a, tmk, tmv, st);
+    if (a.D == 128 && a.B == 16) return dispatch_decode_mma_hg<T, 128, 16>(a, tmk, tmv, st);
+    if (a.D == 128 && a.B == 32) return dispatch_decode_mma_hg<T, 128, 32>(a, tmk, tmv, st);
     return cudaErrorNotSupported;
 }
 

@@ -23,8 +23,13 @@ struct DecodeArgs {
     int4 *plan_list; // (sequence, partition, tokens, partitions of the sequence) per item, largest first
     unsigned int *err;
     int S, Hq, Hkv, D, B, N, max_blocks, partition_size, max_parts;
+    int head_group;  // KV heads per tensor-core work item (decode_head_group)
     float scale;
 };
+
+// KV heads that one tensor-core work item (one CTA) covers: 4 when they divide
+// Hkv, else 2, else 1.
+inline int decode_head_group(int Hkv) { return Hkv % 4 == 0 ? 4 : (Hkv % 2 == 0 ? 2 : 1); }
 
 // Tokens per partition upper bound (table slice staged in shared memory).
 constexpr int kMaxPartitionBlocks = 256;
@@ -51,9 +56,11 @@ cudaError_t launch_decode_mma_f16(const DecodeArgs &a, const CUtensorMap &tmk, c
 cudaError_t launch_decode_mma_bf16(const DecodeArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                    cudaStream_t st);
 
-// Encode the tensor map of one cache ([N*Hkv*B, D] 16-bit rows; boxes of
-// 64 columns by kChunkRows rows).
-cudaError_t make_cache_tensor_map(CUtensorMap *map, const void *cache, bool bf16, int D, long long rows);
+// Encode the tensor map of one cache [N, Hkv, B, D] of 16-bit elements as a
+// 3-D tensor {D, B, N*Hkv}; a box is 64 columns x kChunkRows rows x head_group
+// (block, head) pairs.
+cudaError_t make_cache_tensor_map(CUtensorMap *map, const void *cache, bool bf16, int D, int B,
+                                  long long block_heads, int head_group);
 
 cudaError_t launch_write_kv(const void *k, const void *v, const int64_t *slots, int T, int Hkv,
                             int row_bytes, int B, int N, void *k_cache, void *v_cache,

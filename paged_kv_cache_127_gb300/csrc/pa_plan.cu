@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeArgs a) {
             start[z] = acc;
             acc += hist[z];
         }
-        a.plan_hdr[0] = acc * a.Hkv;
+        a.plan_hdr[0] = acc * (a.Hkv / a.head_group);  // items: (sequence, partition, head group)
     }
     __syncthreads();
     for (int s = tid; s < a.S; s += blockDim.x) {

@@ -1,11 +1,11 @@
 // pa_tmap.cu -- tensor maps (TMA descriptors) for the KV caches.
 //
-// A cache [N, Hkv, B, D] of 16-bit elements is described as a 2-D tensor of
-// N*Hkv*B rows by D columns.  A box is 64 columns (128 bytes) by kChunkRows
-// (16) rows -- 16 token rows of one (physical block, KV head), or the left or
-// right half of them when D is 128 -- written to shared memory with the
-// 128-byte swizzle so that ldmatrix reads of 8 rows hit 8 different bank
-// groups.
+// A cache [N, Hkv, B, D] of 16-bit elements is described as a 3-D tensor
+// {D columns, B rows, N*Hkv (block, head) pairs}.  A box is 64 columns (128
+// bytes) x 16 rows x HG consecutive (block, head) pairs: 16 token rows of HG
+// KV heads of one physical block, the left or right half of D.  It lands in
+// shared memory as [HG][16][128 bytes] with the 128-byte swizzle, so ldmatrix
+// reads of 8 rows hit 8 different bank groups, and one copy moves HG x 2 KB.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -30,14 +30,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 }  // namespace
 
-cudaError_t make_cache_tensor_map(CUtensorMap *map, const void *cache, bool bf16, int D, long long rows) {
+cudaError_t make_cache_tensor_map(CUtensorMap *map, const void *cache, bool bf16, int D, int B,
+                                  long long block_heads, int head_group) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
-    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    const cuuint32_t box[2] = {64u, (cuuint32_t)kChunkRows};
-    const cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)B, (cuuint64_t)block_heads};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)B * D * 2};
+    const cuuint32_t box[3] = {64u, (cuuint32_t)kChunkRows, (cuuint32_t)head_group};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                      const_cast<void *>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
