@@ -88,7 +88,7 @@ typedef struct pa_dims {
 
 /*
  * pa_decode_workspace_bytes -- bytes of device scratch pa_decode needs: a
- * work list and counters (S * Hkv + S * P * 4 ints), plus, when one sequence
+ * work list (S * P * 4 ints after a 256-byte header), plus, when one sequence
  * can span several partitions (P > 1), the split-K partials: S * Hq * P *
  * (D + 2) floats; P = ceil(max_blocks_per_seq * B / partition_size).  Each part
  * is rounded up to 256 bytes.  Returns 0 for S == 0 and for invalid dims.

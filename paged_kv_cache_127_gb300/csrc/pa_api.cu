@@ -75,12 +75,11 @@ int32_t check_decode_dims(const pa_dims *d, int32_t *max_parts) {
 
 // Workspace layout, each part 256-byte aligned:
 //   header    2 ints: work items, claim counter
-//   counters  int [S, Hkv]: partitions finished per (sequence, KV head)
 //   list      int4 [S * P]: (sequence, partition, tokens, partitions) work items, largest first
 //   acc       float [S, Hq, P, D]: split-K partial sums          (only if P > 1)
 //   ml        float [S, Hq, P, 2]: partial (max in log2 units, sum) (only if P > 1)
 struct WsLayout {
-    size_t cnt, list, acc, ml, total;
+    size_t list, acc, ml, total;
 };
 
 WsLayout workspace_layout(const pa_dims *d, int32_t max_parts) {
@@ -88,8 +87,6 @@ WsLayout workspace_layout(const pa_dims *d, int32_t max_parts) {
     const size_t S = (size_t)d->num_seqs;
     WsLayout L{};
     size_t off = 256;
-    L.cnt = off;
-    off += up(S * d->num_kv_heads * sizeof(int));
     L.list = off;
     off += up(S * max_parts * 4 * sizeof(int));
     L.acc = off;
@@ -181,7 +178,6 @@ int32_t pa_decode(const pa_dims *dims, const void *q, const void *k_cache, const
     a.out = out;
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     a.plan_hdr = reinterpret_cast<int *>(ws);
-    a.plan_cnt = reinterpret_cast<int *>(ws + L.cnt);
     a.plan_list = reinterpret_cast<int4 *>(ws + L.list);
     a.ws_acc = parts > 1 ? reinterpret_cast<float *>(ws + L.acc) : nullptr;
     a.ws_ml = parts > 1 ? reinterpret_cast<float *>(ws + L.ml) : nullptr;
@@ -211,7 +207,8 @@ int32_t pa_decode(const pa_dims *dims, const void *q, const void *k_cache, const
         }
         return PA_OK;
     }
-    // f16 / bf16 caches: work list, then the persistent tensor-core kernel
+    // f16 / bf16 caches: work list, the persistent tensor-core kernel, then the
+    // split-K merge (each launch a programmatic dependent of the previous one)
     const bool bf16 = dims->kv_dtype == PA_BF16;
     const long long block_heads = (long long)dims->num_blocks * dims->num_kv_heads;
     CUtensorMap tmk, tmv;
@@ -222,6 +219,8 @@ int32_t pa_decode(const pa_dims *dims, const void *q, const void *k_cache, const
     e = pa::launch_decode_plan(a, st);
     if (e != cudaSuccess) return to_status(e);
     e = bf16 ? pa::launch_decode_mma_bf16(a, tmk, tmv, st) : pa::launch_decode_mma_f16(a, tmk, tmv, st);
+    if (e != cudaSuccess) return to_status(e);
+    if (parts > 1) e = pa::launch_decode_merge(a, st);
     return to_status(e);
 }
 

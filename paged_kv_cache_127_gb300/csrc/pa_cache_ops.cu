@@ -69,9 +69,14 @@ __global__ void copy_blocks_kernel(uint4 *kc, uint4 *vc, const int64_t *__restri
 }
 
 // One warp per (sequence, query head); lane i owns D/32 consecutive outputs.
+// Partials are read kU partitions per round trip.  The kernel may be launched
+// as a programmatic dependent of the decode kernel: it waits for that grid
+// (and so for every partial) before reading.
 template <int D>
 __global__ void decode_merge_kernel(const DecodeArgs a) {
     constexpr int kPer = D / 32;
+    constexpr int kU = 4;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int gw = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
     if (gw >= a.S * a.Hq) return;
@@ -93,12 +98,23 @@ __global__ void decode_merge_kernel(const DecodeArgs a) {
 #pragma unroll
     for (int i = 0; i < kPer; ++i) o[i] = 0.f;
     if (M != -INFINITY) {
-        for (int p = 0; p < np; ++p) {
-            const float w = ex2(ml[2 * p] - M);
-            L += w * ml[2 * p + 1];
-            const float *x = acc + (size_t)p * D + lane * kPer;
+        for (int p0 = 0; p0 < np; p0 += kU) {
+            float2 w[kU];
+            float x[kU][kPer];
 #pragma unroll
-            for (int i = 0; i < kPer; ++i) o[i] += w * x[i];
+            for (int u = 0; u < kU; ++u) {
+                const int p = p0 + u < np ? p0 + u : p0;
+                w[u] = p0 + u < np ? *reinterpret_cast<const float2 *>(ml + 2 * p) : make_float2(-INFINITY, 0.f);
+#pragma unroll
+                for (int i = 0; i < kPer; ++i) x[u][i] = acc[(size_t)p * D + lane * kPer + i];
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const float wt = ex2(w[u].x - M);  // 0 for the padding entries
+                L += wt * w[u].y;
+#pragma unroll
+                for (int i = 0; i < kPer; ++i) o[i] += wt * x[u][i];
+            }
         }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
@@ -109,15 +125,19 @@ __global__ void decode_merge_kernel(const DecodeArgs a) {
 
 cudaError_t launch_decode_merge(const DecodeArgs &a, cudaStream_t st) {
     const int warps = a.S * a.Hq;
-    const int per_block = 8;
-    const dim3 grid((unsigned)((warps + per_block - 1) / per_block));
-    if (a.D == 64)
-        decode_merge_kernel<64><<<grid, per_block * 32, 0, st>>>(a);
-    else if (a.D == 128)
-        decode_merge_kernel<128><<<grid, per_block * 32, 0, st>>>(a);
-    else
-        return cudaErrorNotSupported;
-    return cudaGetLastError();
+    const int per_block = 4;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((warps + per_block - 1) / per_block));
+    cfg.blockDim = dim3(per_block * 32);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (a.D == 64) return cudaLaunchKernelEx(&cfg, decode_merge_kernel<64>, a);
+    if (a.D == 128) return cudaLaunchKernelEx(&cfg, decode_merge_kernel<128>, a);
+    return cudaErrorNotSupported;
 }
 
 cudaError_t launch_write_kv(const void *k, const void *v, const int64_t *slots, int T, int Hkv,

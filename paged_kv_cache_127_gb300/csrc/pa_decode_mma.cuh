@@ -33,8 +33,10 @@
 // (so NaN in unused slots cannot leak through 0 * NaN).
 //
 // Finish: an item that covers its whole sequence writes out[] directly;
-// otherwise it stores (m, l, acc) for its partition, and the warp that
-// completes the last partition of a (sequence, KV head) merges them.
+// otherwise it stores (m, l, acc) for its partition and the merge kernel,
+// launched right after this one, combines the partitions.  (Merging in the
+// last-finishing warp instead needs a device-wide fence per partial and
+// stalls the CTA's stage ring while that warp merges; measured slower.)
 #pragma once
 
 #include <cuda.h>
@@ -135,59 +137,6 @@ struct Mma16<__half> {
     }
 };
 
-// ------------------------------------------------------------------ split-K merge
-// o = sum_b 2^(m_b - m*) acc_b / sum_b 2^(m_b - m*) l_b over the np partitions
-// of (s, kvh), for each of its G query heads ("Paged Attention and vLLM",
-// "Paged Attention CUDA Kernel", the merge equation; m in log2 units).  One warp;
-// the partials are read through L2 (they were written by other SMs), several
-// partitions per round trip.
-template <int D>
-__device__ __forceinline__ void merge_partitions(const DecodeArgs &a, int s, int kvh, int G, int np, int lane) {
-    constexpr int kPer = D / 32;
-    constexpr int kU = 4;  // partitions loaded per round trip
-    for (int gg = 0; gg < G; ++gg) {
-        const size_t r0 = ((size_t)s * a.Hq + kvh * G + gg) * a.max_parts;
-        float Mx = -INFINITY;
-        for (int pp = lane; pp < np; pp += 32) Mx = fmaxf(Mx, __ldcg(a.ws_ml + 2 * (r0 + pp)));
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, off));
-        float L = 0.f, acc[kPer];
-#pragma unroll
-        for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
-        if (Mx != -INFINITY) {
-            for (int p0 = 0; p0 < np; p0 += kU) {
-                float2 ml[kU];
-                float v[kU][kPer];
-#pragma unroll
-                for (int u = 0; u < kU; ++u) {
-                    const int pp = p0 + u;
-                    ml[u] = pp < np ? __ldcg(reinterpret_cast<const float2 *>(a.ws_ml + 2 * (r0 + pp)))
-                                    : make_float2(-INFINITY, 0.f);
-                    const float *src = a.ws_acc + (r0 + (pp < np ? pp : p0)) * D + lane * kPer;
-                    if constexpr (kPer == 4) {
-                        const float4 x = __ldcg(reinterpret_cast<const float4 *>(src));
-                        v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
-                    } else {
-                        const float2 x = __ldcg(reinterpret_cast<const float2 *>(src));
-                        v[u][0] = x.x; v[u][1] = x.y;
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < kU; ++u) {
-                    const float w = ex2(ml[u].x - Mx);  // 0 for the padding partitions
-                    L += w * ml[u].y;
-#pragma unroll
-                    for (int i = 0; i < kPer; ++i) acc[i] += w * v[u][i];
-                }
-            }
-        }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-        float *dst = a.out + ((size_t)s * a.Hq + kvh * G + gg) * D + lane * kPer;
-#pragma unroll
-        for (int i = 0; i < kPer; ++i) dst[i] = acc[i] * inv;
-    }
-}
-
 // ------------------------------------------------------------------ configuration
 // A CTA owns HG consecutive KV heads of one (sequence, partition) work item --
 // one warp per head.  A stage holds one 16-token chunk of the item for all HG
@@ -267,6 +216,9 @@ __global__ void __launch_bounds__(MmaCfg<D, HG>::kThreads, 2)
     }
     __syncthreads();
     griddep_wait();  // the plan kernel's work list must be complete (no-op without PDL)
+    // The merge kernel may be scheduled now: it only waits (griddepcontrol.wait)
+    // beside this grid, which already fills every SM, and starts on completion.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int n_items = a.plan_hdr[0];
 
     // ---- lane roles in the MMA fragments
@@ -532,15 +484,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HG>::kThreads, 2)
                         make_float2(o[nt][0] + o[nt][2], o[nt][1] + o[nt][3]);
                 if ((lane & 3) == 0) *reinterpret_cast<float2 *>(a.ws_ml + 2 * r) = make_float2(m_run, lt);
             }
-            __threadfence();
-            __syncwarp();
-            int done = 0;
-            if (lane == 0) done = atomicAdd(a.plan_cnt + (size_t)s * a.Hkv + kvh, 1);
-            done = __shfl_sync(0xffffffffu, done, 0);
-            if (done == np - 1) {  // last partition of this (sequence, KV head): merge
-                __threadfence();
-                merge_partitions<D>(a, s, kvh, G, np, lane);
-            }
+
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(iempty0 + 8 * slot);  // this warp is done with the item slot
@@ -593,6 +537,9 @@ template <typename T, int D, int B>
 cudaError_t dispatch_decode_mma_hg(const DecodeArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                    cudaStream_t st) {
     switch (a.head_group) {
+#if PA_MMA_HEAD_GROUP >= 8
+        case 8: return launch_decode_mma_t<T, D, B, 8>(a, tmk, tmv, st);
+#endif
         case 4: return launch_decode_mma_t<T, D, B, 4>(a, tmk, tmv, st);
         case 2: return launch_decode_mma_t<T, D, B, 2>(a, tmk, tmv, st);
         default: return launch_decode_mma_t<T, D, B, 1>(a, tmk, tmv, st);

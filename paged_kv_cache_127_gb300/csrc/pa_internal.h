@@ -19,7 +19,6 @@ struct DecodeArgs {
     float *ws_ml;    // [S, Hq, P, 2]  (m in log2 units, l)
     float *ws_acc;   // [S, Hq, P, D]
     int *plan_hdr;   // [0] work items, [1] claim counter
-    int *plan_cnt;   // [S, Hkv] partitions finished (split-K merge)
     int4 *plan_list; // (sequence, partition, tokens, partitions of the sequence) per item, largest first
     unsigned int *err;
     int S, Hq, Hkv, D, B, N, max_blocks, partition_size, max_parts;
@@ -27,9 +26,16 @@ struct DecodeArgs {
     float scale;
 };
 
-// KV heads that one tensor-core work item (one CTA) covers: 4 when they divide
-// Hkv, else 2, else 1.
-inline int decode_head_group(int Hkv) { return Hkv % 4 == 0 ? 4 : (Hkv % 2 == 0 ? 2 : 1); }
+// KV heads that one tensor-core work item (one CTA) covers: PA_MMA_HEAD_GROUP
+// (4 by default) when they divide Hkv, else the largest power of two that does.
+#ifndef PA_MMA_HEAD_GROUP
+#define PA_MMA_HEAD_GROUP 4
+#endif
+inline int decode_head_group(int Hkv) {
+    int hg = PA_MMA_HEAD_GROUP;
+    while (hg > 1 && Hkv % hg != 0) hg /= 2;
+    return hg;
+}
 
 // Tokens per partition upper bound (table slice staged in shared memory).
 constexpr int kMaxPartitionBlocks = 256;
@@ -43,7 +49,7 @@ constexpr int kChunkRows = 16;
 // CUDA-core decode (fp32 caches).
 cudaError_t launch_decode_f32(const DecodeArgs &a, cudaStream_t st);
 
-// Cross-partition merge (dtype independent; f32 path).
+// Cross-partition merge of the split-K partials (dtype independent).
 cudaError_t launch_decode_merge(const DecodeArgs &a, cudaStream_t st);
 
 // Work list for the tensor-core decode (f16 / bf16 path).

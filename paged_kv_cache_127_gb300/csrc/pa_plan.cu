@@ -4,9 +4,9 @@
 // partition's token count and the sequence's partition count -- largest
 // partition first (a counting sort on the partition's block count), so the
 // persistent decode kernel hands out big items before small ones and its
-// tail is short.  It also resets the claim counter and the per-(sequence,
-// KV head) merge counters, writes the all-zero output rows of empty contexts,
-// and flags context lengths outside [0, max_blocks * B].
+// tail is short.  It also resets the claim counter, writes the all-zero
+// output rows of empty contexts, and flags context lengths outside
+// [0, max_blocks * B].
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -26,7 +26,6 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeArgs a) {
     const int cap = a.max_blocks * B;
     const int maxpb = Pt / B;
     for (int i = tid; i <= maxpb; i += blockDim.x) hist[i] = 0;
-    for (int i = tid; i < a.S * a.Hkv; i += blockDim.x) a.plan_cnt[i] = 0;
     if (tid == 0) a.plan_hdr[1] = 0;
     __syncthreads();
     for (int s = tid; s < a.S; s += blockDim.x) {

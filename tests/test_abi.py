@@ -64,10 +64,10 @@ def test_workspace_bytes(pa):
     d = pa.make_dims(num_seqs=S, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, block_size=16,
                      num_blocks=1000, max_blocks_per_seq=256, partition_size=512, kv_dtype="bf16")
     P = (256 * 16 + 511) // 512
-    expect = 256 + up(S * Hkv * 4) + up(S * P * 16) + up(S * Hq * P * D * 4) + up(S * Hq * P * 2 * 4)
+    expect = 256 + up(S * P * 16) + up(S * Hq * P * D * 4) + up(S * Hq * P * 2 * 4)
     assert pa.pa_decode_workspace_bytes(d) == expect
     d.max_blocks_per_seq = 32            # one partition covers every context: no partials
-    assert pa.pa_decode_workspace_bytes(d) == 256 + up(S * Hkv * 4) + up(S * 16)
+    assert pa.pa_decode_workspace_bytes(d) == 256 + up(S * 16)
     d.num_seqs = 0
     assert pa.pa_decode_workspace_bytes(d) == 0
     d.num_seqs = S
