@@ -23,8 +23,10 @@ __global__ void write_kv_kernel(const uint4 *__restrict__ k, const uint4 *__rest
                                 const int64_t *__restrict__ slots, int Hkv, int row_chunks, int B,
                                 int N, uint4 *__restrict__ kc, uint4 *__restrict__ vc,
                                 unsigned int *err) {
-    // a following kernel launched as a programmatic dependent may start its
-    // set-up now; it waits for this grid before it reads the caches
+    // Launched as a programmatic dependent: wait for the previous kernel in the
+    // stream (it may still be reading the caches), then let the next one start
+    // its set-up -- it waits for this grid before it reads the caches.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int t = blockIdx.x;
     const int64_t slot = slots[t];
@@ -52,6 +54,7 @@ __global__ void write_kv_kernel(const uint4 *__restrict__ k, const uint4 *__rest
 
 __global__ void copy_blocks_kernel(uint4 *kc, uint4 *vc, const int64_t *__restrict__ pairs,
                                    int64_t chunks, int N, unsigned int *err) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int p = blockIdx.x;
     const int64_t src = pairs[2 * p];
@@ -144,10 +147,18 @@ cudaError_t launch_write_kv(const void *k, const void *v, const int64_t *slots, 
                             int row_bytes, int B, int N, void *k_cache, void *v_cache,
                             unsigned int *err, cudaStream_t st) {
     if (T == 0) return cudaSuccess;
-    write_kv_kernel<<<T, 128, 0, st>>>(static_cast<const uint4 *>(k), static_cast<const uint4 *>(v),
-                                       slots, Hkv, row_bytes / 16, B, N, static_cast<uint4 *>(k_cache),
-                                       static_cast<uint4 *>(v_cache), err);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)T);
+    cfg.blockDim = dim3(128);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, write_kv_kernel, static_cast<const uint4 *>(k), static_cast<const uint4 *>(v),
+                              slots, Hkv, row_bytes / 16, B, N, static_cast<uint4 *>(k_cache),
+                              static_cast<uint4 *>(v_cache), err);
 }
 
 cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, int P,
@@ -158,9 +169,17 @@ cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *pair
     int z = (int)((chunks + threads * 8 - 1) / (threads * 8));  // ~8 vectors per thread
     if (z < 1) z = 1;
     if (z > 64) z = 64;
-    copy_blocks_kernel<<<dim3((unsigned)P, 2, (unsigned)z), threads, 0, st>>>(
-        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), pairs, chunks, N, err);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)P, 2, (unsigned)z);
+    cfg.blockDim = dim3(threads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, copy_blocks_kernel, static_cast<uint4 *>(k_cache),
+                              static_cast<uint4 *>(v_cache), pairs, chunks, N, err);
 }
 
 }  // namespace pa
