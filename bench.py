@@ -29,6 +29,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import re
 import subprocess
@@ -390,6 +391,105 @@ def run_ours(args):
     return line
 
 
+# --------------------------------------------------------------------------- multi-layer step
+def run_layers(args):
+    """One decode step over L layers of a multi-layer pool: a captured step graph
+    (write_kv + decode per layer) against the same launches issued one by one."""
+    import torch
+
+    from paged_kv_cache_127_gb300 import binding as pa
+    from paged_kv_cache_127_gb300 import workloads
+
+    rank, local_rank, world = dist_env()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    dist = dist_init(world, "nccl")
+    L = args.layers
+    step = workloads.build_step(args.workload, seed=rank, binding=pa)
+    if args.num_seqs:
+        step = step.first(args.num_seqs)
+    if args.partition_size:
+        step.partition_size = args.partition_size
+    dims = step.dims(pa)
+    S, Hq, Hkv, D, B, N = (step.num_seqs, step.num_q_heads, step.num_kv_heads, step.head_dim,
+                           step.block_size, step.num_blocks)
+    kvt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[step.dtype]
+
+    def host(x):
+        if step.dtype == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(x))
+
+    gen = torch.Generator(device=device)
+    gen.manual_seed(1234 + rank)
+
+    def layered(first, shape, std):
+        t = torch.empty((L,) + tuple(shape), dtype=kvt, device=device)
+        t[0].copy_(host(first))
+        for layer in range(1, L):
+            t[layer].copy_(torch.randn(shape, generator=gen, device=device) * std)
+        return t
+
+    w_std = 1.0
+    kc = layered(step.k_cache, step.k_cache.shape, w_std)
+    vc = layered(step.v_cache, step.v_cache.shape, w_std)
+    q = layered(step.q, step.q.shape, w_std * (1.0 / math.sqrt(D) if step.name.startswith("gqa8b") else 1.0))
+    kn = layered(step.k_new, step.k_new.shape, w_std)
+    vn = layered(step.v_new, step.v_new.shape, w_std)
+    slots = torch.from_numpy(step.slots).to(device)
+    tables = torch.from_numpy(step.tables).to(device)
+    lens = torch.from_numpy(step.lens).to(device)
+    out = torch.empty((L, S, Hq, D), dtype=torch.float32, device=device)
+    ws = torch.empty(max(pa.pa_decode_workspace_bytes(dims), 256), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    graph = pa.pa_step_graph_create(dims, kc, vc, q, kn, vn, slots, tables, lens, step.scale, out, ws)
+
+    def eager():
+        for layer in range(L):
+            pa.pa_write_kv(dims, kn[layer], vn[layer], slots, kc[layer], vc[layer], stream)
+            pa.pa_decode(dims, q[layer], kc[layer], vc[layer], tables, lens, step.scale, out[layer], ws, stream)
+
+    def timed(fn, n):
+        barrier(dist, device)
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        return reduce_scalar(dist, e0.elapsed_time(e1) / n, "max", device)
+
+    pa.pa_device_errors(clear=True)
+    sampler = ClockSampler(device.index).start() if rank == 0 else None
+    for _ in range(args.warmup):
+        graph.launch(stream)
+        eager()
+    graph_ms = timed(graph.launch, args.steps)
+    eager_ms = timed(eager, max(1, args.steps // 2))
+    clocks = sampler.stop() if sampler else None
+    assert pa.pa_device_errors(clear=True) == 0
+    graph.close()
+    kv_bytes = step.kv_bytes_logical() * L
+    kv_all = reduce_scalar(dist, kv_bytes, "sum", device)
+    if rank != 0:
+        return None
+    return {
+        "metric": METRIC + f" -- one decode step over {L} layers",
+        "value": round(kv_all / (graph_ms / 1e3) / 1e9, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(graph_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": step.dtype,
+        "data": "synthetic (layer 0 from the workload generator, layers 1.. from a seeded device generator)",
+        "config": {"workload": args.workload, "layers": L, "num_seqs": S, "num_q_heads": Hq,
+                   "num_kv_heads": Hkv, "head_dim": D, "block_size": B, "num_blocks_per_layer": N,
+                   "kv_bytes_per_step": kv_bytes},
+        "graph_ms_per_step": round(graph_ms, 4), "eager_ms_per_step": round(eager_ms, 4),
+        "eager_over_graph": round(eager_ms / graph_ms, 3),
+        "gpu_launches": L * (2 + (2 if step.max_blocks * B > step.partition_size else 1)) * args.steps,
+        "clocks": clocks,
+    }
+
+
 # --------------------------------------------------------------------------- reference arm
 def run_reference(args):
     """Time the CPU oracle on host cores: each step one bounded sample of the workload."""
@@ -452,12 +552,21 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--num-seqs", type=int, default=0,
+                    help="with --layers: use only the first K sequences of the workload")
+    ap.add_argument("--layers", type=int, default=1,
+                    help="time one step over this many layers through the captured step graph")
     ap.add_argument("--partition-size", type=int, default=0,
                     help="context tokens per split-K partition (default: the workload's, 512)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if args.impl == "reference":
+        line = run_reference(args)
+    elif args.layers > 1:
+        line = run_layers(args)
+    else:
+        line = run_ours(args)
     if line is not None:
         print(json.dumps(line), flush=True)
     if dist_env()[2] > 1:

@@ -193,6 +193,48 @@ PA_API int32_t pa_copy_blocks(const pa_dims *dims, void *k_cache, void *v_cache,
                        const int64_t *src_dst_pairs, int32_t num_pairs, void *stream);
 
 /*
+ * pa_copy_blocks_layers -- pa_copy_blocks for num_layers caches at once: layer
+ * l's caches start layer_stride_bytes * l after k_caches / v_caches (a
+ * multi-layer pool [L, N, Hkv, B, D]; the block manager's ids are the same in
+ * every layer).  layer_stride_bytes must be a multiple of 16 and at least one
+ * pool (N * Hkv * B * D elements) when num_layers > 1.  One launch for all
+ * layers.  Same preconditions and errors as pa_copy_blocks.
+ */
+PA_API int32_t pa_copy_blocks_layers(const pa_dims *dims, void *k_caches, void *v_caches, int32_t num_layers,
+                                     int64_t layer_stride_bytes, const int64_t *src_dst_pairs, int32_t num_pairs,
+                                     void *stream);
+
+/*
+ * Step graph -- one decode step over num_layers layers, captured once into a
+ * CUDA graph: for l = 0 .. L-1, pa_write_kv then pa_decode of layer l.  Every
+ * pointer is a fixed device buffer read at each launch (update the buffers,
+ * then launch); layer l uses
+ *     k_caches + l * cache_layer_stride      (and v_caches)
+ *     q        + l * q_layer_stride          [S, Hq, D]
+ *     k_new    + l * kv_new_layer_stride     [num_tokens, Hkv, D] (and v_new)
+ *     out      + l * out_layer_stride        [S, Hq, D] fp32
+ * (strides in bytes); slot_mapping, block_tables, context_lens and the
+ * workspace are shared by all layers (layers run in order).  Arguments are
+ * validated as by the two calls; on failure NULL is returned and *status
+ * (nullable) holds the pa_status.  Copy-on-write copies, which are rare and
+ * vary in number, are not in the graph: run pa_copy_blocks_layers first.
+ * Launch with pa_step_graph_launch (asynchronous on `stream`); destroy with
+ * pa_step_graph_destroy.  Creation must not overlap a capture on the calling
+ * thread.
+ */
+typedef struct pa_step_graph pa_step_graph;
+PA_API pa_step_graph *pa_step_graph_create(const pa_dims *dims, int32_t num_layers, void *k_caches,
+                                           void *v_caches, int64_t cache_layer_stride, const void *q,
+                                           int64_t q_layer_stride, const void *k_new, const void *v_new,
+                                           int64_t kv_new_layer_stride, const int64_t *slot_mapping,
+                                           int32_t num_tokens, const int32_t *block_tables,
+                                           const int32_t *context_lens, float scale, float *out,
+                                           int64_t out_layer_stride, void *workspace, size_t workspace_bytes,
+                                           int32_t *status);
+PA_API int32_t pa_step_graph_launch(pa_step_graph *graph, void *stream);
+PA_API void pa_step_graph_destroy(pa_step_graph *graph);
+
+/*
  * pa_device_errors -- read (and, if clear != 0, reset) the sticky PA_DEVERR_*
  * bits of the current device.  Synchronises with the device.
  */

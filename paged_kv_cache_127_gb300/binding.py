@@ -55,6 +55,11 @@ _SIGNATURES = {
     "pa_decode_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
     "pa_write_kv": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp]),
     "pa_copy_blocks": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp]),
+    "pa_copy_blocks_layers": (_i32, [_vp, _vp, _vp, _i32, _i64, _vp, _i32, _vp]),
+    "pa_step_graph_create": (_vp, [_vp, _i32, _vp, _vp, _i64, _vp, _i64, _vp, _vp, _i64, _vp, _i32, _vp, _vp,
+                                   ctypes.c_float, _vp, _i64, _vp, _sz, _vp]),
+    "pa_step_graph_launch": (_i32, [_vp, _vp]),
+    "pa_step_graph_destroy": (None, [_vp]),
     "pa_device_errors": (_i32, [_vp, _i32]),
     "pa_version": (ctypes.c_char_p, []),
     "pa_pool_create": (_vp, [_i32, _i32, _vp]),
@@ -223,6 +228,92 @@ def pa_copy_blocks(dims: pa_dims, k_cache, v_cache, src_dst_pairs, stream=None) 
     st = lib.pa_copy_blocks(ctypes.byref(dims), k_cache.data_ptr(), v_cache.data_ptr(),
                             src_dst_pairs.data_ptr(), P, _stream_ptr(stream, dev))
     _check(st, "pa_copy_blocks")
+
+
+def pa_copy_blocks_layers(dims: pa_dims, k_caches, v_caches, src_dst_pairs, stream=None) -> None:
+    """Copy whole blocks src -> dst in every layer of [L, N, Hkv, B, D] K and V pools."""
+    t = _torch()
+    d, kv = dims, _torch_dtype(dims.kv_dtype)
+    dev = k_caches.device
+    L = int(k_caches.shape[0])
+    P = int(src_dst_pairs.shape[0])
+    pool_shape = (L, d.num_blocks, d.num_kv_heads, d.block_size, d.head_dim)
+    _expect(k_caches, "k_caches", pool_shape, kv, dev)
+    _expect(v_caches, "v_caches", pool_shape, kv, dev)
+    _expect(src_dst_pairs, "src_dst_pairs", (P, 2), t.int64, dev)
+    stride = k_caches.stride(0) * k_caches.element_size()
+    st = lib.pa_copy_blocks_layers(ctypes.byref(dims), k_caches.data_ptr(), v_caches.data_ptr(), L, stride,
+                                   src_dst_pairs.data_ptr(), P, _stream_ptr(stream, dev))
+    _check(st, "pa_copy_blocks_layers")
+
+
+class StepGraph:
+    """pa_step_graph: one L-layer decode step (write_kv + decode per layer) as a CUDA graph.
+
+    All tensors are kept referenced for the graph's lifetime; update their
+    contents in place, then call launch().
+      k_caches, v_caches  [L, N, Hkv, B, D]      q      [L, S, Hq, D]
+      k_new, v_new        [L, T, Hkv, D]         out    [L, S, Hq, D] fp32
+      slot_mapping int64 [T]; block_tables int32 [S, max_blocks]; context_lens int32 [S]
+    """
+
+    def __init__(self, dims: pa_dims, k_caches, v_caches, q, k_new, v_new, slot_mapping, block_tables,
+                 context_lens, scale: float, out, workspace):
+        t = _torch()
+        d, kv = dims, _torch_dtype(dims.kv_dtype)
+        dev = q.device
+        L = int(q.shape[0])
+        T = int(slot_mapping.shape[0])
+        _expect(k_caches, "k_caches", (L, d.num_blocks, d.num_kv_heads, d.block_size, d.head_dim), kv, dev)
+        _expect(v_caches, "v_caches", tuple(k_caches.shape), kv, dev)
+        _expect(q, "q", (L, d.num_seqs, d.num_q_heads, d.head_dim), kv, dev)
+        _expect(k_new, "k_new", (L, T, d.num_kv_heads, d.head_dim), kv, dev)
+        _expect(v_new, "v_new", (L, T, d.num_kv_heads, d.head_dim), kv, dev)
+        _expect(slot_mapping, "slot_mapping", (T,), t.int64, dev)
+        _expect(block_tables, "block_tables", (d.num_seqs, d.max_blocks_per_seq), t.int32, dev)
+        _expect(context_lens, "context_lens", (d.num_seqs,), t.int32, dev)
+        _expect(out, "out", (L, d.num_seqs, d.num_q_heads, d.head_dim), t.float32, dev)
+        if not workspace.is_cuda or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        self._keep = (dims, k_caches, v_caches, q, k_new, v_new, slot_mapping, block_tables, context_lens, out,
+                      workspace)
+        es = k_caches.element_size()
+        status = ctypes.c_int32(0)
+        self.handle = lib.pa_step_graph_create(
+            ctypes.byref(dims), L, k_caches.data_ptr(), v_caches.data_ptr(), k_caches.stride(0) * es,
+            q.data_ptr(), q.stride(0) * es, k_new.data_ptr(), v_new.data_ptr(), k_new.stride(0) * es,
+            slot_mapping.data_ptr(), T, block_tables.data_ptr(), context_lens.data_ptr(), float(scale),
+            out.data_ptr(), out.stride(0) * 4, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+            ctypes.byref(status))
+        if not self.handle:
+            raise PaError(status.value, "pa_step_graph_create")
+        self.device = dev
+
+    def launch(self, stream=None) -> None:
+        _check(lib.pa_step_graph_launch(self.handle, _stream_ptr(stream, self.device)), "pa_step_graph_launch")
+
+    def close(self) -> None:
+        if self.handle:
+            lib.pa_step_graph_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        self.close()
+
+
+def pa_step_graph_create(dims: pa_dims, k_caches, v_caches, q, k_new, v_new, slot_mapping, block_tables,
+                         context_lens, scale: float, out, workspace) -> "StepGraph":
+    """Capture one L-layer decode step; returns the owning StepGraph."""
+    return StepGraph(dims, k_caches, v_caches, q, k_new, v_new, slot_mapping, block_tables, context_lens,
+                     scale, out, workspace)
+
+
+def pa_step_graph_launch(graph: "StepGraph", stream=None) -> None:
+    graph.launch(stream)
+
+
+def pa_step_graph_destroy(graph: "StepGraph") -> None:
+    graph.close()
 
 
 def pa_device_errors(clear: bool = True) -> int:

@@ -244,19 +244,31 @@ int32_t pa_write_kv(const pa_dims *dims, const void *k, const void *v, const int
 
 int32_t pa_copy_blocks(const pa_dims *dims, void *k_cache, void *v_cache, const int64_t *src_dst_pairs,
                        int32_t num_pairs, void *stream) {
+    const int64_t layer_bytes = dims ? (int64_t)dims->num_blocks * dims->num_kv_heads * dims->block_size *
+                                           dims->head_dim * elem_bytes(dims->kv_dtype)
+                                     : 0;
+    return pa_copy_blocks_layers(dims, k_cache, v_cache, 1, layer_bytes, src_dst_pairs, num_pairs, stream);
+}
+
+int32_t pa_copy_blocks_layers(const pa_dims *dims, void *k_caches, void *v_caches, int32_t num_layers,
+                              int64_t layer_stride_bytes, const int64_t *src_dst_pairs, int32_t num_pairs,
+                              void *stream) {
     int32_t rc = check_cache_dims(dims);
     if (rc != PA_OK) return rc;
-    if (num_pairs < 0) return PA_ERR_INVALID;
-    if (num_pairs == 0) return PA_OK;
-    if (!k_cache || !v_cache || !src_dst_pairs || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
-        !aligned(src_dst_pairs, 8))
-        return PA_ERR_INVALID;
-    unsigned int *err = error_word();
-    if (!err) return PA_ERR_CUDA;
+    if (num_pairs < 0 || num_layers < 0 || num_layers > 32768) return PA_ERR_INVALID;
+    if (num_pairs == 0 || num_layers == 0) return PA_OK;
     const int64_t block_bytes =
         (int64_t)dims->num_kv_heads * dims->block_size * dims->head_dim * elem_bytes(dims->kv_dtype);
-    return to_status(pa::launch_copy_blocks(k_cache, v_cache, src_dst_pairs, num_pairs, block_bytes,
-                                            dims->num_blocks, err, static_cast<cudaStream_t>(stream)));
+    const int64_t pool_bytes = block_bytes * dims->num_blocks;
+    if (!k_caches || !v_caches || !src_dst_pairs || !aligned(k_caches, 16) || !aligned(v_caches, 16) ||
+        !aligned(src_dst_pairs, 8))
+        return PA_ERR_INVALID;
+    if (num_layers > 1 && (layer_stride_bytes < pool_bytes || layer_stride_bytes % 16 != 0)) return PA_ERR_INVALID;
+    unsigned int *err = error_word();
+    if (!err) return PA_ERR_CUDA;
+    return to_status(pa::launch_copy_blocks(k_caches, v_caches, src_dst_pairs, num_pairs, block_bytes,
+                                            dims->num_blocks, num_layers, layer_stride_bytes, err,
+                                            static_cast<cudaStream_t>(stream)));
 }
 
 int32_t pa_device_errors(uint32_t *flags, int32_t clear) {

@@ -52,8 +52,9 @@ __global__ void write_kv_kernel(const uint4 *__restrict__ k, const uint4 *__rest
     }
 }
 
+// grid: (pair, 2 * layer + {0: K, 1: V}, slice of the block)
 __global__ void copy_blocks_kernel(uint4 *kc, uint4 *vc, const int64_t *__restrict__ pairs,
-                                   int64_t chunks, int N, unsigned int *err) {
+                                   int64_t chunks, int64_t layer_chunks, int N, unsigned int *err) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int p = blockIdx.x;
@@ -63,7 +64,7 @@ __global__ void copy_blocks_kernel(uint4 *kc, uint4 *vc, const int64_t *__restri
         if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) set_error(err, PA_DEVERR_BAD_PAIR);
         return;
     }
-    uint4 *base = blockIdx.y ? vc : kc;
+    uint4 *base = ((blockIdx.y & 1) ? vc : kc) + (int64_t)(blockIdx.y >> 1) * layer_chunks;
     const uint4 *from = base + src * chunks;
     uint4 *to = base + dst * chunks;
     for (int64_t i = threadIdx.x + (int64_t)blockIdx.z * blockDim.x; i < chunks;
@@ -162,15 +163,16 @@ cudaError_t launch_write_kv(const void *k, const void *v, const int64_t *slots, 
 }
 
 cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, int P,
-                               int64_t block_bytes, int N, unsigned int *err, cudaStream_t st) {
-    if (P == 0) return cudaSuccess;
+                               int64_t block_bytes, int N, int layers, int64_t layer_bytes, unsigned int *err,
+                               cudaStream_t st) {
+    if (P == 0 || layers == 0) return cudaSuccess;
     const int64_t chunks = block_bytes / 16;
     const int threads = 256;
     int z = (int)((chunks + threads * 8 - 1) / (threads * 8));  // ~8 vectors per thread
     if (z < 1) z = 1;
     if (z > 64) z = 64;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)P, 2, (unsigned)z);
+    cfg.gridDim = dim3((unsigned)P, 2u * (unsigned)layers, (unsigned)z);
     cfg.blockDim = dim3(threads);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -179,7 +181,7 @@ cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *pair
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, copy_blocks_kernel, static_cast<uint4 *>(k_cache),
-                              static_cast<uint4 *>(v_cache), pairs, chunks, N, err);
+                              static_cast<uint4 *>(v_cache), pairs, chunks, layer_bytes / 16, N, err);
 }
 
 }  // namespace pa

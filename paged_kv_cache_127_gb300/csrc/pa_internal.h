@@ -72,7 +72,9 @@ cudaError_t launch_write_kv(const void *k, const void *v, const int64_t *slots, 
                             int row_bytes, int B, int N, void *k_cache, void *v_cache,
                             unsigned int *err, cudaStream_t st);
 
+// Copy whole blocks for `layers` caches laid out layer_bytes apart (K and V).
 cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *pairs, int P,
-                               int64_t block_bytes, int N, unsigned int *err, cudaStream_t st);
+                               int64_t block_bytes, int N, int layers, int64_t layer_bytes, unsigned int *err,
+                               cudaStream_t st);
 
 }  // namespace pa

@@ -68,6 +68,15 @@ class DecodeStep:
                     total += min(B, n - j * B)
         return total * self.kv_bytes_per_token()
 
+    def first(self, k: int) -> "DecodeStep":
+        """The same step restricted to the first k sequences (pool unchanged)."""
+        import copy
+        sub = copy.copy(self)
+        sub.tables, sub.lens, sub.slots = self.tables[:k], self.lens[:k], self.slots[:k]
+        if self.q is not None:
+            sub.q, sub.k_new, sub.v_new = self.q[:k], self.k_new[:k], self.v_new[:k]
+        return sub
+
     def dims(self, binding):
         return binding.make_dims(self.num_seqs, self.num_q_heads, self.num_kv_heads, self.head_dim,
                                  self.block_size, self.num_blocks, self.max_blocks, self.partition_size,
