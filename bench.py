@@ -490,6 +490,68 @@ def run_layers(args):
     }
 
 
+# --------------------------------------------------------------------------- block swap
+def run_swap(args):
+    """Swap-out / swap-in bandwidth: N whole blocks (all KV heads, K and V)
+    between the device pool and pinned host memory, one pa_swap_blocks call per
+    direction per step."""
+    import torch
+
+    from paged_kv_cache_127_gb300 import binding as pa
+    from paged_kv_cache_127_gb300 import synth
+
+    rank, local_rank, world = dist_env()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    w = synth.workload(args.workload)
+    nb = args.swap_blocks
+    N = 2 * nb
+    dims = pa.make_dims(0, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, N, 1, 0, w.dtype)
+    kvt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[w.dtype]
+    shape = (N, w.num_kv_heads, w.block_size, w.head_dim)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(99 + rank)
+    kc = torch.randn(shape, generator=gen, device=device).to(kvt)
+    vc = torch.randn(shape, generator=gen, device=device).to(kvt)
+    hk = torch.empty((nb,) + shape[1:], dtype=kvt).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    rng = np.random.default_rng(5 + rank)
+    dev_ids = rng.permutation(N)[:nb]
+    out_pairs = torch.from_numpy(np.stack([dev_ids, rng.permutation(nb)], 1).astype(np.int64)).to(device)
+    in_pairs = torch.from_numpy(np.stack([out_pairs[:, 1].cpu().numpy(), rng.permutation(N)[:nb]], 1)
+                                .astype(np.int64)).to(device)
+    stream = torch.cuda.current_stream(device)
+    block_bytes = 2 * w.num_kv_heads * w.block_size * w.head_dim * synth.ELEM_BYTES[w.dtype]
+
+    def timed(direction, pairs, n):
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            pa.pa_swap_blocks(dims, kc, vc, hk, hv, pairs, direction, stream)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        return e0.elapsed_time(e1) / n
+
+    for _ in range(args.warmup):
+        pa.pa_swap_blocks(dims, kc, vc, hk, hv, out_pairs, pa.PA_SWAP_OUT, stream)
+        pa.pa_swap_blocks(dims, kc, vc, hk, hv, in_pairs, pa.PA_SWAP_IN, stream)
+    out_ms = timed(pa.PA_SWAP_OUT, out_pairs, args.steps)
+    in_ms = timed(pa.PA_SWAP_IN, in_pairs, args.steps)
+    assert pa.pa_device_errors(clear=True) == 0
+    if rank != 0:
+        return None
+    total = nb * block_bytes
+    return {"metric": "block swap GB/s (device pool <-> pinned host memory)", "unit": "GB/s",
+            "value": round(total / (out_ms / 1e3) / 1e9, 1), "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True,
+            "config": {"workload": args.workload, "blocks": nb, "bytes_per_block": block_bytes,
+                       "bytes_per_call": total},
+            "swap_out_gbs": round(total / (out_ms / 1e3) / 1e9, 1), "swap_out_ms": round(out_ms, 4),
+            "swap_in_gbs": round(total / (in_ms / 1e3) / 1e9, 1), "swap_in_ms": round(in_ms, 4),
+            "gpu_launches": 2 * args.steps}
+
+
 # --------------------------------------------------------------------------- reference arm
 def run_reference(args):
     """Time the CPU oracle on host cores: each step one bounded sample of the workload."""
@@ -554,6 +616,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--num-seqs", type=int, default=0,
                     help="with --layers: use only the first K sequences of the workload")
+    ap.add_argument("--swap-blocks", type=int, default=0,
+                    help="measure block swap bandwidth for this many blocks instead")
     ap.add_argument("--layers", type=int, default=1,
                     help="time one step over this many layers through the captured step graph")
     ap.add_argument("--partition-size", type=int, default=0,
@@ -563,6 +627,8 @@ def main(argv=None):
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         line = run_reference(args)
+    elif args.swap_blocks > 0:
+        line = run_swap(args)
     elif args.layers > 1:
         line = run_layers(args)
     else:

@@ -235,6 +235,32 @@ PA_API int32_t pa_step_graph_launch(pa_step_graph *graph, void *stream);
 PA_API void pa_step_graph_destroy(pa_step_graph *graph);
 
 /*
+ * pa_swap_blocks -- block-granular swap between the device pools and a host
+ * pool, for preempting a sequence (its blocks move to host memory, the device
+ * blocks are reused) and resuming it later.  ("Paged Attention and vLLM",
+ * "Continuous Batching and Scheduler": evict a sequence's physical blocks to
+ * CPU, swap them back on resume, paying only for those blocks.)
+ *
+ *   host_k, host_v    [num_layers][num_host_blocks, Hkv, B, D] kv_dtype in host
+ *                     memory the GPU can access directly (pinned or registered,
+ *                     e.g. cudaHostAlloc); anything else gives PA_ERR_INVALID
+ *   pairs             int64 [num_pairs, 2], device: PA_SWAP_OUT copies device
+ *                     block pairs[i][0] to host block pairs[i][1]; PA_SWAP_IN
+ *                     copies host block pairs[i][0] to device block pairs[i][1]
+ *   strides           bytes between layers (used when num_layers > 1)
+ * One kernel moves every pair of every layer, K and V, with the GPU reading
+ * and writing host memory directly; bit-exact.  Ids outside the pools are
+ * skipped and flagged (PA_DEVERR_BAD_PAIR).  Destinations must be distinct.
+ * pa_seq_swap_out / pa_seq_swap_in produce the pairs.
+ */
+#define PA_SWAP_OUT 0
+#define PA_SWAP_IN 1
+PA_API int32_t pa_swap_blocks(const pa_dims *dims, void *k_cache, void *v_cache, void *host_k, void *host_v,
+                              int32_t num_host_blocks, int32_t num_layers, int64_t dev_layer_stride_bytes,
+                              int64_t host_layer_stride_bytes, const int64_t *pairs, int32_t num_pairs,
+                              int32_t direction, void *stream);
+
+/*
  * pa_device_errors -- read (and, if clear != 0, reset) the sticky PA_DEVERR_*
  * bits of the current device.  Synchronises with the device.
  */
@@ -338,6 +364,29 @@ PA_API int32_t pa_pool_export(const pa_pool *pool, const int32_t *seqs, int32_t 
 PA_API int32_t pa_pool_num_free(const pa_pool *pool);
 PA_API int32_t pa_block_refcount(const pa_pool *pool, int32_t block);   /* -PA_ERR_BAD_INDEX if bad id */
 PA_API int32_t pa_pool_get_stats(const pa_pool *pool, pa_pool_stats *out);
+
+/*
+ * Swap a sequence out of the device pool `dev` into the host-slot pool `host`
+ * (a second pa_pool of the same block size whose block ids index the host
+ * KV pool).  Every block of the sequence gets a private host block (shared
+ * prefix blocks are duplicated on the host, not shared there); the pairs
+ * (device block, host block) are written to pairs_out[2 * n] in table order;
+ * the device sequence is then freed (blocks other sequences still use stay).
+ * *host_seq receives the sequence's id in `host`.  Run pa_swap_blocks
+ * (PA_SWAP_OUT) on the pairs before any kernel writes to a freed device block.
+ * All-or-nothing: PA_ERR_OOM if the host pool is short, nothing changed.
+ */
+PA_API int32_t pa_seq_swap_out(pa_pool *dev, pa_pool *host, int32_t seq, int32_t *host_seq, int64_t *pairs_out,
+                               int32_t *n_pairs);
+
+/*
+ * Swap a host sequence back in: fresh private device blocks, pairs (host
+ * block, device block) in table order, the host sequence freed; *dev_seq gets
+ * the new device id.  Run pa_swap_blocks (PA_SWAP_IN) before the sequence's
+ * next decode.  All-or-nothing: PA_ERR_OOM if the device pool is short.
+ */
+PA_API int32_t pa_seq_swap_in(pa_pool *dev, pa_pool *host, int32_t host_seq, int32_t *dev_seq, int64_t *pairs_out,
+                              int32_t *n_pairs);
 
 /*
  * Fault injection for tests: let only n more block allocations succeed; any

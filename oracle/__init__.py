@@ -42,8 +42,10 @@ def _load():
         lib.pa_oracle_copy_blocks.argtypes = [i32] * 5 + [vp] * 3 + [i32]
         lib.pa_oracle_slot_mapping.argtypes = [i32, vp, i32, i32, vp, vp, vp]
         lib.pa_oracle_slot.argtypes = [vp, i32, i32, ctypes.POINTER(i64)]
+        lib.pa_oracle_swap_blocks.argtypes = [i32] * 4 + [vp, vp, i32, vp, vp, i32, vp, i32]
         for f in (lib.pa_oracle_decode, lib.pa_oracle_decode_partitioned, lib.pa_oracle_write_kv,
-                  lib.pa_oracle_copy_blocks, lib.pa_oracle_slot_mapping, lib.pa_oracle_slot):
+                  lib.pa_oracle_copy_blocks, lib.pa_oracle_slot_mapping, lib.pa_oracle_slot,
+                  lib.pa_oracle_swap_blocks):
             f.restype = i32
         _lib = lib
     return _lib
@@ -128,6 +130,22 @@ def copy_blocks(k_cache, v_cache, pairs, dtype: str) -> None:
                                        _ptr(v_cache), _ptr(pairs), pairs.shape[0])
     if rc:
         raise ValueError("oracle copy_blocks: block id out of range")
+
+
+def swap_blocks(from_k, from_v, to_k, to_v, pairs, dtype: str) -> None:
+    """In place: to[dst] = from[src] (whole blocks, K and V) for each (src, dst) pair."""
+    for c in (from_k, from_v, to_k, to_v):
+        if c.dtype != _STORAGE[dtype] or not c.flags.c_contiguous:
+            raise TypeError("pools must be contiguous arrays of the storage dtype")
+    pairs = np.ascontiguousarray(np.asarray(pairs, dtype=np.int64).reshape(-1, 2))
+    Nf, Hkv, B, D = from_k.shape
+    Nt = to_k.shape[0]
+    if to_k.shape[1:] != from_k.shape[1:] or from_v.shape != from_k.shape or to_v.shape != to_k.shape:
+        raise ValueError("pool shapes differ")
+    rc = _load().pa_oracle_swap_blocks(Hkv, D, B, DTYPE_CODE[dtype], _ptr(from_k), _ptr(from_v), Nf, _ptr(to_k),
+                                       _ptr(to_v), Nt, _ptr(pairs), pairs.shape[0])
+    if rc:
+        raise ValueError("oracle swap_blocks: block id out of range")
 
 
 def slot_mapping(tables, block_size: int, seq_of, positions) -> np.ndarray:

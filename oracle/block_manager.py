@@ -33,7 +33,12 @@ Readings where the pages leave the policy open:
   next belongs to a scheduler ("Growing a request", last paragraph);
 * within one append, the copy-on-write block is allocated before any new
   growth block;
-* sequence ids are handed out 0, 1, 2, ... and never reused.
+* sequence ids are handed out 0, 1, 2, ... and never reused;
+* swapping a sequence out ("Paged Attention and vLLM", "Continuous Batching
+  and Scheduler": evict its physical blocks to CPU, bring them back later)
+  gives every table entry a private host block -- blocks it shared stay with
+  their other users on the device and are duplicated on the host -- and
+  swapping in gives every entry a fresh private device block.
 """
 from __future__ import annotations
 
@@ -134,6 +139,40 @@ class BlockManager:
         s = self.seqs.pop(sid)
         for b in s.table:
             self._release(b)
+
+    # -- preemption: swap a sequence to another pool and back ---------------------
+    def swap_out(self, sid: int, host: "BlockManager"):
+        """Move sequence `sid` into `host`: a private host block per table entry,
+        then release the device sequence.  Returns (host id, [(device, host)]).
+        All-or-nothing: OutOfBlocks if `host` is short."""
+        s = self.seqs[sid]
+        if len(s.table) > len(host.free) or (host._fail_budget is not None and len(s.table) > host._fail_budget):
+            raise OutOfBlocks("host pool too small")
+        hid = host.create()
+        pairs = []
+        for b in s.table:
+            hb = host._alloc()
+            host.seqs[hid].table.append(hb)
+            pairs.append((b, hb))
+        host.seqs[hid].length = s.length
+        self.free_seq(sid)
+        return hid, pairs
+
+    def swap_in(self, hid: int, host: "BlockManager"):
+        """Move host sequence `hid` back: fresh private blocks here, then release
+        it in `host`.  Returns (new id, [(host, device)])."""
+        hs = host.seqs[hid]
+        if len(hs.table) > len(self.free) or (self._fail_budget is not None and len(hs.table) > self._fail_budget):
+            raise OutOfBlocks("device pool too small")
+        sid = self.create()
+        pairs = []
+        for hb in hs.table:
+            b = self._alloc()
+            self.seqs[sid].table.append(b)
+            pairs.append((hb, b))
+        self.seqs[sid].length = hs.length
+        host.free_seq(hid)
+        return sid, pairs
 
     # -- queries ----------------------------------------------------------------
     def table(self, sid: int) -> list:

@@ -41,6 +41,11 @@
  *    all B slots, keys and values).  (Same section; "Paged Attention and vLLM",
  *    "Continuous Batching and Scheduler", the copy-on-write rule.)
  *
+ *  - Block swap: the same whole-block copy between two pools (device blocks to
+ *    host blocks and back), for preemption ("Paged Attention and vLLM",
+ *    "Continuous Batching and Scheduler": evict a sequence's physical blocks to
+ *    CPU and swap them back later).
+ *
  * Readings where the pages are silent (each is also listed in the design notes):
  *  - the query-head to KV-head map is consecutive grouping: kv = h / (Hq/Hkv);
  *  - ctx_len == 0 gives an all-zero output;
@@ -352,6 +357,22 @@ int pa_oracle_copy_blocks(int Hkv, int D, int B, int N, int dtype,
             return -1;
         memmove((char *)k_cache + (size_t)dst * blk, (const char *)k_cache + (size_t)src * blk, blk);
         memmove((char *)v_cache + (size_t)dst * blk, (const char *)v_cache + (size_t)src * blk, blk);
+    }
+    return 0;
+}
+
+/* ---- block swap between two pools: whole-block copy for each (src, dst) pair */
+
+int pa_oracle_swap_blocks(int Hkv, int D, int B, int dtype, const void *from_k, const void *from_v, int from_n,
+                          void *to_k, void *to_v, int to_n, const int64_t *pairs, int P)
+{
+    const size_t blk = (size_t)Hkv * B * D * elem_size(dtype);
+    for (int p = 0; p < P; ++p) {
+        const int64_t src = pairs[2 * p], dst = pairs[2 * p + 1];
+        if (src < 0 || src >= from_n || dst < 0 || dst >= to_n)
+            return -1;
+        memcpy((char *)to_k + (size_t)dst * blk, (const char *)from_k + (size_t)src * blk, blk);
+        memcpy((char *)to_v + (size_t)dst * blk, (const char *)from_v + (size_t)src * blk, blk);
     }
     return 0;
 }

@@ -22,6 +22,7 @@ PA_F32, PA_F16, PA_BF16 = 0, 1, 2
 DTYPE_CODES = {"f32": PA_F32, "f16": PA_F16, "bf16": PA_BF16}
 STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_OOM",
                 4: "PA_ERR_BAD_INDEX", 5: "PA_ERR_CUDA", 6: "PA_ERR_TOO_LARGE"}
+PA_SWAP_OUT, PA_SWAP_IN = 0, 1
 PA_DEVERR_BAD_BLOCK, PA_DEVERR_BAD_LEN, PA_DEVERR_BAD_SLOT, PA_DEVERR_BAD_PAIR, PA_DEVERR_TIMEOUT = (
     1, 2, 4, 8, 16)
 
@@ -76,6 +77,9 @@ _SIGNATURES = {
     "pa_block_refcount": (_i32, [_vp, _i32]),
     "pa_pool_get_stats": (_i32, [_vp, _vp]),
     "pa_pool_set_fail_after": (_i32, [_vp, _i32]),
+    "pa_swap_blocks": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i64, _i64, _vp, _i32, _i32, _vp]),
+    "pa_seq_swap_out": (_i32, [_vp, _vp, _i32, _vp, _vp, _vp]),
+    "pa_seq_swap_in": (_i32, [_vp, _vp, _i32, _vp, _vp, _vp]),
 }
 
 
@@ -314,6 +318,58 @@ def pa_step_graph_launch(graph: "StepGraph", stream=None) -> None:
 
 def pa_step_graph_destroy(graph: "StepGraph") -> None:
     graph.close()
+
+
+def pa_swap_blocks(dims: pa_dims, k_cache, v_cache, host_k, host_v, pairs, direction: int, stream=None) -> None:
+    """Move whole blocks device -> host (PA_SWAP_OUT) or host -> device (PA_SWAP_IN).
+
+    Device caches [N, Hkv, B, D] or [L, N, Hkv, B, D]; host pools the same with
+    their own block count, in pinned host memory (e.g. torch pin_memory=True)."""
+    t = _torch()
+    d, kv = dims, _torch_dtype(dims.kv_dtype)
+    dev = k_cache.device
+    layered = k_cache.dim() == 5
+    L = int(k_cache.shape[0]) if layered else 1
+    tail = (d.num_kv_heads, d.block_size, d.head_dim)
+    _expect(k_cache, "k_cache", ((L,) if layered else ()) + (d.num_blocks,) + tail, kv, dev)
+    _expect(v_cache, "v_cache", tuple(k_cache.shape), kv, dev)
+    nh = int(host_k.shape[1] if layered else host_k.shape[0])
+    for name, h in (("host_k", host_k), ("host_v", host_v)):
+        if h.is_cuda or not h.is_pinned() or not h.is_contiguous() or h.dtype != kv:
+            raise ValueError(f"{name} must be a contiguous pinned host tensor of the cache dtype")
+        if tuple(h.shape) != ((L,) if layered else ()) + (nh,) + tail:
+            raise ValueError(f"{name} has shape {tuple(h.shape)}")
+    P = int(pairs.shape[0])
+    _expect(pairs, "pairs", (P, 2), t.int64, dev)
+    es = k_cache.element_size()
+    dstride = k_cache.stride(0) * es if layered else 0
+    hstride = host_k.stride(0) * es if layered else 0
+    _check(lib.pa_swap_blocks(ctypes.byref(dims), k_cache.data_ptr(), v_cache.data_ptr(), host_k.data_ptr(),
+                              host_v.data_ptr(), nh, L, dstride, hstride, pairs.data_ptr(), P, int(direction),
+                              _stream_ptr(stream, dev)), "pa_swap_blocks")
+
+
+def _swap_seq(fn, dev_pool, host_pool, seq, name):
+    # the sequence's table length bounds the pairs; ask the pool that owns it
+    owner = dev_pool if name == "pa_seq_swap_out" else host_pool
+    nb = lib.pa_seq_table(owner, seq, None, 0)
+    if nb < 0:
+        raise PaError(-nb, name)
+    pairs = np.empty((max(nb, 1), 2), dtype=np.int64)
+    out_id = ctypes.c_int32(0)
+    npairs = ctypes.c_int32(0)
+    _check(fn(dev_pool, host_pool, seq, ctypes.byref(out_id), _np_ptr(pairs), ctypes.byref(npairs)), name)
+    return out_id.value, pairs[:npairs.value].copy()
+
+
+def pa_seq_swap_out(dev_pool, host_pool, seq: int):
+    """Returns (host sequence id, pairs int64 [n, 2] of (device block, host block))."""
+    return _swap_seq(lib.pa_seq_swap_out, dev_pool, host_pool, seq, "pa_seq_swap_out")
+
+
+def pa_seq_swap_in(dev_pool, host_pool, host_seq: int):
+    """Returns (device sequence id, pairs int64 [n, 2] of (host block, device block))."""
+    return _swap_seq(lib.pa_seq_swap_in, dev_pool, host_pool, host_seq, "pa_seq_swap_in")
 
 
 def pa_device_errors(clear: bool = True) -> int:

@@ -284,6 +284,53 @@ int32_t pa_pool_get_stats(const pa_pool *pool, pa_pool_stats *out) {
     return PA_OK;
 }
 
+int32_t pa_seq_swap_out(pa_pool *dev, pa_pool *host, int32_t seq, int32_t *host_seq, int64_t *pairs_out,
+                        int32_t *n_pairs) {
+    if (!dev || !host || !host_seq || !n_pairs || dev == host || dev->B != host->B) return PA_ERR_INVALID;
+    if (!valid_seq(dev, seq)) return PA_ERR_BAD_INDEX;
+    const pa_seq_rec &s = dev->seqs[seq];
+    const int64_t nb = (int64_t)s.table.size();
+    if (nb > 0 && !pairs_out) return PA_ERR_INVALID;
+    if (nb > available(host)) return PA_ERR_OOM;
+    // host copy of the sequence: one private host slot per block, same length
+    const int32_t h = pa_seq_create(host);
+    pa_seq_rec &hs = host->seqs[h];
+    for (int64_t j = 0; j < nb; ++j) {
+        const int32_t hb = take_block(host);
+        hs.table.push_back(hb);
+        pairs_out[2 * j] = s.table[j];
+        pairs_out[2 * j + 1] = hb;
+    }
+    hs.len = s.len;
+    *host_seq = h;
+    *n_pairs = (int32_t)nb;
+    pa_seq_free(dev, seq);  // blocks still used by other sequences stay on the device
+    return PA_OK;
+}
+
+int32_t pa_seq_swap_in(pa_pool *dev, pa_pool *host, int32_t host_seq, int32_t *dev_seq, int64_t *pairs_out,
+                       int32_t *n_pairs) {
+    if (!dev || !host || !dev_seq || !n_pairs || dev == host || dev->B != host->B) return PA_ERR_INVALID;
+    if (!valid_seq(host, host_seq)) return PA_ERR_BAD_INDEX;
+    const pa_seq_rec &hs = host->seqs[host_seq];
+    const int64_t nb = (int64_t)hs.table.size();
+    if (nb > 0 && !pairs_out) return PA_ERR_INVALID;
+    if (nb > available(dev)) return PA_ERR_OOM;
+    const int32_t d = pa_seq_create(dev);
+    pa_seq_rec &ds = dev->seqs[d];
+    for (int64_t j = 0; j < nb; ++j) {
+        const int32_t db = take_block(dev);
+        ds.table.push_back(db);
+        pairs_out[2 * j] = hs.table[j];
+        pairs_out[2 * j + 1] = db;
+    }
+    ds.len = hs.len;
+    *dev_seq = d;
+    *n_pairs = (int32_t)nb;
+    pa_seq_free(host, host_seq);
+    return PA_OK;
+}
+
 int32_t pa_pool_set_fail_after(pa_pool *pool, int32_t n) {
     if (!pool) return PA_ERR_INVALID;
     pool->fail_budget = n < 0 ? -1 : n;

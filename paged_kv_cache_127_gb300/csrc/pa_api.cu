@@ -271,6 +271,53 @@ int32_t pa_copy_blocks_layers(const pa_dims *dims, void *k_caches, void *v_cache
                                             static_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+// The device-side address of host memory the GPU can access directly (pinned
+// or registered), or nullptr.
+void *device_alias_of_host(void *p) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (at.type != cudaMemoryTypeHost) return nullptr;
+    return at.devicePointer;
+}
+}  // namespace
+
+int32_t pa_swap_blocks(const pa_dims *dims, void *k_cache, void *v_cache, void *host_k, void *host_v,
+                       int32_t num_host_blocks, int32_t num_layers, int64_t dev_layer_stride_bytes,
+                       int64_t host_layer_stride_bytes, const int64_t *pairs, int32_t num_pairs, int32_t direction,
+                       void *stream) {
+    int32_t rc = check_cache_dims(dims);
+    if (rc != PA_OK) return rc;
+    if (num_pairs < 0 || num_layers < 0 || num_layers > 32768 || num_host_blocks <= 0 ||
+        (direction != PA_SWAP_OUT && direction != PA_SWAP_IN))
+        return PA_ERR_INVALID;
+    if (num_pairs == 0 || num_layers == 0) return PA_OK;
+    const int64_t block_bytes =
+        (int64_t)dims->num_kv_heads * dims->block_size * dims->head_dim * elem_bytes(dims->kv_dtype);
+    if (!k_cache || !v_cache || !host_k || !host_v || !pairs || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(host_k, 16) || !aligned(host_v, 16) || !aligned(pairs, 8))
+        return PA_ERR_INVALID;
+    if (num_layers > 1 && (dev_layer_stride_bytes < block_bytes * dims->num_blocks || dev_layer_stride_bytes % 16 ||
+                           host_layer_stride_bytes < block_bytes * num_host_blocks || host_layer_stride_bytes % 16))
+        return PA_ERR_INVALID;
+    void *hk = device_alias_of_host(host_k);
+    void *hv = device_alias_of_host(host_v);
+    if (!hk || !hv) return PA_ERR_INVALID;  // not pinned / registered host memory
+    unsigned int *err = error_word();
+    if (!err) return PA_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (direction == PA_SWAP_OUT)
+        return to_status(pa::launch_swap_blocks(k_cache, v_cache, hk, hv, pairs, num_pairs, block_bytes, num_layers,
+                                                dev_layer_stride_bytes, host_layer_stride_bytes, dims->num_blocks,
+                                                num_host_blocks, err, st));
+    return to_status(pa::launch_swap_blocks(hk, hv, k_cache, v_cache, pairs, num_pairs, block_bytes, num_layers,
+                                            host_layer_stride_bytes, dev_layer_stride_bytes, num_host_blocks,
+                                            dims->num_blocks, err, st));
+}
+
 int32_t pa_device_errors(uint32_t *flags, int32_t clear) {
     if (!flags) return PA_ERR_INVALID;
     unsigned int v = 0;

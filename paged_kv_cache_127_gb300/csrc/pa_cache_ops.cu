@@ -72,6 +72,54 @@ __global__ void copy_blocks_kernel(uint4 *kc, uint4 *vc, const int64_t *__restri
         to[i] = from[i];
 }
 
+// Block swap between a device pool and a host pool (pinned host memory the
+// GPU reads and writes directly over the CPU-GPU link).  grid: (pair,
+// 2 * layer + {0: K, 1: V}, slice).  pairs[i] = (source block, destination
+// block) in the direction's (from, to) pools.
+__global__ void swap_blocks_kernel(const uint4 *from_k, const uint4 *from_v, uint4 *to_k, uint4 *to_v,
+                                   const int64_t *__restrict__ pairs, int64_t chunks, int64_t from_layer,
+                                   int64_t to_layer, int from_n, int to_n, unsigned int *err) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int p = blockIdx.x;
+    const int64_t src = pairs[2 * p];
+    const int64_t dst = pairs[2 * p + 1];
+    if (src < 0 || src >= from_n || dst < 0 || dst >= to_n) {
+        if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) set_error(err, PA_DEVERR_BAD_PAIR);
+        return;
+    }
+    const int64_t layer = blockIdx.y >> 1;
+    const uint4 *from = ((blockIdx.y & 1) ? from_v : from_k) + layer * from_layer + src * chunks;
+    uint4 *to = ((blockIdx.y & 1) ? to_v : to_k) + layer * to_layer + dst * chunks;
+    for (int64_t i = threadIdx.x + (int64_t)blockIdx.z * blockDim.x; i < chunks;
+         i += (int64_t)blockDim.x * gridDim.z)
+        to[i] = from[i];
+}
+
+cudaError_t launch_swap_blocks(const void *from_k, const void *from_v, void *to_k, void *to_v,
+                               const int64_t *pairs, int P, int64_t block_bytes, int layers, int64_t from_layer_bytes,
+                               int64_t to_layer_bytes, int from_n, int to_n, unsigned int *err, cudaStream_t st) {
+    if (P == 0 || layers == 0) return cudaSuccess;
+    const int64_t chunks = block_bytes / 16;
+    const int threads = 256;
+    int z = (int)((chunks + threads * 8 - 1) / (threads * 8));
+    if (z < 1) z = 1;
+    if (z > 64) z = 64;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)P, 2u * (unsigned)layers, (unsigned)z);
+    cfg.blockDim = dim3(threads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, swap_blocks_kernel, static_cast<const uint4 *>(from_k),
+                              static_cast<const uint4 *>(from_v), static_cast<uint4 *>(to_k),
+                              static_cast<uint4 *>(to_v), pairs, chunks, from_layer_bytes / 16, to_layer_bytes / 16,
+                              from_n, to_n, err);
+}
+
 // One warp per (sequence, query head); lane i owns D/32 consecutive outputs.
 // Partials are read kU partitions per round trip.  The kernel may be launched
 // as a programmatic dependent of the decode kernel: it waits for that grid

@@ -77,4 +77,9 @@ cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int64_t *pair
                                int64_t block_bytes, int N, int layers, int64_t layer_bytes, unsigned int *err,
                                cudaStream_t st);
 
+// Copy whole blocks between two pools (device <-> pinned host), `layers` deep.
+cudaError_t launch_swap_blocks(const void *from_k, const void *from_v, void *to_k, void *to_v,
+                               const int64_t *pairs, int P, int64_t block_bytes, int layers, int64_t from_layer_bytes,
+                               int64_t to_layer_bytes, int from_n, int to_n, unsigned int *err, cudaStream_t st);
+
 }  // namespace pa

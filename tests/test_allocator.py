@@ -225,3 +225,85 @@ def _run_stream(pa, seed, num_blocks, B, steps, batch):
                                                       (3, 300, 32, True), (4, 12, 1, True)])
 def test_matches_block_manager_oracle(pa, seed, num_blocks, B, batch):
     assert _run_stream(pa, seed, num_blocks, B, 1500, batch) == 1500
+
+
+def test_swap_matches_block_manager_oracle(pa):
+    """Random create / fork / append / free / swap-out / swap-in streams on a device
+    pool and a host pool: the C++ pools and the oracle model agree exactly."""
+    rng = synth.make_rng(77)
+    B = 8
+    order_d = synth.free_order(rng, 60)
+    order_h = synth.free_order(rng, 40)
+    bd, bh = BlockManager(60, B, order_d), BlockManager(40, B, order_h)
+    pd, ph = pa.Pool(60, B, order_d), pa.Pool(40, B, order_h)
+    live, swapped = [], []
+    for _ in range(2000):
+        op = int(rng.integers(0, 8))
+        if op == 0 or not live:
+            a, b = bd.create(), pa.pa_seq_create(pd.handle)
+            assert a == b
+            live.append(a)
+        elif op == 1:
+            par = live[int(rng.integers(len(live)))]
+            a, b = bd.fork(par), pa.pa_seq_fork(pd.handle, par)
+            assert a == b
+            live.append(a)
+        elif op == 2:
+            s = live.pop(int(rng.integers(len(live))))
+            bd.free_seq(s)
+            pa.pa_seq_free(pd.handle, s)
+        elif op == 3:
+            s = live[int(rng.integers(len(live)))]
+            try:
+                want = bd.swap_out(s, bh)
+            except OutOfBlocks:
+                want = None
+            try:
+                hid, pairs = pa.pa_seq_swap_out(pd.handle, ph.handle, s)
+                got = (hid, [tuple(x) for x in pairs.tolist()])
+            except pa.PaError as e:
+                assert e.status == pa.PA_ERR_OOM
+                got = None
+            assert got == want
+            if got:
+                live.remove(s)
+                swapped.append(got[0])
+        elif op == 4 and swapped:
+            h = swapped[int(rng.integers(len(swapped)))]
+            try:
+                want = bd.swap_in(h, bh)
+            except OutOfBlocks:
+                want = None
+            try:
+                sid, pairs = pa.pa_seq_swap_in(pd.handle, ph.handle, h)
+                got = (sid, [tuple(x) for x in pairs.tolist()])
+            except pa.PaError as e:
+                assert e.status == pa.PA_ERR_OOM
+                got = None
+            assert got == want
+            if got:
+                swapped.remove(h)
+                live.append(got[0])
+        else:
+            s = live[int(rng.integers(len(live)))]
+            n = int(rng.integers(0, 2 * B + 3))
+            try:
+                want = bd.append(s, n)
+            except OutOfBlocks:
+                want = None
+            try:
+                slots, pairs = pa.pa_seq_append(pd.handle, s, n)
+                got = (slots.tolist(), [tuple(x) for x in pairs.tolist()])
+            except pa.PaError as e:
+                assert e.status == pa.PA_ERR_OOM
+                got = None
+            assert got == want
+        for s in live:
+            assert pa.pa_seq_table(pd.handle, s).tolist() == bd.table(s)
+        for h in swapped:
+            assert pa.pa_seq_table(ph.handle, h).tolist() == bh.table(h)
+            assert pa.pa_seq_len(ph.handle, h) == bh.length(h)
+        assert pa.pa_pool_num_free(pd.handle) == bd.num_free()
+        assert pa.pa_pool_num_free(ph.handle) == bh.num_free()
+    pd.close()
+    ph.close()

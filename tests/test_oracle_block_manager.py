@@ -136,3 +136,39 @@ def test_random_operations_keep_the_invariants():
                 counts[x] += 1
         assert counts == bm.ref
         assert sorted(bm.free) == [x for x in range(200) if counts[x] == 0]
+
+
+def test_swap_out_and_in_keeps_tables_and_sharing_rules():
+    dev = BlockManager(12, 4)
+    host = BlockManager(8, 4)
+    a = dev.create()
+    dev.append(a, 10)                       # blocks 0, 1, 2
+    b = dev.fork(a)                         # shares all three
+    dev.append(b, 3)                        # b copies block 2 (partial) and grows
+    shared = dev.table(a)[:2]
+    b_table = dev.table(b)
+    hid, pairs = dev.swap_out(b, host)
+    assert [p[0] for p in pairs] == b_table          # every entry, in table order
+    assert len(pairs) == 4 and host.length(hid) == 13
+    assert [p[1] for p in pairs] == host.table(hid)
+    # the blocks b shared with a stay on the device, with a's reference only
+    assert all(dev.refcount(x) == 1 for x in shared)
+    assert b not in dev.seqs and dev.table(a)[:2] == shared
+    # the blocks only b used are free again on the device
+    assert dev.num_free() == 12 - 3
+    sid, back = dev.swap_in(hid, host)
+    assert [p[0] for p in back] == [p[1] for p in pairs]
+    assert dev.table(sid) == [p[1] for p in back] and dev.length(sid) == 13
+    assert all(dev.refcount(x) == 1 for x in dev.table(sid))     # private after swap-in
+    assert host.num_free() == 8 and hid not in host.seqs
+
+
+def test_swap_is_all_or_nothing():
+    dev = BlockManager(8, 4)
+    host = BlockManager(2, 4)
+    a = dev.create()
+    dev.append(a, 12)                       # 3 blocks, host has 2
+    snap = (dev.table(a), list(dev.free), list(host.free))
+    with pytest.raises(OutOfBlocks):
+        dev.swap_out(a, host)
+    assert (dev.table(a), list(dev.free), list(host.free)) == snap

@@ -89,3 +89,25 @@ def test_copy_blocks_copies_whole_blocks_only(dtype):
     assert vc[others].tobytes() == v0[others].tobytes()
     with pytest.raises(ValueError):
         oracle.copy_blocks(kc, vc, np.array([[0, N]]), dtype)
+
+
+@pytest.mark.parametrize("dtype", synth.DTYPES)
+def test_swap_blocks_moves_whole_blocks_between_pools(dtype):
+    rng = synth.make_rng(14)
+    Hkv, B, D = 2, 16, 8
+    dev_k = synth.normal(rng, (10, Hkv, B, D), 1.0, dtype)
+    dev_v = synth.normal(rng, (10, Hkv, B, D), 1.0, dtype)
+    host_k = np.zeros((6, Hkv, B, D), synth.STORAGE[dtype])
+    host_v = np.zeros((6, Hkv, B, D), synth.STORAGE[dtype])
+    pairs = np.array([[7, 0], [2, 5], [9, 3]])
+    oracle.swap_blocks(dev_k, dev_v, host_k, host_v, pairs, dtype)
+    for src, dst in pairs:
+        assert host_k[dst].tobytes() == dev_k[src].tobytes()
+        assert host_v[dst].tobytes() == dev_v[src].tobytes()
+    assert not host_k[[1, 2, 4]].view(np.uint8).any()        # untouched host blocks
+    back_k, back_v = np.zeros_like(dev_k), np.zeros_like(dev_v)
+    oracle.swap_blocks(host_k, host_v, back_k, back_v, pairs[:, ::-1], dtype)
+    for src, dst in pairs:
+        assert back_k[src].tobytes() == dev_k[src].tobytes()
+    with pytest.raises(ValueError):
+        oracle.swap_blocks(dev_k, dev_v, host_k, host_v, np.array([[0, 6]]), dtype)
