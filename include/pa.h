@@ -388,6 +388,49 @@ PA_API int32_t pa_seq_swap_out(pa_pool *dev, pa_pool *host, int32_t seq, int32_t
 PA_API int32_t pa_seq_swap_in(pa_pool *dev, pa_pool *host, int32_t host_seq, int32_t *dev_seq, int64_t *pairs_out,
                               int32_t *n_pairs);
 
+/* ------------------------------------------------------- prefix cache
+ *
+ * A radix tree of cached token sequences over the pool's blocks, for reusing
+ * the K/V of shared prompt prefixes across requests.  ("KV Cache Optimization
+ * and Management", "RadixAttention: caching, not just packing, the prefix":
+ * match a new request's tokens against the tree, reuse every matched token's
+ * blocks, evict least-recently-used leaves when memory runs low, and let
+ * reference counts protect what running requests still use.)  Only whole
+ * blocks are cached and reused.  The cache holds one pool reference on every
+ * block it keeps.  Exact rules:
+ *  - pa_prefix_match returns the blocks of the longest cached block-aligned
+ *    prefix of tokens (writing at most cap of them; the return value is the
+ *    full count) and marks them as just used;
+ *  - pa_prefix_insert caches the first min(n_blocks, n_tokens / B) blocks of a
+ *    sequence under its tokens; prefixes already cached keep their blocks; the
+ *    return value counts newly cached blocks.  A block is cached under one
+ *    prefix at most: if a block to be newly cached is cached already, or occurs
+ *    twice among them, it returns -PA_ERR_INVALID and changes nothing; a block
+ *    id out of range or not allocated gives -PA_ERR_BAD_INDEX;
+ *  - pa_prefix_evict drops, one block at a time, a cached prefix with no cached
+ *    extension whose block no sequence uses (pool refcount 1), least recently
+ *    used first (ties: lower block id), until n_blocks blocks have been freed
+ *    or nothing qualifies; returns the number freed.
+ * Token ids are int32.  Negative returns are -pa_status.
+ */
+typedef struct pa_prefix_cache pa_prefix_cache;
+PA_API pa_prefix_cache *pa_prefix_cache_create(pa_pool *pool);
+PA_API void pa_prefix_cache_destroy(pa_prefix_cache *cache);  /* drops its block references */
+PA_API int32_t pa_prefix_match(pa_prefix_cache *cache, const int32_t *tokens, int32_t n_tokens,
+                               int32_t *blocks_out, int32_t cap);
+PA_API int32_t pa_prefix_insert(pa_prefix_cache *cache, const int32_t *tokens, int32_t n_tokens,
+                                const int32_t *blocks, int32_t n_blocks);
+PA_API int32_t pa_prefix_evict(pa_prefix_cache *cache, int32_t n_blocks);
+PA_API int32_t pa_prefix_cached_blocks(const pa_prefix_cache *cache);
+
+/*
+ * A new sequence whose table starts with n_blocks existing blocks (each gains
+ * a reference; e.g. the blocks pa_prefix_match returned) and whose length is
+ * n_blocks * B; append the rest of its tokens with pa_seq_append.  Returns the
+ * id or -pa_status.
+ */
+PA_API int32_t pa_seq_create_from_prefix(pa_pool *pool, const int32_t *blocks, int32_t n_blocks);
+
 /*
  * Fault injection for tests: let only n more block allocations succeed; any
  * operation needing more fails with PA_ERR_OOM and changes nothing.  n < 0

@@ -80,6 +80,13 @@ _SIGNATURES = {
     "pa_swap_blocks": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i64, _i64, _vp, _i32, _i32, _vp]),
     "pa_seq_swap_out": (_i32, [_vp, _vp, _i32, _vp, _vp, _vp]),
     "pa_seq_swap_in": (_i32, [_vp, _vp, _i32, _vp, _vp, _vp]),
+    "pa_prefix_cache_create": (_vp, [_vp]),
+    "pa_prefix_cache_destroy": (None, [_vp]),
+    "pa_prefix_match": (_i32, [_vp, _vp, _i32, _vp, _i32]),
+    "pa_prefix_insert": (_i32, [_vp, _vp, _i32, _vp, _i32]),
+    "pa_prefix_evict": (_i32, [_vp, _i32]),
+    "pa_prefix_cached_blocks": (_i32, [_vp]),
+    "pa_seq_create_from_prefix": (_i32, [_vp, _vp, _i32]),
 }
 
 
@@ -103,8 +110,9 @@ def _check(status: int, what: str) -> None:
         raise PaError(status, what)
 
 
-def _np_ptr(a: np.ndarray):
-    return a.ctypes.data_as(ctypes.c_void_p)
+def _np_ptr(a: np.ndarray) -> int:
+    # the address as a plain int (c_void_p argument); the caller keeps `a` alive over the call
+    return a.ctypes.data
 
 
 def make_dims(num_seqs=0, num_q_heads=1, num_kv_heads=1, head_dim=128, block_size=16, num_blocks=1,
@@ -485,6 +493,51 @@ def pa_pool_get_stats(pool) -> dict:
 
 def pa_pool_set_fail_after(pool, n) -> None:
     _check(lib.pa_pool_set_fail_after(pool, -1 if n is None else int(n)), "pa_pool_set_fail_after")
+
+
+def _neg(r: int, what: str) -> int:
+    if r < 0:
+        raise PaError(-r, what)
+    return r
+
+
+def pa_prefix_cache_create(pool) -> int:
+    h = lib.pa_prefix_cache_create(pool)
+    if not h:
+        raise PaError(PA_ERR_INVALID, "pa_prefix_cache_create")
+    return h
+
+
+def pa_prefix_cache_destroy(cache) -> None:
+    lib.pa_prefix_cache_destroy(cache)
+
+
+def pa_prefix_match(cache, tokens) -> np.ndarray:
+    """Blocks (int32) of the longest cached block-aligned prefix of `tokens`."""
+    t = np.ascontiguousarray(tokens, dtype=np.int32)
+    cap = max(1, t.shape[0])
+    out = np.empty(cap, dtype=np.int32)
+    n = _neg(lib.pa_prefix_match(cache, _np_ptr(t), t.shape[0], _np_ptr(out), cap), "pa_prefix_match")
+    return out[:n].copy()
+
+
+def pa_prefix_insert(cache, tokens, blocks) -> int:
+    t = np.ascontiguousarray(tokens, dtype=np.int32)
+    b = np.ascontiguousarray(blocks, dtype=np.int32)
+    return _neg(lib.pa_prefix_insert(cache, _np_ptr(t), t.shape[0], _np_ptr(b), b.shape[0]), "pa_prefix_insert")
+
+
+def pa_prefix_evict(cache, n_blocks: int) -> int:
+    return _neg(lib.pa_prefix_evict(cache, int(n_blocks)), "pa_prefix_evict")
+
+
+def pa_prefix_cached_blocks(cache) -> int:
+    return _neg(lib.pa_prefix_cached_blocks(cache), "pa_prefix_cached_blocks")
+
+
+def pa_seq_create_from_prefix(pool, blocks) -> int:
+    b = np.ascontiguousarray(blocks, dtype=np.int32)
+    return _neg(lib.pa_seq_create_from_prefix(pool, _np_ptr(b), b.shape[0]), "pa_seq_create_from_prefix")
 
 
 class Pool:

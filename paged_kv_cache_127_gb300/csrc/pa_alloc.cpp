@@ -30,22 +30,7 @@
 
 #include "../../include/pa.h"
 
-struct pa_seq_rec {
-    std::vector<int32_t> table;
-    int64_t len = 0;
-    bool live = false;
-};
-
-struct pa_pool {
-    int32_t num_blocks = 0;
-    int32_t B = 0;
-    std::deque<int32_t> free_list;
-    std::vector<int32_t> ref;
-    std::vector<pa_seq_rec> seqs;
-    int32_t live = 0;
-    int64_t cow_copies = 0;
-    int64_t fail_budget = -1;  // < 0: unlimited
-};
+#include "pa_pool.h"
 
 namespace {
 
@@ -55,11 +40,8 @@ bool valid_seq(const pa_pool *p, int32_t s) {
 
 int64_t blocks_for(int64_t tokens, int32_t B) { return (tokens + B - 1) / B; }
 
-int64_t available(const pa_pool *p) {
-    int64_t f = (int64_t)p->free_list.size();
-    if (p->fail_budget >= 0 && p->fail_budget < f) f = p->fail_budget;
-    return f;
-}
+using pa_pool_detail::available;
+using pa_pool_detail::release_block;
 
 int32_t take_block(pa_pool *p) {
     int32_t b = p->free_list.front();
@@ -69,9 +51,6 @@ int32_t take_block(pa_pool *p) {
     return b;
 }
 
-void release_block(pa_pool *p, int32_t b) {
-    if (--p->ref[b] == 0) p->free_list.push_back(b);
-}
 
 // Blocks one append of n tokens needs, given the refcount already given up on
 // the sequence's last block by earlier copies in the same batch.

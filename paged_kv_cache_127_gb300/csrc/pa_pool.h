@@ -1,0 +1,42 @@
+// pa_pool.h -- internal layout of the host block pool, shared by the
+// allocator (pa_alloc.cpp) and the prefix cache (pa_prefix.cpp).
+#pragma once
+
+#include <cstdint>
+#include <deque>
+#include <vector>
+
+#include "../../include/pa.h"
+
+struct pa_seq_rec {
+    std::vector<int32_t> table;
+    int64_t len = 0;
+    bool live = false;
+};
+
+struct pa_pool {
+    int32_t num_blocks = 0;
+    int32_t B = 0;
+    std::deque<int32_t> free_list;
+    std::vector<int32_t> ref;
+    std::vector<pa_seq_rec> seqs;
+    int32_t live = 0;
+    int64_t cow_copies = 0;
+    int64_t fail_budget = -1;  // < 0: unlimited
+};
+
+
+namespace pa_pool_detail {
+
+inline int64_t available(const pa_pool *p) {
+    int64_t f = (int64_t)p->free_list.size();
+    if (p->fail_budget >= 0 && p->fail_budget < f) f = p->fail_budget;
+    return f;
+}
+
+// Drop one reference; a block reaching zero goes to the back of the free list.
+inline void release_block(pa_pool *p, int32_t b) {
+    if (--p->ref[b] == 0) p->free_list.push_back(b);
+}
+
+}  // namespace pa_pool_detail

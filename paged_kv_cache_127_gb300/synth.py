@@ -154,6 +154,32 @@ def copy_pairs(rng, n: int, num_blocks: int) -> np.ndarray:
     return np.stack([ids[:n], ids[n:2 * n]], axis=1).astype(np.int64)
 
 
+def prefix_requests(rng, n: int, families: int = 8, family_median: float = 512, own_median: float = 90,
+                    followup: float = 0.3, vocab: int = 32000, max_len: int = 8192) -> list:
+    """n request token streams (int32 arrays) for prefix-cache workloads.
+
+    Each request is one of `families` shared prompts (lengths lognormal around
+    `family_median`; family i drawn with weight 1 / (i + 1)) followed by its
+    own tokens (lognormal around `own_median`); a fraction `followup` instead
+    continue one of the last 64 requests (its whole token list plus new own
+    tokens), as a multi-turn conversation does.  Lengths are capped at max_len.
+    """
+    fam_len = lognormal_lengths(rng, families, family_median, 0.5, 16, max_len // 2)
+    fams = [rng.integers(0, vocab, size=int(k), dtype=np.int32) for k in fam_len]
+    w = 1.0 / np.arange(1, families + 1)
+    w /= w.sum()
+    out = []
+    for _ in range(n):
+        own = rng.integers(0, vocab, size=int(lognormal_lengths(rng, 1, own_median, 0.8, 1, 2048)[0]),
+                           dtype=np.int32)
+        if out and rng.random() < followup:
+            base = out[-1 - int(rng.integers(0, min(64, len(out))))]
+        else:
+            base = fams[int(rng.choice(families, p=w))]
+        out.append(np.concatenate([base, own])[:max_len])
+    return out
+
+
 # ---------------------------------------------------------------- workloads
 @dataclass
 class Workload:
