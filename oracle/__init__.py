@@ -6,11 +6,13 @@ Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 
 Contents
 --------
-* ``decode`` / ``decode_partitioned`` / ``write_kv`` / ``copy_blocks`` /
-  ``slot_mapping``: ctypes wrappers over the fp64 C oracle in ``pa_oracle.c``
-  (plain definitions; see that file's header for the page citations).
+* ``decode`` / ``decode_partitioned`` / ``chunk_attention`` / ``write_kv`` /
+  ``copy_blocks`` / ``swap_blocks`` / ``slot_mapping``: ctypes wrappers over the
+  fp64 C oracle in ``pa_oracle.c`` (plain definitions; see that file's header
+  for the page citations).
 * ``block_manager.BlockManager``: a plain Python model of the block manager
-  (free list, reference counts, fork, growth, copy-on-write).
+  (free list, reference counts, fork, growth, copy-on-write, swap).
+* ``prefix_cache.PrefixCache``: a plain model of the block-level prefix cache.
 * ``bookkeeping``: the pages' block-count and fragmentation arithmetic.
 
 Array conventions: f32 data as ``np.float32``, f16 as ``np.float16``, bf16 as
@@ -43,9 +45,10 @@ def _load():
         lib.pa_oracle_slot_mapping.argtypes = [i32, vp, i32, i32, vp, vp, vp]
         lib.pa_oracle_slot.argtypes = [vp, i32, i32, ctypes.POINTER(i64)]
         lib.pa_oracle_swap_blocks.argtypes = [i32] * 4 + [vp, vp, i32, vp, vp, i32, vp, i32]
+        lib.pa_oracle_chunk_attention.argtypes = [i32] * 8 + [vp] * 6 + [i32, dbl, vp]
         for f in (lib.pa_oracle_decode, lib.pa_oracle_decode_partitioned, lib.pa_oracle_write_kv,
                   lib.pa_oracle_copy_blocks, lib.pa_oracle_slot_mapping, lib.pa_oracle_slot,
-                  lib.pa_oracle_swap_blocks):
+                  lib.pa_oracle_swap_blocks, lib.pa_oracle_chunk_attention):
             f.restype = i32
         _lib = lib
     return _lib
@@ -98,6 +101,30 @@ def decode_partitioned(q, k_cache, v_cache, tables, lens, scale: float, dtype: s
         _ptr(tables), _ptr(lens), float(scale), int(partition_size), _ptr(out))
     if rc:
         raise ValueError(f"oracle decode_partitioned rejected its inputs (rc={rc})")
+    return out
+
+
+def chunk_attention(q, k_cache, v_cache, tables, lens, query_start, scale: float, dtype: str) -> np.ndarray:
+    """fp64 causal attention of each sequence's last n_s tokens over its paged
+    context: q [T, Hq, D] with sequence s owning rows query_start[s]..query_start[s+1]-1;
+    the query at position pos = lens[s] - n_s + t sees keys 0..pos.  Returns [T, Hq, D]."""
+    q = _check(q, dtype, "q")
+    k_cache = _check(k_cache, dtype, "k_cache")
+    v_cache = _check(v_cache, dtype, "v_cache")
+    tables = np.ascontiguousarray(tables, dtype=np.int32)
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    query_start = np.ascontiguousarray(query_start, dtype=np.int32)
+    T, Hq, D = q.shape
+    N, Hkv, B, D2 = k_cache.shape
+    S = lens.shape[0]
+    if D2 != D or v_cache.shape != k_cache.shape or tables.shape[0] != S or query_start.shape != (S + 1,):
+        raise ValueError("shape mismatch between q, caches, tables, lens and query_start")
+    out = np.zeros((T, Hq, D), dtype=np.float64)
+    rc = _load().pa_oracle_chunk_attention(S, Hq, Hkv, D, B, N, tables.shape[1], DTYPE_CODE[dtype], _ptr(q),
+                                           _ptr(k_cache), _ptr(v_cache), _ptr(tables), _ptr(lens),
+                                           _ptr(query_start), T, float(scale), _ptr(out))
+    if rc:
+        raise ValueError(f"oracle chunk_attention rejected its inputs (rc={rc})")
     return out
 
 

@@ -41,6 +41,16 @@
  *    all B slots, keys and values).  (Same section; "Paged Attention and vLLM",
  *    "Continuous Batching and Scheduler", the copy-on-write rule.)
  *
+ *  - Attention for a chunk of query tokens per sequence (chunked prefill,
+ *    verification of drafted tokens): the n_s query tokens of sequence s are
+ *    its last n_s positions, len - n_s .. len - 1, and the query at position
+ *    pos attends to positions 0 .. pos only -- the cache a one-token-at-a-time
+ *    decode would hold at that point ("Paged Attention and vLLM", "KV Cache
+ *    Fundamentals": the key cache at length t is the keys of tokens 1..t;
+ *    "KV Cache Optimization and Management", "Common misconception": paging
+ *    leaves the scores and the softmax unchanged).  Plain definition again,
+ *    one query row at a time.
+ *
  *  - Block swap: the same whole-block copy between two pools (device blocks to
  *    host blocks and back), for preemption ("Paged Attention and vLLM",
  *    "Continuous Batching and Scheduler": evict a sequence's physical blocks to
@@ -53,7 +63,8 @@
  *  - q is stored in the cache dtype, the output is returned in double.
  *
  * Storage layouts (row-major, element type given by `dtype`):
- *   q        [S, Hq, D]
+ *   q        [S, Hq, D]   (chunk attention: [T, Hq, D], T query tokens,
+ *                          sequence s owning rows query_start[s] .. query_start[s+1]-1)
  *   k_cache  [N, Hkv, B, D]     v_cache the same
  *   tables   int32 [S, max_blocks]
  *   lens     int32 [S]
@@ -226,6 +237,74 @@ int pa_oracle_decode(int S, int Hq, int Hkv, int D, int B, int N, int max_blocks
                     o[d] += z[i] * Vc[(size_t)i * D + d];
             for (int d = 0; d < D; ++d)
                 o[d] /= den;
+        }
+        free(Kc);
+        free(Vc);
+        free(z);
+    }
+    return rc;
+}
+
+/* ---- chunk attention: several query tokens per sequence, causal -------------- */
+
+int pa_oracle_chunk_attention(int S, int Hq, int Hkv, int D, int B, int N, int max_blocks, int dtype,
+                              const void *q, const void *k_cache, const void *v_cache,
+                              const int32_t *tables, const int32_t *lens, const int32_t *query_start,
+                              int T, double scale, double *out)
+{
+    if (check_dims(S, Hq, Hkv, D, B, N, max_blocks, dtype, lens) || T < 0 || query_start[0] != 0 ||
+        query_start[S] != T)
+        return -1;
+    for (int s = 0; s < S; ++s) {
+        const int n = query_start[s + 1] - query_start[s];
+        if (n < 0 || n > lens[s])
+            return -1;
+    }
+    const int G = Hq / Hkv;
+    int rc = 0;
+    for (int s = 0; s < S && rc == 0; ++s) {
+        const int len = lens[s];
+        const int n = query_start[s + 1] - query_start[s];
+        const int32_t *row = tables + (size_t)s * max_blocks;
+        double *Kc = malloc(sizeof(double) * ((size_t)len * D + 1));
+        double *Vc = malloc(sizeof(double) * ((size_t)len * D + 1));
+        double *z = malloc(sizeof(double) * ((size_t)len + 1));
+        if (!Kc || !Vc || !z) { free(Kc); free(Vc); free(z); return -2; }
+        for (int kvh = 0; kvh < Hkv && rc == 0 && n > 0; ++kvh) {
+            if (gather(k_cache, v_cache, dtype, Hkv, B, D, N, row, len, kvh, Kc, Vc)) {
+                rc = -1;
+                break;
+            }
+            for (int t = 0; t < n; ++t) {
+                const int pos = len - n + t;   /* this query's position; keys 0..pos */
+                const size_t tok = (size_t)query_start[s] + t;
+                for (int h = kvh * G; h < (kvh + 1) * G; ++h) {
+                    const size_t qbase = (tok * Hq + h) * D;
+                    double *o = out + qbase;
+                    for (int i = 0; i <= pos; ++i) {
+                        double dot = 0.0;
+                        for (int d = 0; d < D; ++d)
+                            dot += load_elem(q, qbase + d, dtype) * Kc[(size_t)i * D + d];
+                        z[i] = scale * dot;
+                    }
+                    double m = z[0];
+                    for (int i = 1; i <= pos; ++i)
+                        if (z[i] > m)
+                            m = z[i];
+                    double den = 0.0;
+                    for (int i = 0; i <= pos; ++i) {
+                        z[i] = exp(z[i] - m);
+                        den += z[i];
+                    }
+                    for (int d = 0; d < D; ++d)
+                        o[d] = 0.0;
+                    for (int i = 0; i <= pos; ++i)
+                        for (int d = 0; d < D; ++d)
+                            o[d] += z[i] * Vc[(size_t)i * D + d];
+                    for (int d = 0; d < D; ++d)
+                        o[d] /= den;
+                }
+            }
         }
         free(Kc);
         free(Vc);
