@@ -48,7 +48,7 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 126 * 2**20
 KERNEL_SOURCES = ("pa_decode_mma.cuh", "pa_plan.cu", "pa_cache_ops.cu", "pa_tmap.cu", "pa_api.cu",
-                  "pa_device.cuh", "pa_internal.h")
+                  "pa_device.cuh", "pa_internal.h", "pa_mma.cuh")
 
 
 # --------------------------------------------------------------------------- distributed helpers
@@ -389,6 +389,134 @@ def run_ours(args):
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = {k: v for k, v in cpu_baseline(step).items() if k != "seconds"}
+    return line
+
+
+# --------------------------------------------------------------------------- chunk attention
+def measured_bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (cuBLAS bf16 GEMM, burst)"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def run_chunk(args):
+    """Chunk attention (several query tokens per sequence): one step is the KV
+    write of every new token followed by pa_chunk_attention over them."""
+    import torch
+
+    import oracle
+    from paged_kv_cache_127_gb300 import binding as pa
+    from paged_kv_cache_127_gb300 import workloads
+
+    rank, local_rank, world = dist_env()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    dist = dist_init(world, "nccl")
+    step = workloads.build_step(args.workload, seed=rank, binding=pa)
+    if args.partition_size:
+        step.partition_size = args.partition_size
+    dims = step.dims(pa)
+    T, Hq, D, n = step.num_tokens, step.num_q_heads, step.head_dim, step.query_len
+    kvt = torch.bfloat16 if step.dtype == "bf16" else torch.float16
+
+    def dev(x, dt=None):
+        if dt is None:
+            return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(kvt).to(device)
+        return torch.from_numpy(np.ascontiguousarray(x)).to(device)
+
+    d_q, d_k, d_v = dev(step.q), dev(step.k_new), dev(step.v_new)
+    d_kc, d_vc = dev(step.k_cache), dev(step.v_cache)
+    d_slots, d_tables = dev(step.slots, 1), dev(step.tables, 1)
+    d_lens, d_qs = dev(step.lens, 1), dev(step.query_start(), 1)
+    d_out = torch.empty((T, Hq, D), dtype=torch.float32, device=device)
+    ws = torch.empty(max(pa.pa_chunk_workspace_bytes(dims, T, n), 16), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    split = step.max_blocks * step.block_size > step.partition_size
+    launches_per_step = 1 + 2 + (1 if split else 0)   # write_kv, plan, chunk kernel, merge
+    ev = []
+
+    def device_step(record=False):
+        pa.pa_write_kv(dims, d_k, d_v, d_slots, d_kc, d_vc, stream)
+        if record:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        pa.pa_chunk_attention(dims, d_q, d_kc, d_vc, d_tables, d_lens, d_qs, step.scale, d_out, n, ws, stream)
+        if record:
+            e1.record(stream)
+            ev.append((e0, e1))
+
+    pa.pa_device_errors(clear=True)
+    sampler = ClockSampler(device.index).start() if rank == 0 else None
+    for _ in range(args.warmup):
+        device_step()
+    torch.cuda.synchronize(device)
+    barrier(dist, device)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        device_step(record=True)
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(dist, device)
+    clocks = sampler.stop() if sampler else None
+    assert pa.pa_device_errors(clear=True) == 0, "device error flags set during the timed steps"
+    assert torch.isfinite(d_out).all().item()
+    ms = reduce_scalar(dist, t0.elapsed_time(t1), "max", device) / args.steps
+    call_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    kv = step.kv_bytes_unique()      # every visible KV slot once (the last query sees the whole context)
+    flops = step.chunk_flops()
+    if rank != 0:
+        return None
+    hbm_peak, hbm_kind = measured_hbm_peak()
+    tc_peak, tc_kind = measured_bf16_peak()
+    gbs = kv / (call_ms / 1e3) / 1e9
+    tfs = flops / (call_ms / 1e3) / 1e12
+    hbm_bound = kv / (hbm_peak * 1e9) > flops / (tc_peak * 1e12)
+    roof = ({"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "peak_kind": hbm_kind, "unit": "GB/s",
+             "frac": round(gbs / hbm_peak, 4)} if hbm_bound else
+            {"bound": "tensor", "achieved": round(tfs, 2), "peak": tc_peak, "peak_kind": tc_kind, "unit": "TFLOP/s",
+             "frac": round(tfs / tc_peak, 4)})
+    roof.update({"traffic": None, "kernel": "pa_chunk_attention (plan + tensor-core chunk kernel + merge)",
+                 "call_ms": round(call_ms, 5),
+                 "bytes": "distinct visible KV slots per call", "flops": "4 * D * Hq per (query, visible key)"})
+    line = {
+        "metric": "paged chunk-attention query-tokens/s (KV write + causal attention of every new token)",
+        "value": round(T * world / (ms / 1e3), 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": step.dtype, "data": "synthetic (seeded)",
+        "config": {"workload": args.workload, "num_seqs": step.num_seqs, "query_len": n, "num_q_heads": Hq,
+                   "num_kv_heads": step.num_kv_heads, "head_dim": D, "block_size": step.block_size,
+                   "context_tokens": int(step.lens.sum()), "kv_bytes_unique_per_step": kv,
+                   "flops_per_step": flops,
+                   "l2": f"{kv / 2**20:.0f} MiB of KV per step vs {L2_BYTES / 2**20:.0f} MiB L2; no flush"},
+        "kv_gbs": round(gbs, 1), "tflops": round(tfs, 2),
+        "roofline": roof, "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        rng = np.random.default_rng(7)
+        order = rng.permutation(step.num_seqs)
+        kc, vc = step.k_cache, step.v_cache
+        oracle.write_kv(step.k_new, step.v_new, step.slots, kc, vc, step.dtype)
+        secs, done, toks = 0.0, 0, 0
+        # a sample of query rows: rows a..b-1 of a chunk are the last b - a queries of
+        # the context cut after row b - 1, so a long chunk is sampled a few rows at a time
+        r = min(n, 8)
+        for s_ in order:
+            a0 = int(rng.integers(0, n - r + 1))
+            cut = int(step.lens[s_]) - n + a0 + r
+            c0 = time.perf_counter()
+            oracle.chunk_attention(step.q[s_ * n + a0:s_ * n + a0 + r], kc, vc, step.tables[s_:s_ + 1],
+                                   np.array([cut], np.int32), np.array([0, r], np.int32), step.scale, step.dtype)
+            secs += time.perf_counter() - c0
+            done += 1
+            toks += r
+            if secs > 15.0:
+                break
+        line["cpu_baseline"] = {"value": round(toks / secs, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{toks} query tokens ({r} consecutive rows from each of {done} sequences), "
+                                          f"fp64 chunk attention, single thread, {secs:.1f} s"}
     return line
 
 
@@ -782,6 +910,8 @@ def main(argv=None):
         line = run_reference(args)
     elif args.prefix_requests > 0:
         line = run_prefix(args)
+    elif args.workload in ("verify8b", "prefill8b"):
+        line = run_chunk(args)
     elif args.swap_blocks > 0:
         line = run_swap(args)
     elif args.layers > 1:

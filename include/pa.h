@@ -156,6 +156,50 @@ PA_API int32_t pa_decode_noalloc(const pa_dims *dims, const void *q, const void 
                                  const int32_t *context_lens, float scale, float *out, void *stream);
 
 /*
+ * pa_chunk_attention -- paged attention for several query tokens per sequence
+ * (a prefill chunk, or drafted tokens being verified), over the same cache:
+ * the n_s = query_start[s+1] - query_start[s] query rows of sequence s are its
+ * last n_s positions, whose keys and values are already in the cache
+ * (pa_write_kv), and the query at position pos = context_lens[s] - n_s + t
+ * attends to positions 0 .. pos only:
+ *
+ *     out[i, h, :] = softmax(scale * q[i, h, :] . K_s[0..pos]^T) . V_s[0..pos],
+ *     i = query_start[s] + t
+ *
+ * -- the result of decoding those tokens one at a time.  ("Paged Attention and
+ * vLLM", "KV Cache Fundamentals": the cache of a sequence at length t holds
+ * tokens 1..t; "Block Table and Logical-to-Physical Mapping" for the paged
+ * read; "Paged Attention CUDA Kernel" for the per-partition terms and their
+ * merge.  "KV Cache Optimization and Management", "Common misconception":
+ * paging changes neither the scores nor the softmax.)
+ *
+ *   q             [T, Hq, D] kv_dtype, device; T = num_tokens
+ *   query_start   int32 [S + 1], device: non-decreasing, query_start[0] >= 0,
+ *                 query_start[S] <= T; rows outside every range are not written
+ *   max_query_len an upper bound on every n_s (host-known; sizes the work split)
+ *   out           float32 [T, Hq, D], device, written for the rows of valid
+ *                 sequences
+ *   other arguments as for pa_decode; kv_dtype must be PA_F16 or PA_BF16
+ *                 (PA_ERR_UNSUPPORTED for PA_F32)
+ * A sequence with n_s > context_lens[s] or n_s > max_query_len is skipped and
+ * PA_DEVERR_BAD_LEN is set; a query_start that is not non-decreasing within
+ * [0, T] skips every sequence and sets PA_DEVERR_BAD_LEN.
+ *
+ * pa_chunk_workspace_bytes -- the scratch it needs: a work list of S * P * R
+ * int4 entries after a 256-byte header, a token-to-sequence map of T ints,
+ * and for P > 1 the split-K partials T * Hq * P * (D + 2) floats, each part
+ * rounded up to 256 bytes; P as for pa_decode, R = ceil(ceil(max_query_len *
+ * Hq / Hkv / 16) / W), W = 2 if max_query_len * Hq / Hkv > 16, else 1.
+ * Returns 0 for invalid arguments.
+ */
+PA_API size_t pa_chunk_workspace_bytes(const pa_dims *dims, int32_t num_tokens, int32_t max_query_len);
+PA_API int32_t pa_chunk_attention(const pa_dims *dims, const void *q, const void *k_cache,
+                                  const void *v_cache, const int32_t *block_tables,
+                                  const int32_t *context_lens, const int32_t *query_start,
+                                  int32_t num_tokens, int32_t max_query_len, float scale, float *out,
+                                  void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * pa_write_kv -- the KV write (reshape-and-cache): store each new token's key
  * and value rows in its slot, for every KV head:
  *

@@ -54,6 +54,9 @@ _SIGNATURES = {
     "pa_decode_workspace_bytes": (_sz, [_vp]),
     "pa_decode": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _sz, _vp]),
     "pa_decode_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
+    "pa_chunk_workspace_bytes": (_sz, [_vp, _i32, _i32]),
+    "pa_chunk_attention": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float, _vp, _vp, _sz,
+                                  _vp]),
     "pa_write_kv": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp]),
     "pa_copy_blocks": (_i32, [_vp, _vp, _vp, _vp, _i32, _vp]),
     "pa_copy_blocks_layers": (_i32, [_vp, _vp, _vp, _i32, _i64, _vp, _i32, _vp]),
@@ -208,6 +211,42 @@ def pa_decode_noalloc(dims: pa_dims, q, k_cache, v_cache, block_tables, context_
                                block_tables.data_ptr(), context_lens.data_ptr(), float(scale), out.data_ptr(),
                                _stream_ptr(stream, dev))
     _check(st, "pa_decode_noalloc")
+
+
+def pa_chunk_workspace_bytes(dims: pa_dims, num_tokens: int, max_query_len: int) -> int:
+    return int(lib.pa_chunk_workspace_bytes(ctypes.byref(dims), int(num_tokens), int(max_query_len)))
+
+
+def pa_chunk_attention(dims: pa_dims, q, k_cache, v_cache, block_tables, context_lens, query_start, scale: float,
+                       out, max_query_len: int, workspace=None, stream=None) -> None:
+    """Causal paged attention for the last n_s = query_start[s+1] - query_start[s]
+    tokens of each sequence: the query at position pos sees keys 0..pos."""
+    t = _torch()
+    d, kv = dims, _torch_dtype(dims.kv_dtype)
+    dev = q.device
+    T = q.shape[0]
+    _expect(q, "q", (T, d.num_q_heads, d.head_dim), kv, dev)
+    cache_shape = (d.num_blocks, d.num_kv_heads, d.block_size, d.head_dim)
+    _expect(k_cache, "k_cache", cache_shape, kv, dev)
+    _expect(v_cache, "v_cache", cache_shape, kv, dev)
+    _expect(block_tables, "block_tables", (d.num_seqs, d.max_blocks_per_seq), t.int32, dev)
+    _expect(context_lens, "context_lens", (d.num_seqs,), t.int32, dev)
+    _expect(query_start, "query_start", (d.num_seqs + 1,), t.int32, dev)
+    _expect(out, "out", (T, d.num_q_heads, d.head_dim), t.float32, dev)
+    need = pa_chunk_workspace_bytes(dims, T, max_query_len)
+    ws_ptr, ws_bytes = None, 0
+    if need:
+        if workspace is None:
+            raise ValueError(f"pa_chunk_attention needs a workspace of {need} bytes")
+        if not workspace.is_cuda or not workspace.is_contiguous() or workspace.device != dev:
+            raise ValueError("workspace must be a contiguous CUDA tensor on the same device")
+        ws_bytes = workspace.numel() * workspace.element_size()
+        ws_ptr = ctypes.c_void_p(workspace.data_ptr())
+    st = lib.pa_chunk_attention(ctypes.byref(dims), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                block_tables.data_ptr(), context_lens.data_ptr(), query_start.data_ptr(), T,
+                                int(max_query_len), float(scale), out.data_ptr(), ws_ptr, ws_bytes,
+                                _stream_ptr(stream, dev))
+    _check(st, "pa_chunk_attention")
 
 
 def pa_write_kv(dims: pa_dims, k, v, slot_mapping, k_cache, v_cache, stream=None) -> None:

@@ -101,6 +101,45 @@ size_t workspace_bytes_for(const pa_dims *d, int32_t max_parts) {
     return d->num_seqs > 0 ? workspace_layout(d, max_parts).total : 0;
 }
 
+// Chunk-attention checks: the decode checks, 16-bit caches only, and a token
+// count and query-length bound whose scratch sizes stay addressable.
+int32_t check_chunk_dims(const pa_dims *d, int32_t T, int32_t max_q, int32_t *max_parts) {
+    int32_t rc = check_decode_dims(d, max_parts);
+    if (rc != PA_OK) return rc;
+    if (d->kv_dtype == PA_F32) return PA_ERR_UNSUPPORTED;
+    if (T < 0 || max_q < 1 || max_q > (1 << 20)) return PA_ERR_INVALID;
+    if ((int64_t)T * d->num_q_heads > INT32_MAX) return PA_ERR_INVALID;
+    return PA_OK;
+}
+
+// Chunk workspace, each part 256-byte aligned:
+//   header    2 ints: work items, claim counter
+//   list      int4 [S * P * R]: (sequence, partition, tokens, row block)
+//   tok       int32 [T]: sequence of each query row
+//   acc, ml   float [T, Hq, P, D] and [T, Hq, P, 2]   (only if P > 1)
+struct ChunkLayout {
+    size_t list, tok, acc, ml, total;
+};
+
+ChunkLayout chunk_layout(const pa_dims *d, int32_t T, int32_t max_q, int32_t max_parts) {
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    const int64_t G = d->num_q_heads / d->num_kv_heads;
+    const int64_t rpb = 16 * pa::chunk_row_warps(max_q, (int)G);
+    const int64_t R = ((int64_t)max_q * G + rpb - 1) / rpb;
+    ChunkLayout L{};
+    size_t off = 256;
+    L.list = off;
+    off += up((size_t)d->num_seqs * max_parts * R * 4 * sizeof(int));
+    L.tok = off;
+    off += up((size_t)T * sizeof(int32_t));
+    L.acc = off;
+    off += max_parts > 1 ? up((size_t)T * d->num_q_heads * max_parts * d->head_dim * sizeof(float)) : 0;
+    L.ml = off;
+    off += max_parts > 1 ? up((size_t)T * d->num_q_heads * max_parts * 2 * sizeof(float)) : 0;
+    L.total = off;
+    return L;
+}
+
 // Tensor maps of the two caches, re-encoded only when the cache or its shape
 // changes (per host thread).
 struct TmapEntry {
@@ -221,6 +260,74 @@ int32_t pa_decode(const pa_dims *dims, const void *q, const void *k_cache, const
     e = bf16 ? pa::launch_decode_mma_bf16(a, tmk, tmv, st) : pa::launch_decode_mma_f16(a, tmk, tmv, st);
     if (e != cudaSuccess) return to_status(e);
     if (parts > 1) e = pa::launch_decode_merge(a, st);
+    return to_status(e);
+}
+
+size_t pa_chunk_workspace_bytes(const pa_dims *dims, int32_t num_tokens, int32_t max_query_len) {
+    int32_t parts = 0;
+    if (check_chunk_dims(dims, num_tokens, max_query_len, &parts) != PA_OK) return 0;
+    return chunk_layout(dims, num_tokens, max_query_len, parts).total;
+}
+
+int32_t pa_chunk_attention(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *block_tables, const int32_t *context_lens, const int32_t *query_start,
+                           int32_t num_tokens, int32_t max_query_len, float scale, float *out, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+    int32_t parts = 0;
+    int32_t rc = check_chunk_dims(dims, num_tokens, max_query_len, &parts);
+    if (rc != PA_OK) return rc;
+    if (dims->num_seqs == 0 || num_tokens == 0) return PA_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start || !out) return PA_ERR_INVALID;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(query_start, 4))
+        return PA_ERR_INVALID;
+    const ChunkLayout L = chunk_layout(dims, num_tokens, max_query_len, parts);
+    if (!workspace || workspace_bytes < L.total || !aligned(workspace, 256)) return PA_ERR_INVALID;
+
+    pa::ChunkArgs a{};
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.query_start = query_start;
+    a.out = out;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    a.plan_hdr = reinterpret_cast<int *>(ws);
+    a.plan_list = reinterpret_cast<int4 *>(ws + L.list);
+    a.tok_seq = reinterpret_cast<int32_t *>(ws + L.tok);
+    a.ws_acc = parts > 1 ? reinterpret_cast<float *>(ws + L.acc) : nullptr;
+    a.ws_ml = parts > 1 ? reinterpret_cast<float *>(ws + L.ml) : nullptr;
+    a.err = error_word();
+    if (!a.err) return PA_ERR_CUDA;
+    a.S = dims->num_seqs;
+    a.T = num_tokens;
+    a.Hq = dims->num_q_heads;
+    a.Hkv = dims->num_kv_heads;
+    a.D = dims->head_dim;
+    a.B = dims->block_size;
+    a.N = dims->num_blocks;
+    a.max_blocks = dims->max_blocks_per_seq;
+    a.partition_size = effective_partition(dims);
+    a.max_parts = parts;
+    a.max_query_len = max_query_len;
+    a.head_group = pa::decode_head_group(dims->num_kv_heads);
+    a.row_warps = pa::chunk_row_warps(max_query_len, dims->num_q_heads / dims->num_kv_heads);
+    a.scale = scale;
+
+    const bool bf16 = dims->kv_dtype == PA_BF16;
+    const long long block_heads = (long long)dims->num_blocks * dims->num_kv_heads;
+    CUtensorMap tmk, tmv;
+    cudaError_t e = cache_tensor_map(k_cache, bf16, dims->head_dim, dims->block_size, block_heads, a.head_group, &tmk);
+    if (e == cudaSuccess)
+        e = cache_tensor_map(v_cache, bf16, dims->head_dim, dims->block_size, block_heads, a.head_group, &tmv);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    e = pa::launch_chunk_plan(a, st);
+    if (e != cudaSuccess) return to_status(e);
+    e = bf16 ? pa::launch_chunk_mma_bf16(a, tmk, tmv, st) : pa::launch_chunk_mma_f16(a, tmk, tmv, st);
+    if (e != cudaSuccess) return to_status(e);
+    if (parts > 1) e = pa::launch_chunk_merge(a, st);
     return to_status(e);
 }
 

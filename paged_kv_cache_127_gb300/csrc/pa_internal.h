@@ -26,6 +26,31 @@ struct DecodeArgs {
     float scale;
 };
 
+// Everything a chunk-attention launch needs (several query tokens per sequence).
+struct ChunkArgs {
+    const void *q;                  // [T, Hq, D]
+    const void *k_cache;
+    const void *v_cache;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    const int32_t *query_start;     // [S + 1]
+    float *out;                     // [T, Hq, D]
+    float *ws_ml;                   // [T, Hq, P, 2]
+    float *ws_acc;                  // [T, Hq, P, D]
+    int *plan_hdr;                  // [0] work items, [1] claim counter
+    int4 *plan_list;                // (sequence, partition, tokens, row block), largest first
+    int32_t *tok_seq;               // [T]: sequence of each query row, -1 if none
+    unsigned int *err;
+    int S, T, Hq, Hkv, D, B, N, max_blocks, partition_size, max_parts, max_query_len;
+    int head_group;                 // KV heads per work item
+    int row_warps;                  // 16-row query tiles per KV head per work item (1 or 2)
+    float scale;
+};
+
+// Row warps of a chunk-attention work item: two 16-row tiles per KV head when
+// a sequence can have more than 16 (query token, query head) rows, else one.
+inline int chunk_row_warps(int max_query_len, int G) { return (long long)max_query_len * G > 16 ? 2 : 1; }
+
 // KV heads that one tensor-core work item (one CTA) covers: PA_MMA_HEAD_GROUP
 // (4 by default) when they divide Hkv, else the largest power of two that does.
 #ifndef PA_MMA_HEAD_GROUP
@@ -67,6 +92,14 @@ cudaError_t launch_decode_mma_bf16(const DecodeArgs &a, const CUtensorMap &tmk, 
 // (block, head) pairs.
 cudaError_t make_cache_tensor_map(CUtensorMap *map, const void *cache, bool bf16, int D, int B,
                                   long long block_heads, int head_group);
+
+// Chunk attention: work list, tensor-core partition kernel, split-K merge.
+cudaError_t launch_chunk_plan(const ChunkArgs &a, cudaStream_t st);
+cudaError_t launch_chunk_mma_f16(const ChunkArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                                 cudaStream_t st);
+cudaError_t launch_chunk_mma_bf16(const ChunkArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                                  cudaStream_t st);
+cudaError_t launch_chunk_merge(const ChunkArgs &a, cudaStream_t st);
 
 cudaError_t launch_write_kv(const void *k, const void *v, const int64_t *slots, int T, int Hkv,
                             int row_bytes, int B, int N, void *k_cache, void *v_cache,

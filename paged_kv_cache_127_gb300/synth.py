@@ -26,6 +26,11 @@ layer, a shared-prefix batch and a long-context 70B-shaped layer):
               800-token prefix plus private suffixes U{1..512}; 32 pairs sharing
               a 24-token prefix whose next write forces a block copy; one new
               token per sequence per step
+  verify8b    the gqa8b_b16 layer with 5 query tokens per sequence (4 drafted
+              tokens + the last accepted one being verified): 256 sequences,
+              cached context lognormal (median 600, sigma 0.8) + the 5 tokens
+  prefill8b   the same layer, chunked prefill: 16 sequences each adding a
+              512-token chunk to a cached context U{0..3584}
   long70b     Hq 64 / Hkv 8, D 128, bf16, B 16; 32 sequences, lengths
               U{8192..32768}; shuffled placement; partitions of 512 tokens;
               N(0, 1); scale 1/sqrt(128)
@@ -202,6 +207,7 @@ class Workload:
     prefix_group: int = 0
     pair_count: int = 0
     pair_prefix: int = 0
+    query_len: int = 1             # query tokens per sequence per step (chunk workloads)
 
 
 def workload(name: str, seed: int = 0) -> Workload:
@@ -227,7 +233,16 @@ def workload(name: str, seed: int = 0) -> Workload:
     if name == "long70b":
         return Workload(name, "bf16", 64, 8, 128, 16, 512, 1.0 / math.sqrt(128), 1.0,
                         num_seqs=32, lengths=uniform_lengths(rng, 32, 8192, 32768))
+    if name == "verify8b":
+        ctx = lognormal_lengths(rng, 256, 600, 0.8, 1, 4096 - 5)
+        return Workload(name, "bf16", 32, 8, 128, 16, 512, 1.0, 1.0, q_prescale=1.0 / math.sqrt(128),
+                        num_seqs=256, lengths=ctx + 5, query_len=5)
+    if name == "prefill8b":
+        ctx = uniform_lengths(rng, 16, 0, 4096 - 512)
+        return Workload(name, "bf16", 32, 8, 128, 16, 512, 1.0, 1.0, q_prescale=1.0 / math.sqrt(128),
+                        num_seqs=16, lengths=ctx + 512, query_len=512)
     raise KeyError(name)
 
 
 WORKLOADS = ("tiny", "mha7b", "gqa8b_b16", "gqa8b_b32", "prefix_cow", "long70b")
+CHUNK_WORKLOADS = ("verify8b", "prefill8b")

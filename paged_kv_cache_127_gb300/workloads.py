@@ -9,6 +9,10 @@ A decode step is the whole hot path once:
          pa_decode(q over every sequence's full context).
 The step is idempotent (the same slots are rewritten with the same rows), so a
 benchmark can repeat it.
+
+Chunk workloads (``synth.CHUNK_WORKLOADS``) append query_len tokens to every
+sequence instead of one; the GPU step is then pa_write_kv of all S * query_len
+new rows followed by pa_chunk_attention over them (query_start = s * query_len).
 """
 from __future__ import annotations
 
@@ -33,9 +37,10 @@ class DecodeStep:
     scale: float
     free_order: np.ndarray     # the pool's initial free list
     tables: np.ndarray         # int32 [S, max_blocks] after the step's appends (pad -1)
-    lens: np.ndarray           # int32 [S] context lengths including the new token
-    slots: np.ndarray          # int64 [S] slot of each sequence's new token
+    lens: np.ndarray           # int32 [S] context lengths including the new token(s)
+    slots: np.ndarray          # int64 [S * query_len] slots of the new tokens, sequence-major
     pairs: np.ndarray          # int64 [P, 2] copy-on-write pairs of this step
+    query_len: int = 1         # new (query) tokens per sequence
     q: np.ndarray | None = None
     k_new: np.ndarray | None = None
     v_new: np.ndarray | None = None
@@ -68,13 +73,28 @@ class DecodeStep:
                     total += min(B, n - j * B)
         return total * self.kv_bytes_per_token()
 
+    @property
+    def num_tokens(self) -> int:
+        return self.num_seqs * self.query_len
+
+    def query_start(self) -> np.ndarray:
+        return (np.arange(self.num_seqs + 1) * self.query_len).astype(np.int32)
+
+    def chunk_flops(self) -> int:
+        """Attention FLOPs of a chunk step: 2 (q.k) + 2 (p.v) per head dimension,
+        per query head, per visible key; the query at position pos sees pos + 1 keys."""
+        n = self.query_len
+        vis = (self.lens.astype(np.int64)[:, None] - n + np.arange(n)[None, :] + 1).sum()
+        return int(4 * self.head_dim * self.num_q_heads * vis)
+
     def first(self, k: int) -> "DecodeStep":
         """The same step restricted to the first k sequences (pool unchanged)."""
         import copy
         sub = copy.copy(self)
-        sub.tables, sub.lens, sub.slots = self.tables[:k], self.lens[:k], self.slots[:k]
+        t = k * self.query_len
+        sub.tables, sub.lens, sub.slots = self.tables[:k], self.lens[:k], self.slots[:t]
         if self.q is not None:
-            sub.q, sub.k_new, sub.v_new = self.q[:k], self.k_new[:k], self.v_new[:k]
+            sub.q, sub.k_new, sub.v_new = self.q[:t], self.k_new[:t], self.v_new[:t]
         return sub
 
     def dims(self, binding):
@@ -88,7 +108,7 @@ def _max_len(w: synth.Workload) -> int:
         return 64
     if w.name == "mha7b":
         return 2048
-    if w.name.startswith("gqa8b"):
+    if w.name.startswith("gqa8b") or w.name in synth.CHUNK_WORKLOADS:
         return 4096
     if w.name == "prefix_cow":
         return w.prefix_len + 512 + 16
@@ -136,21 +156,21 @@ def build_step(name: str, seed: int = 0, values: bool = True, binding=None) -> D
     else:
         for n in w.lengths:
             s = binding.pa_seq_create(h)
-            binding.pa_seq_append(h, s, int(n) - 1)   # the context already cached
+            binding.pa_seq_append(h, s, int(n) - w.query_len)   # the context already cached
             seqs.append(s)
-    slots, pairs = binding.pa_seq_append_batch(h, seqs, 1)   # this step's new token
+    slots, pairs = binding.pa_seq_append_batch(h, seqs, w.query_len)   # this step's new tokens
     tables, lens = binding.pa_pool_export(h, seqs, max_blocks, -1)
     pool.close()
 
     step = DecodeStep(name=name, dtype=w.dtype, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
                       head_dim=w.head_dim, block_size=B, num_blocks=N, max_blocks=max_blocks,
                       partition_size=w.partition_size, scale=w.scale, free_order=order, tables=tables,
-                      lens=lens, slots=slots[:, 0].copy(), pairs=pairs)
+                      lens=lens, slots=slots.reshape(-1).copy(), pairs=pairs, query_len=w.query_len)
     if values:
-        S, Hq, Hkv, D = len(seqs), w.num_q_heads, w.num_kv_heads, w.head_dim
-        step.q = synth.normal(rng, (S, Hq, D), w.std * w.q_prescale, w.dtype)
-        step.k_new = synth.normal(rng, (S, Hkv, D), w.std, w.dtype)
-        step.v_new = synth.normal(rng, (S, Hkv, D), w.std, w.dtype)
+        T, Hq, Hkv, D = len(seqs) * w.query_len, w.num_q_heads, w.num_kv_heads, w.head_dim
+        step.q = synth.normal(rng, (T, Hq, D), w.std * w.q_prescale, w.dtype)
+        step.k_new = synth.normal(rng, (T, Hkv, D), w.std, w.dtype)
+        step.v_new = synth.normal(rng, (T, Hkv, D), w.std, w.dtype)
         step.k_cache = synth.normal(rng, (N, Hkv, B, D), w.std, w.dtype)
         step.v_cache = synth.normal(rng, (N, Hkv, B, D), w.std, w.dtype)
     return step

@@ -115,3 +115,47 @@ def test_write_and_copy_reject_bad_arguments_on_the_host(pa):
     assert pa.lib.pa_copy_blocks(ctypes.byref(d), ok, ok, ok, 0, None) == pa.PA_OK        # no-op
     bad = pa.make_dims(num_kv_heads=2, head_dim=4, block_size=16, num_blocks=8, kv_dtype="f16")
     assert pa.lib.pa_copy_blocks(ctypes.byref(bad), ok, ok, ok, 1, None) == pa.PA_ERR_UNSUPPORTED
+
+
+def test_chunk_workspace_bytes(pa):
+    def up(x):
+        return (x + 255) // 256 * 256
+
+    S, Hq, Hkv, D, T = 64, 32, 8, 128, 320
+    d = pa.make_dims(num_seqs=S, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, block_size=16,
+                     num_blocks=1000, max_blocks_per_seq=256, partition_size=512, kv_dtype="bf16")
+    P = (256 * 16 + 511) // 512
+    # five queries per sequence, G = 4: 20 rows -> two 16-row tiles, one row block of two
+    R = 1
+    expect = 256 + up(S * P * R * 16) + up(T * 4) + up(T * Hq * P * D * 4) + up(T * Hq * P * 2 * 4)
+    assert pa.pa_chunk_workspace_bytes(d, T, 5) == expect
+    # four queries: 16 rows, one tile per block; 64 queries: 256 rows in blocks of 32 -> 8 blocks
+    assert pa.pa_chunk_workspace_bytes(d, T, 4) == 256 + up(S * P * 16) + up(T * 4) + \
+        up(T * Hq * P * D * 4) + up(T * Hq * P * 2 * 4)
+    assert pa.pa_chunk_workspace_bytes(d, T, 64) == 256 + up(S * P * 8 * 16) + up(T * 4) + \
+        up(T * Hq * P * D * 4) + up(T * Hq * P * 2 * 4)
+    d.max_blocks_per_seq = 32            # one partition: no partials
+    assert pa.pa_chunk_workspace_bytes(d, T, 5) == 256 + up(S * 16) + up(T * 4)
+    assert pa.pa_chunk_workspace_bytes(d, T, 0) == 0          # max_query_len < 1
+    assert pa.pa_chunk_workspace_bytes(d, -1, 5) == 0
+    d.kv_dtype = pa.PA_F32                                      # tensor-core path only
+    assert pa.pa_chunk_workspace_bytes(d, T, 5) == 0
+
+
+def test_chunk_rejects_bad_arguments_on_the_host(pa):
+    def status(T=4, max_q=2, ws=None, ws_bytes=0, **over):
+        kw = dict(num_seqs=2, num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16, num_blocks=8,
+                  max_blocks_per_seq=4, partition_size=0, kv_dtype="bf16")
+        kw.update(over)
+        d = pa.make_dims(**kw)
+        fake = ctypes.c_void_p(0x10000)
+        return pa.lib.pa_chunk_attention(ctypes.byref(d), fake, fake, fake, fake, fake, fake, T, max_q, 1.0,
+                                         fake, ws, ws_bytes, None)
+    assert status(kv_dtype="f32") == pa.PA_ERR_UNSUPPORTED
+    assert status(head_dim=96) == pa.PA_ERR_UNSUPPORTED
+    assert status(num_q_heads=7) == pa.PA_ERR_INVALID
+    assert status(max_q=0) == pa.PA_ERR_INVALID
+    assert status(T=-3) == pa.PA_ERR_INVALID
+    assert status() == pa.PA_ERR_INVALID                        # no workspace
+    assert status(T=0) == pa.PA_OK                              # nothing to do
+    assert status(num_seqs=0) == pa.PA_OK
