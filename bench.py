@@ -49,6 +49,8 @@ FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 126 * 2**20
 KERNEL_SOURCES = ("pa_decode_mma.cuh", "pa_plan.cu", "pa_cache_ops.cu", "pa_tmap.cu", "pa_api.cu",
                   "pa_device.cuh", "pa_internal.h", "pa_mma.cuh")
+CHUNK_SOURCES = ("pa_chunk_mma.cuh", "pa_chunk.cu", "pa_tmap.cu", "pa_api.cu", "pa_device.cuh", "pa_internal.h",
+                 "pa_mma.cuh")
 
 
 # --------------------------------------------------------------------------- distributed helpers
@@ -95,23 +97,23 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in sources:
         with open(os.path.join(ROOT, "paged_kv_cache_127_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """ncu DRAM bytes per decode launch, if the summary matches the current kernel sources."""
-    path = os.path.join(ROOT, "profiles", f"decode_{workload}.md")
+def profiled_traffic(workload: str, kind: str = "decode", sources=KERNEL_SOURCES):
+    """ncu DRAM bytes per call, if the summary matches the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"{kind}_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
         return None
     m = re.search(r"traffic_bytes_per_launch:\s*(\d+)\s+sources:\s*([0-9a-f]+)", text)
-    if not m or m.group(2) != kernel_source_hash():
+    if not m or m.group(2) != kernel_source_hash(sources):
         return None
     return int(m.group(1))
 
@@ -478,7 +480,8 @@ def run_chunk(args):
              "frac": round(gbs / hbm_peak, 4)} if hbm_bound else
             {"bound": "tensor", "achieved": round(tfs, 2), "peak": tc_peak, "peak_kind": tc_kind, "unit": "TFLOP/s",
              "frac": round(tfs / tc_peak, 4)})
-    roof.update({"traffic": None, "kernel": "pa_chunk_attention (plan + tensor-core chunk kernel + merge)",
+    roof.update({"traffic": profiled_traffic(args.workload, "chunk", CHUNK_SOURCES),
+                 "kernel": "pa_chunk_attention (plan + tensor-core chunk kernel + merge)",
                  "call_ms": round(call_ms, 5),
                  "bytes": "distinct visible KV slots per call", "flops": "4 * D * Hq per (query, visible key)"})
     line = {
