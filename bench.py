@@ -49,8 +49,8 @@ FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 126 * 2**20
 KERNEL_SOURCES = ("pa_decode_mma.cuh", "pa_plan.cu", "pa_cache_ops.cu", "pa_tmap.cu", "pa_api.cu",
                   "pa_device.cuh", "pa_internal.h", "pa_mma.cuh")
-CHUNK_SOURCES = ("pa_chunk_mma.cuh", "pa_chunk.cu", "pa_tmap.cu", "pa_api.cu", "pa_device.cuh", "pa_internal.h",
-                 "pa_mma.cuh")
+CHUNK_SOURCES = ("pa_chunk_mma.cuh", "pa_chunk_umma.cuh", "pa_tcgen05.cuh", "pa_chunk.cu", "pa_tmap.cu", "pa_api.cu",
+                 "pa_device.cuh", "pa_internal.h", "pa_mma.cuh")
 
 
 # --------------------------------------------------------------------------- distributed helpers
@@ -435,7 +435,9 @@ def run_chunk(args):
     d_out = torch.empty((T, Hq, D), dtype=torch.float32, device=device)
     ws = torch.empty(max(pa.pa_chunk_workspace_bytes(dims, T, n), 16), dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
-    split = step.max_blocks * step.block_size > step.partition_size
+    G = Hq // step.num_kv_heads
+    umma = n * G >= 64                                # long chunks: the tcgen05 kernel, no split-K merge
+    split = step.max_blocks * step.block_size > step.partition_size and not umma
     launches_per_step = 1 + 2 + (1 if split else 0)   # write_kv, plan, chunk kernel, merge
     ev = []
 
@@ -481,7 +483,8 @@ def run_chunk(args):
             {"bound": "tensor", "achieved": round(tfs, 2), "peak": tc_peak, "peak_kind": tc_kind, "unit": "TFLOP/s",
              "frac": round(tfs / tc_peak, 4)})
     roof.update({"traffic": profiled_traffic(args.workload, "chunk", CHUNK_SOURCES),
-                 "kernel": "pa_chunk_attention (plan + tensor-core chunk kernel + merge)",
+                 "kernel": ("pa_chunk_attention (plan + tcgen05 chunk kernel)" if umma else
+                            "pa_chunk_attention (plan + mma.sync chunk kernel + split-K merge)"),
                  "call_ms": round(call_ms, 5),
                  "bytes": "distinct visible KV slots per call", "flops": "4 * D * Hq per (query, visible key)"})
     line = {

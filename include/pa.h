@@ -185,12 +185,18 @@ PA_API int32_t pa_decode_noalloc(const pa_dims *dims, const void *q, const void 
  * PA_DEVERR_BAD_LEN is set; a query_start that is not non-decreasing within
  * [0, T] skips every sequence and sets PA_DEVERR_BAD_LEN.
  *
+ * Two kernels serve it: while max_query_len * Hq / Hkv (query rows per KV
+ * head) is below 64, a persistent mma.sync kernel over context partitions
+ * with a split-K merge; from 64 rows on, a tcgen05 kernel with 128-row tiles
+ * whose accumulators live in tensor memory, one CTA per (tile, KV head,
+ * sequence), walking each tile's whole context (no partitions, no merge).
+ *
  * pa_chunk_workspace_bytes -- the scratch it needs: a work list of S * P * R
  * int4 entries after a 256-byte header, a token-to-sequence map of T ints,
- * and for P > 1 the split-K partials T * Hq * P * (D + 2) floats, each part
- * rounded up to 256 bytes; P as for pa_decode, R = ceil(ceil(max_query_len *
- * Hq / Hkv / 16) / W), W = 2 if max_query_len * Hq / Hkv > 16, else 1.
- * Returns 0 for invalid arguments.
+ * and, on the mma.sync path with P > 1, the split-K partials T * Hq * P *
+ * (D + 2) floats, each part rounded up to 256 bytes; P as for pa_decode,
+ * R = ceil(ceil(max_query_len * Hq / Hkv / 16) / W), W = 2 if max_query_len *
+ * Hq / Hkv > 16, else 1.  Returns 0 for invalid arguments.
  */
 PA_API size_t pa_chunk_workspace_bytes(const pa_dims *dims, int32_t num_tokens, int32_t max_query_len);
 PA_API int32_t pa_chunk_attention(const pa_dims *dims, const void *q, const void *k_cache,

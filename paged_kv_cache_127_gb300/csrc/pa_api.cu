@@ -109,6 +109,7 @@ int32_t check_chunk_dims(const pa_dims *d, int32_t T, int32_t max_q, int32_t *ma
     if (d->kv_dtype == PA_F32) return PA_ERR_UNSUPPORTED;
     if (T < 0 || max_q < 1 || max_q > (1 << 20)) return PA_ERR_INVALID;
     if ((int64_t)T * d->num_q_heads > INT32_MAX) return PA_ERR_INVALID;
+    if (d->num_seqs > 65535) return PA_ERR_INVALID;  // the tcgen05 grid's z extent
     return PA_OK;
 }
 
@@ -132,10 +133,12 @@ ChunkLayout chunk_layout(const pa_dims *d, int32_t T, int32_t max_q, int32_t max
     off += up((size_t)d->num_seqs * max_parts * R * 4 * sizeof(int));
     L.tok = off;
     off += up((size_t)T * sizeof(int32_t));
+    // split-K partials only on the mma.sync path (the tcgen05 path walks a tile's whole context)
+    const bool partials = max_parts > 1 && !pa::chunk_uses_umma(max_q, (int)G);
     L.acc = off;
-    off += max_parts > 1 ? up((size_t)T * d->num_q_heads * max_parts * d->head_dim * sizeof(float)) : 0;
+    off += partials ? up((size_t)T * d->num_q_heads * max_parts * d->head_dim * sizeof(float)) : 0;
     L.ml = off;
-    off += max_parts > 1 ? up((size_t)T * d->num_q_heads * max_parts * 2 * sizeof(float)) : 0;
+    off += partials ? up((size_t)T * d->num_q_heads * max_parts * 2 * sizeof(float)) : 0;
     L.total = off;
     return L;
 }
@@ -316,15 +319,21 @@ int32_t pa_chunk_attention(const pa_dims *dims, const void *q, const void *k_cac
     a.scale = scale;
 
     const bool bf16 = dims->kv_dtype == PA_BF16;
+    const bool umma = pa::chunk_uses_umma(max_query_len, dims->num_q_heads / dims->num_kv_heads);
+    const int box_heads = umma ? 1 : a.head_group;
     const long long block_heads = (long long)dims->num_blocks * dims->num_kv_heads;
     CUtensorMap tmk, tmv;
-    cudaError_t e = cache_tensor_map(k_cache, bf16, dims->head_dim, dims->block_size, block_heads, a.head_group, &tmk);
+    cudaError_t e = cache_tensor_map(k_cache, bf16, dims->head_dim, dims->block_size, block_heads, box_heads, &tmk);
     if (e == cudaSuccess)
-        e = cache_tensor_map(v_cache, bf16, dims->head_dim, dims->block_size, block_heads, a.head_group, &tmv);
+        e = cache_tensor_map(v_cache, bf16, dims->head_dim, dims->block_size, block_heads, box_heads, &tmv);
     if (e != cudaSuccess) return PA_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     e = pa::launch_chunk_plan(a, st);
     if (e != cudaSuccess) return to_status(e);
+    if (umma) {
+        e = bf16 ? pa::launch_chunk_umma_bf16(a, tmk, tmv, st) : pa::launch_chunk_umma_f16(a, tmk, tmv, st);
+        return to_status(e);
+    }
     e = bf16 ? pa::launch_chunk_mma_bf16(a, tmk, tmv, st) : pa::launch_chunk_mma_f16(a, tmk, tmv, st);
     if (e != cudaSuccess) return to_status(e);
     if (parts > 1) e = pa::launch_chunk_merge(a, st);

@@ -380,22 +380,33 @@ __global__ void __launch_bounds__(ChunkCfg<D, HG, RW>::kThreads, ChunkCfg<D, HG,
                     mlo = (c2 < nv ? 0x0000ffffu : 0u) | (c2 + 1 < nv ? 0xffff0000u : 0u);
                     mhi = (c2 + 8 < nv ? 0x0000ffffu : 0u) | (c2 + 9 < nv ? 0xffff0000u : 0u);
                 }
-                // ---- O += P_hi V + P_lo V
+                // ---- O += P_hi V + P_lo V, two 16-column groups at a time so that the
+                // two MMAs into one accumulator are four issues apart
 #pragma unroll
-                for (int ntp = 0; ntp < C::kNT / 2; ++ntp) {
-                    const uint32_t addr = vst + (uint32_t)((ntp >> 2) * C::kBoxBytes) +
-                                          (uint32_t)(((lm & 1) * 8 + lr) * 128) +
-                                          (((uint32_t)(2 * (ntp & 3)) ^ vx) << 4);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(addr, b0, b1, b2, b3);
-                    b0 &= mlo;
-                    b1 &= mhi;
-                    b2 &= mlo;
-                    b3 &= mhi;
-                    M::mma(o[2 * ntp], h0a, h1a, h0b, h1b, b0, b1);
-                    M::mma(o[2 * ntp], l0a, l1a, l0b, l1b, b0, b1);
-                    M::mma(o[2 * ntp + 1], h0a, h1a, h0b, h1b, b2, b3);
-                    M::mma(o[2 * ntp + 1], l0a, l1a, l0b, l1b, b2, b3);
+                for (int ntq = 0; ntq < C::kNT / 4; ++ntq) {
+                    uint32_t b[2][4];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int ntp = 2 * ntq + u;
+                        const uint32_t addr = vst + (uint32_t)((ntp >> 2) * C::kBoxBytes) +
+                                              (uint32_t)(((lm & 1) * 8 + lr) * 128) +
+                                              (((uint32_t)(2 * (ntp & 3)) ^ vx) << 4);
+                        ldsm_x4_t(addr, b[u][0], b[u][1], b[u][2], b[u][3]);
+                        b[u][0] &= mlo;
+                        b[u][1] &= mhi;
+                        b[u][2] &= mlo;
+                        b[u][3] &= mhi;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        M::mma(o[4 * ntq + 2 * u], h0a, h1a, h0b, h1b, b[u][0], b[u][1]);
+                        M::mma(o[4 * ntq + 2 * u + 1], h0a, h1a, h0b, h1b, b[u][2], b[u][3]);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        M::mma(o[4 * ntq + 2 * u], l0a, l1a, l0b, l1b, b[u][0], b[u][1]);
+                        M::mma(o[4 * ntq + 2 * u + 1], l0a, l1a, l0b, l1b, b[u][2], b[u][3]);
+                    }
                 }
             }
             fence_proxy_async_smem();

@@ -1,0 +1,452 @@
+// pa_chunk_umma.cuh -- chunk attention for long query chunks (chunked prefill)
+// on the 5th-generation tensor cores: tcgen05.mma with operands in shared
+// memory and the accumulators in tensor memory (TMEM).
+//
+// What is computed is what pa_chunk_mma.cuh computes (the query at position
+// pos = len_s - n_s + t attends to keys 0..pos; "Paged Attention and vLLM",
+// "KV Cache Fundamentals" and "Block Table and Logical-to-Physical Mapping"),
+// for chunks whose (query token, query head) rows fill 128-row tiles.
+//
+// Work: one CTA per (128-row tile, KV head, sequence); the rows of a KV head
+// are r = t * G + gq.  The CTA walks the visible context in 64-key steps, with
+// no split across CTAs (a tile has enough rows to keep the tensor cores busy),
+// so there is no merge.  Warp roles:
+//   warp 0       producer: 16-row TMA boxes of K and V (one KV head, both
+//                128-byte halves of D) into a 3-stage ring; table entries
+//                outside the pool, or keys past the context, are not loaded
+//                and are marked in a per-stage mask;
+//   warp 1       allocates 256 TMEM columns and issues the MMAs (lane 0):
+//                  S_j = Q K_j^T      M 128, N 64,  K = D    -> TMEM S[j % 2]
+//                  O  += P_j V_j      M 128, N = D, K 64     -> TMEM O
+//                with P_j split into P_hi + P_lo (two bf16 / f16 operands) so
+//                the probabilities keep ~16 significant bits;
+//   warps 4..7   softmax, one thread per row (TMEM lane): read S_j, mask
+//                (causal and not-loaded keys), online softmax in log2 units,
+//                write P_hi / P_lo to shared memory, zero the V rows of keys
+//                that must not contribute (their slots may hold anything);
+//                epilogue O / l to out[].
+// The running maximum is only moved when a row's new maximum exceeds it by
+// more than 2^8 (exp2 units): until then the weights are exp2(x - m) <= 256,
+// exact in fp32, and O and l share the stale maximum, so the result is the
+// same softmax; moving it costs a read-modify-write of the row of O in TMEM.
+//
+// Synchronisation is by mbarriers only, every wait bounded: on a timeout the
+// kernel sets PA_DEVERR_TIMEOUT, waits (bounded) for the MMAs and copies it
+// issued, frees its TMEM and returns.
+#pragma once
+
+#include <cuda.h>
+
+#include <cmath>
+#include <type_traits>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+#include "pa_mma.cuh"
+#include "pa_tcgen05.cuh"
+
+namespace pa {
+
+template <int D>
+struct UmmaCfg {
+    static constexpr int kM = 128;                         // rows per tile (TMEM lanes)
+    static constexpr int kN = 64;                          // keys per step
+    static constexpr int kBoxes = kN / 16;                 // 16-row TMA boxes per step
+    static constexpr int kSub = D / 64;                    // 128-byte halves of a row
+    static constexpr int kKS = D / 16;                     // k-steps of S = Q K^T
+    static constexpr int kStages = 3;
+    static constexpr int kHalf = kN * 128;                 // one half of K (or V) of a step
+    static constexpr int kTile = kSub * kHalf;             // K (or V) of a step
+    static constexpr int kStageBytes = 2 * kTile;
+    static constexpr int kQHalf = kM * 128;
+    static constexpr int kPPart = kM * kN * 2;             // one of P_hi / P_lo
+    static constexpr size_t kQOff = 0;
+    static constexpr size_t kPOff = kQOff + (size_t)kSub * kQHalf;
+    static constexpr size_t kKVOff = kPOff + 4 * (size_t)kPPart;   // 2 buffers x (hi, lo)
+    static constexpr size_t kBarOff = kKVOff + (size_t)kStages * kStageBytes;
+    // barriers: kv_full[3] kv_empty[3] s_full[2] s_free[2] p_full[2] o_done[2] q_full drain
+    static constexpr int kNumBars = 2 * kStages + 8 + 2;
+    static constexpr size_t kMaskOff = kBarOff + 8 * kNumBars;
+    static constexpr size_t kSlotOff = kMaskOff + 4 * kStages;
+    static constexpr size_t kSmem = kSlotOff + 16 + 1024;  // + alignment slack
+    static constexpr uint32_t kTmemCols = 256;             // S[2] (2 x 64) + O (D <= 128)
+    static constexpr uint32_t kSCol = 0;
+    static constexpr uint32_t kOCol = 2 * kN;
+    static_assert(D == 64 || D == 128, "head_dim");
+    static_assert(kOCol + D <= kTmemCols, "TMEM budget");
+    static_assert(kPOff % 1024 == 0 && kKVOff % 1024 == 0, "swizzle atoms 1024-byte aligned");
+    static_assert(kSmem <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+template <typename T, int D, int B>
+__global__ void __launch_bounds__(256, 1)
+    chunk_umma_kernel(const ChunkArgs a, const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmv) {
+    using C = UmmaCfg<D>;
+    using M = Mma16<T>;
+    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char *basep = smem_raw + (base - raw);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    griddep_wait();  // the plan kernel has validated the query ranges (tok_seq)
+    const int s = blockIdx.z;
+    const int kvh = blockIdx.y;
+    const int G = a.Hq / a.Hkv;
+    const int r0 = blockIdx.x * C::kM;
+    const int qs = a.query_start[s];
+    const int n = a.query_start[s + 1] - qs;
+    if (n <= 0 || r0 >= n * G || a.tok_seq[qs] != s) return;  // nothing here, or a skipped sequence
+    const int len = a.context_lens[s];
+    const int t_last = min(n - 1, (r0 + C::kM - 1) / G);
+    const int nch = (len - n + t_last) / C::kN + 1;           // 64-key steps up to the tile's last position
+
+    const uint32_t qb = base + (uint32_t)C::kQOff;
+    const uint32_t pb = base + (uint32_t)C::kPOff;
+    const uint32_t kvb = base + (uint32_t)C::kKVOff;
+    const uint32_t bars = base + (uint32_t)C::kBarOff;
+    auto kv_full = [&](int i) { return bars + 8u * (uint32_t)i; };
+    auto kv_empty = [&](int i) { return bars + 8u * (uint32_t)(C::kStages + i); };
+    auto s_full = [&](int i) { return bars + 8u * (uint32_t)(2 * C::kStages + i); };
+    auto s_free = [&](int i) { return bars + 8u * (uint32_t)(2 * C::kStages + 2 + i); };
+    auto p_full = [&](int i) { return bars + 8u * (uint32_t)(2 * C::kStages + 4 + i); };
+    auto o_done = [&](int i) { return bars + 8u * (uint32_t)(2 * C::kStages + 6 + i); };
+    const uint32_t q_full = bars + 8u * (uint32_t)(2 * C::kStages + 8);
+    const uint32_t drain = bars + 8u * (uint32_t)(2 * C::kStages + 9);
+    int *vmask = reinterpret_cast<int *>(basep + C::kMaskOff);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(basep + C::kSlotOff);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::kStages; ++i) {
+            mbar_init(kv_full(i), 1);
+            mbar_init(kv_empty(i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(s_full(i), 1);
+            mbar_init(s_free(i), 4);
+            mbar_init(p_full(i), 4);
+            mbar_init(o_done(i), 1);
+        }
+        mbar_init(q_full, 4);
+        mbar_init(drain, 1);
+        fence_mbar_init();
+        prefetch_tmap(&tmk);
+        prefetch_tmap(&tmv);
+    }
+    if (warp == 1) tc::tmem_alloc(smem_addr(tslot), C::kTmemCols);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tbase = *tslot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        const int32_t *row = a.block_tables + (size_t)s * a.max_blocks;
+        const uint64_t pol = policy_evict_last();  // the other row tiles of this head reread these keys
+        int j = 0;
+        for (; j < nch; ++j) {
+            const int st = j % C::kStages;
+            if (j >= C::kStages &&
+                !mbar_wait_bounded(kv_empty(st), (uint32_t)((j / C::kStages) - 1) & 1u, kWaitLimit)) {
+                if (lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
+                break;
+            }
+            if (lane == 0) {
+                int mask = 0, blk[C::kBoxes];
+#pragma unroll
+                for (int i = 0; i < C::kBoxes; ++i) {
+                    const int tok = j * C::kN + 16 * i;
+                    blk[i] = -1;
+                    if (tok < len) {
+                        const int pbk = row[tok / B];
+                        if (pbk >= 0 && pbk < a.N) {
+                            blk[i] = pbk;
+                            mask |= 1 << i;
+                        } else {
+                            set_error(a.err, PA_DEVERR_BAD_BLOCK);
+                        }
+                    }
+                }
+                vmask[st] = mask;
+                const uint32_t bar = kv_full(st);
+                const uint32_t bytes = (uint32_t)__popc(mask) * 2u * C::kSub * 2048u;
+                if (bytes == 0) {
+                    mbar_arrive(bar);
+                } else {
+                    mbar_arrive_expect_tx(bar, bytes);
+                    const uint32_t kst = kvb + (uint32_t)(st * C::kStageBytes);
+#pragma unroll
+                    for (int i = 0; i < C::kBoxes; ++i) {
+                        if (!(mask >> i & 1)) continue;
+                        const int y = (j * C::kN + 16 * i) % B;
+                        const int z = blk[i] * a.Hkv + kvh;
+#pragma unroll
+                        for (int sb = 0; sb < C::kSub; ++sb) {
+                            const uint32_t off = (uint32_t)(sb * C::kHalf + i * 2048);
+                            tma_load_3d(kst + off, &tmk, sb * 64, y, z, bar, pol);
+                            tma_load_3d(kst + C::kTile + off, &tmv, sb * 64, y, z, bar, pol);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+        }
+        // copies still in flight must land before the CTA's shared memory is released
+        for (int k = max(0, j - C::kStages); k < j; ++k)
+            mbar_wait_bounded(kv_full(k % C::kStages), (uint32_t)(k / C::kStages) & 1u, kWaitLimit);
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        constexpr uint32_t idesc_s = tc::f16_idesc(kBf16, false, C::kM, C::kN);
+        constexpr uint32_t idesc_o = tc::f16_idesc(kBf16, true, C::kM, D);
+        bool ok = mbar_wait_bounded(q_full, 0u, kWaitLimit);
+        auto pv = [&](int c) {
+            if (!mbar_wait_bounded(p_full(c & 1), (uint32_t)(c >> 1) & 1u, kWaitLimit)) return false;
+            tc::fence_after_sync();
+            if (lane == 0) {
+                const uint32_t vst = kvb + (uint32_t)((c % C::kStages) * C::kStageBytes + C::kTile);
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    const uint32_t pa_ = pb + (uint32_t)(((c & 1) * 2 + part) * C::kPPart);
+#pragma unroll
+                    for (int k = 0; k < C::kN / 16; ++k) {
+                        const uint64_t ad = tc::sw128_desc(pa_ + 32u * k, 16u, 1024u);
+                        const uint64_t bd = tc::sw128_desc(vst + 2048u * k, (uint32_t)C::kHalf, 1024u);
+                        tc::mma_f16_ss(tbase + C::kOCol, ad, bd, idesc_o, (c > 0 || part > 0 || k > 0) ? 1u : 0u);
+                    }
+                }
+                tc::mma_commit(o_done(c & 1));
+                tc::mma_commit(kv_empty(c % C::kStages));
+            }
+            __syncwarp();
+            return true;
+        };
+        int j = 0;
+        for (; ok && j < nch; ++j) {
+            const int st = j % C::kStages;
+            const int b = j & 1;
+            ok = mbar_wait_bounded(kv_full(st), (uint32_t)(j / C::kStages) & 1u, kWaitLimit);
+            if (ok && j >= 2) ok = mbar_wait_bounded(s_free(b), (uint32_t)((j >> 1) - 1) & 1u, kWaitLimit);
+            if (!ok) break;
+            tc::fence_after_sync();
+            if (lane == 0) {
+                const uint32_t kst = kvb + (uint32_t)(st * C::kStageBytes);
+#pragma unroll
+                for (int k = 0; k < C::kKS; ++k) {
+                    const uint64_t ad = tc::sw128_desc(qb + (uint32_t)((k >> 2) * C::kQHalf) + 32u * (k & 3), 16u, 1024u);
+                    const uint64_t bd = tc::sw128_desc(kst + (uint32_t)((k >> 2) * C::kHalf) + 32u * (k & 3), 16u, 1024u);
+                    tc::mma_f16_ss(tbase + C::kSCol + (uint32_t)(b * C::kN), ad, bd, idesc_s, k > 0 ? 1u : 0u);
+                }
+                tc::mma_commit(s_full(b));
+            }
+            __syncwarp();
+            if (j >= 1 && !(ok = pv(j - 1))) break;
+        }
+        if (ok && nch >= 1) ok = pv(nch - 1);
+        if (!ok && lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
+        // every MMA issued by this thread has completed before TMEM is freed
+        if (lane == 0) tc::mma_commit(drain);
+        __syncwarp();
+        mbar_wait_bounded(drain, 0u, kWaitLimit);
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax (one row per thread)
+        const int r = threadIdx.x - 128;
+        const int wq = warp - 4;  // TMEM lanes 32 * wq .. 32 * wq + 31
+        const int R = r0 + r;
+        const int t = R / G;
+        const bool valid = t < n;
+        const int h = kvh * G + R % G;
+        const int pos = len - n + t;
+        const float sl = a.scale * 1.4426950408889634f;
+        {
+            // Q row -> shared memory, 128-byte swizzle (16-byte chunk c of row r at c ^ (r & 7))
+            const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.q) +
+                                                               ((size_t)(qs + (valid ? t : 0)) * a.Hq + h) * D);
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) {
+                const uint4 v = valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+                const uint32_t addr = qb + (uint32_t)((c >> 3) * C::kQHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+                             "r"(v.w)
+                             : "memory");
+            }
+            tc::fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_full);
+        }
+        const uint32_t tl = tbase + ((uint32_t)(wq * 32) << 16);
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nch; ++j) {
+            const int b = j & 1;
+            const int st = j % C::kStages;
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(s_full(b), (uint32_t)(j >> 1) & 1u, kWaitLimit));
+            if (!ok) break;
+            tc::fence_after_sync();
+            uint32_t sv[2][32];
+            tc::tmem_ld32(tl + C::kSCol + (uint32_t)(b * C::kN), sv[0]);
+            tc::tmem_ld32(tl + C::kSCol + (uint32_t)(b * C::kN + 32), sv[1]);
+            tc::tmem_wait_ld();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_free(b));
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(kv_full(st), (uint32_t)(j / C::kStages) & 1u, kWaitLimit));
+            if (!ok) break;
+            const int mask = vmask[st];
+            const int lim = valid ? pos - j * C::kN : -1;  // last visible key of this step
+            float x[C::kN];
+            float mc = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < C::kN; ++c) {
+                const bool vis = c <= lim && (mask >> (c >> 4) & 1);
+                x[c] = vis ? __uint_as_float(sv[c >> 5][c & 31]) * sl : -INFINITY;
+                mc = fmaxf(mc, x[c]);
+            }
+            const bool need = mc > m_used + 8.f;
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+                // move the row's maximum: every earlier P V must have landed in O
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait_bounded(o_done((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u, kWaitLimit));
+                if (!ok) break;
+                tc::fence_after_sync();
+                const float alpha = need ? ex2(m_used - mc) : 1.f;
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q) {
+                    uint32_t ov[32];
+                    tc::tmem_ld32(tl + C::kOCol + 32u * q, ov);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                    tc::tmem_st32(tl + C::kOCol + 32u * q, ov);
+                }
+                tc::tmem_wait_st();
+                l *= alpha;
+            }
+            if (need) m_used = mc;
+            const float mu = m_used == -INFINITY ? 0.f : m_used;
+            if (j >= 2) {  // P buffer b is free once the P V of step j - 2 has completed
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_done(b), (uint32_t)((j - 2) >> 1) & 1u, kWaitLimit));
+                if (!ok) break;
+            }
+            const uint32_t ph = pb + (uint32_t)((b * 2) * C::kPPart) + (uint32_t)(r * 128);
+            const uint32_t plo = ph + (uint32_t)C::kPPart;
+#pragma unroll
+            for (int c8 = 0; c8 < C::kN / 8; ++c8) {
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float p0 = ex2(x[c8 * 8 + 2 * u] - mu);
+                    const float p1 = ex2(x[c8 * 8 + 2 * u + 1] - mu);
+                    l += p0 + p1;
+                    hw[u] = M::pack(p0, p1);
+                    const float2 f = M::unpack(hw[u]);
+                    lw[u] = M::pack(p0 - f.x, p1 - f.y);
+                }
+                const uint32_t off = (uint32_t)((c8 ^ (r & 7)) << 4);
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(ph + off), "r"(hw[0]), "r"(hw[1]),
+                             "r"(hw[2]), "r"(hw[3])
+                             : "memory");
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(plo + off), "r"(lw[0]), "r"(lw[1]),
+                             "r"(lw[2]), "r"(lw[3])
+                             : "memory");
+            }
+            // V rows of keys that were not loaded or lie past the context hold
+            // anything: zero them (row r < 64 of this step's V), whole 128-byte rows
+            if (r < C::kN && (j * C::kN + r >= len || !(mask >> (r >> 4) & 1))) {
+                const uint32_t vrow = kvb + (uint32_t)(st * C::kStageBytes + C::kTile + r * 128);
+#pragma unroll
+                for (int sb = 0; sb < C::kSub; ++sb)
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vrow + sb * C::kHalf + c * 16),
+                                     "r"(0u)
+                                     : "memory");
+            }
+            tc::fence_async_smem();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full(b));
+        }
+        if (!ok) {
+            if (lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
+        } else if (__all_sync(0xffffffffu, mbar_wait_bounded(o_done((nch - 1) & 1),
+                                                              (uint32_t)((nch - 1) >> 1) & 1u, kWaitLimit))) {
+            // ---- epilogue: out = O / l for this row
+            tc::fence_after_sync();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            float *orow = a.out + ((size_t)(qs + (valid ? t : 0)) * a.Hq + h) * D;
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+                uint32_t ov[32];
+                tc::tmem_ld32(tl + C::kOCol + 32u * q, ov);
+                tc::tmem_wait_ld();
+                if (valid) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        *reinterpret_cast<float4 *>(orow + 32 * q + i) =
+                            make_float4(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv,
+                                        __uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv);
+                }
+            }
+            tc::fence_before_sync();
+        } else if (lane == 0) {
+            set_error(a.err, PA_DEVERR_TIMEOUT);
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tbase, C::kTmemCols);
+    }
+}
+
+template <typename T, int D, int B>
+cudaError_t launch_chunk_umma_t(const ChunkArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                                cudaStream_t st) {
+    using C = UmmaCfg<D>;
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(chunk_umma_kernel<T, D, B>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)C::kSmem);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    const int G = a.Hq / a.Hkv;
+    const int tiles = (int)(((long long)a.max_query_len * G + C::kM - 1) / C::kM);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)tiles, (unsigned)a.Hkv, (unsigned)a.S);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, chunk_umma_kernel<T, D, B>, a, tmk, tmv);
+}
+
+template <typename T>
+cudaError_t dispatch_chunk_umma(const ChunkArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                                cudaStream_t st) {
+    if (a.D == 64 && a.B == 16) return launch_chunk_umma_t<T, 64, 16>(a, tmk, tmv, st);
+    if (a.D == 64 && a.B == 32) return launch_chunk_umma_t<T, 64, 32>(a, tmk, tmv, st);
+    if (a.D == 128 && a.B == 16) return launch_chunk_umma_t<T, 128, 16>(a, tmk, tmv, st);
+    if (a.D == 128 && a.B == 32) return launch_chunk_umma_t<T, 128, 32>(a, tmk, tmv, st);
+    return cudaErrorNotSupported;
+}
+
+}  // namespace pa

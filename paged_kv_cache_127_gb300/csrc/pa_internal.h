@@ -51,6 +51,16 @@ struct ChunkArgs {
 // a sequence can have more than 16 (query token, query head) rows, else one.
 inline int chunk_row_warps(int max_query_len, int G) { return (long long)max_query_len * G > 16 ? 2 : 1; }
 
+// Chunk attention on the tcgen05 path: when a sequence can have at least this
+// many (query token, query head) rows per KV head, 128-row tiles with the
+// accumulators in tensor memory replace the mma.sync kernel (and its split-K).
+#ifndef PA_CHUNK_UMMA_MIN_ROWS
+#define PA_CHUNK_UMMA_MIN_ROWS 64
+#endif
+inline bool chunk_uses_umma(int max_query_len, int G) {
+    return (long long)max_query_len * G >= PA_CHUNK_UMMA_MIN_ROWS;
+}
+
 // KV heads that one tensor-core work item (one CTA) covers: PA_MMA_HEAD_GROUP
 // (4 by default) when they divide Hkv, else the largest power of two that does.
 #ifndef PA_MMA_HEAD_GROUP
@@ -100,6 +110,12 @@ cudaError_t launch_chunk_mma_f16(const ChunkArgs &a, const CUtensorMap &tmk, con
 cudaError_t launch_chunk_mma_bf16(const ChunkArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                   cudaStream_t st);
 cudaError_t launch_chunk_merge(const ChunkArgs &a, cudaStream_t st);
+// tcgen05 path: one CTA per (128-row tile, KV head, sequence); tensor maps with
+// one (block, head) per box (make_cache_tensor_map with head_group 1).
+cudaError_t launch_chunk_umma_f16(const ChunkArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                                  cudaStream_t st);
+cudaError_t launch_chunk_umma_bf16(const ChunkArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                                   cudaStream_t st);
 
 cudaError_t launch_write_kv(const void *k, const void *v, const int64_t *slots, int T, int Hkv,
                             int row_bytes, int B, int N, void *k_cache, void *v_cache,

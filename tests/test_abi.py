@@ -132,8 +132,11 @@ def test_chunk_workspace_bytes(pa):
     # four queries: 16 rows, one tile per block; 64 queries: 256 rows in blocks of 32 -> 8 blocks
     assert pa.pa_chunk_workspace_bytes(d, T, 4) == 256 + up(S * P * 16) + up(T * 4) + \
         up(T * Hq * P * D * 4) + up(T * Hq * P * 2 * 4)
-    assert pa.pa_chunk_workspace_bytes(d, T, 64) == 256 + up(S * P * 8 * 16) + up(T * 4) + \
+    # 64 queries x 4 heads >= 64 rows: the tcgen05 path, which keeps no split-K partials
+    assert pa.pa_chunk_workspace_bytes(d, T, 64) == 256 + up(S * P * 8 * 16) + up(T * 4)
+    assert pa.pa_chunk_workspace_bytes(d, T, 15) == 256 + up(S * P * 2 * 16) + up(T * 4) + \
         up(T * Hq * P * D * 4) + up(T * Hq * P * 2 * 4)
+    assert pa.pa_chunk_workspace_bytes(d, T, 16) == 256 + up(S * P * 2 * 16) + up(T * 4)
     d.max_blocks_per_seq = 32            # one partition: no partials
     assert pa.pa_chunk_workspace_bytes(d, T, 5) == 256 + up(S * 16) + up(T * 4)
     assert pa.pa_chunk_workspace_bytes(d, T, 0) == 0          # max_query_len < 1

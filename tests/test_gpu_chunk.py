@@ -44,16 +44,19 @@ def chunk_case(rng, dtype, Hq, Hkv, D, B, lens, nq, std=1.0):
 SHAPES = [(D, B, G) for D in (64, 128) for B in (16, 32) for G in (1, 2, 4, 8)]
 
 
+# Short chunks (at most 7 tokens: fewer than 64 rows per KV head) take the
+# mma.sync kernel with split-K; long ones (70 tokens) the tcgen05 kernel.
+@pytest.mark.parametrize("path", ["mma", "umma"])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("D,B,G", SHAPES)
-def test_chunk_small_shapes(gpu, dtype, D, B, G):
+def test_chunk_small_shapes(gpu, dtype, D, B, G, path):
     torch, pa = gpu
-    rng = synth.make_rng(3000 + D + B + 7 * G + 101 * (dtype == "bf16"))
+    rng = synth.make_rng(3000 + D + B + 7 * G + 101 * (dtype == "bf16") + 13 * (path == "umma"))
     Hkv = 2
     # ragged: one query, a few drafted tokens, a query range crossing blocks and
     # partitions, a whole short sequence, an empty range
     lens = [1, 9, B + 3, 200, 530, 40, 7]
-    nq = [1, 5, B + 3, 33, 70, 0, 7]
+    nq = [1, 5, B + 3, 33, 70, 0, 7] if path == "umma" else [1, 5, 3, 7, 2, 0, 7]
     q, kc, vc, tables, lens, qs = chunk_case(rng, dtype, G * Hkv, Hkv, D, B, lens, nq)
     scale = 1.0 / math.sqrt(D)
     ref = oracle.chunk_attention(q, kc, vc, tables, lens, qs, scale, dtype)
