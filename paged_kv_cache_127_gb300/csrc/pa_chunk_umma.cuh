@@ -7,24 +7,26 @@
 // "KV Cache Fundamentals" and "Block Table and Logical-to-Physical Mapping"),
 // for chunks whose (query token, query head) rows fill 128-row tiles.
 //
-// Work: one CTA per (128-row tile, KV head, sequence); the rows of a KV head
-// are r = t * G + gq.  The CTA walks the visible context in 64-key steps, with
-// no split across CTAs (a tile has enough rows to keep the tensor cores busy),
-// so there is no merge.  Warp roles:
+// Work: one CTA per (MT 128-row tiles, KV head, sequence); the rows of a KV
+// head are r = t * G + gq.  The CTA walks the visible context in 64-key
+// steps, with no split across CTAs (a tile has enough rows to keep the tensor
+// cores busy), so there is no merge.  MT = 2 tiles share every K/V load and
+// give the softmax two warpgroups.  Warp roles:
 //   warp 0       producer: 16-row TMA boxes of K and V (one KV head, both
 //                128-byte halves of D) into a 3-stage ring; table entries
 //                outside the pool, or keys past the context, are not loaded
 //                and are marked in a per-stage mask;
-//   warp 1       allocates 256 TMEM columns and issues the MMAs (lane 0):
-//                  S_j = Q K_j^T      M 128, N 64,  K = D    -> TMEM S[j % 2]
-//                  O  += P_j V_j      M 128, N = D, K 64     -> TMEM O
-//                with P_j split into P_hi + P_lo (two bf16 / f16 operands) so
+//   warp 1       allocates TMEM (256 columns per tile) and issues the MMAs
+//                (lane 0), per tile u:
+//                  S_u,j = Q_u K_j^T   M 128, N 64,  K = D    -> TMEM S[u][j % 2]
+//                  O_u  += P_u,j V_j   M 128, N = D, K 64     -> TMEM O[u]
+//                with P split into P_hi + P_lo (two bf16 / f16 operands) so
 //                the probabilities keep ~16 significant bits;
-//   warps 4..7   softmax, one thread per row (TMEM lane): read S_j, mask
-//                (causal and not-loaded keys), online softmax in log2 units,
-//                write P_hi / P_lo to shared memory, zero the V rows of keys
-//                that must not contribute (their slots may hold anything);
-//                epilogue O / l to out[].
+//   warps 2..    one softmax warpgroup per tile, one thread per row (TMEM
+//                lane 32 * (warp % 4) + lane): read S, mask (causal and
+//                not-loaded keys), online softmax in log2 units, write P_hi /
+//                P_lo to shared memory, zero the V rows of keys that must not
+//                contribute (their slots may hold anything); epilogue O / l.
 // The running maximum is only moved when a row's new maximum exceeds it by
 // more than 2^8 (exp2 units): until then the weights are exp2(x - m) <= 256,
 // exact in fp32, and O and l share the stale maximum, so the result is the
@@ -47,7 +49,7 @@
 
 namespace pa {
 
-template <int D>
+template <int D, int MT>
 struct UmmaCfg {
     static constexpr int kM = 128;                         // rows per tile (TMEM lanes)
     static constexpr int kN = 64;                          // keys per step
@@ -55,25 +57,29 @@ struct UmmaCfg {
     static constexpr int kSub = D / 64;                    // 128-byte halves of a row
     static constexpr int kKS = D / 16;                     // k-steps of S = Q K^T
     static constexpr int kStages = 3;
+    static constexpr int kPBuf = MT == 1 ? 2 : 1;          // P buffers per tile (shared memory budget)
+    static constexpr int kThreads = 64 + 128 * MT;
     static constexpr int kHalf = kN * 128;                 // one half of K (or V) of a step
     static constexpr int kTile = kSub * kHalf;             // K (or V) of a step
     static constexpr int kStageBytes = 2 * kTile;
+    static constexpr int kQTile = kSub * kM * 128;         // Q of one tile (kSub halves of kM x 128 bytes)
     static constexpr int kQHalf = kM * 128;
-    static constexpr int kPPart = kM * kN * 2;             // one of P_hi / P_lo
+    static constexpr int kPPart = kM * kN * 2;             // one of P_hi / P_lo of one tile
     static constexpr size_t kQOff = 0;
-    static constexpr size_t kPOff = kQOff + (size_t)kSub * kQHalf;
-    static constexpr size_t kKVOff = kPOff + 4 * (size_t)kPPart;   // 2 buffers x (hi, lo)
+    static constexpr size_t kPOff = kQOff + (size_t)MT * kQTile;
+    static constexpr size_t kKVOff = kPOff + (size_t)MT * kPBuf * 2 * kPPart;
     static constexpr size_t kBarOff = kKVOff + (size_t)kStages * kStageBytes;
-    // barriers: kv_full[3] kv_empty[3] s_full[2] s_free[2] p_full[2] o_done[2] q_full drain
-    static constexpr int kNumBars = 2 * kStages + 8 + 2;
+    // kv_full[3] kv_empty[3] | per tile: s_full[2] s_free[2] p_full[kPBuf] o_done[kPBuf] q_full | drain
+    static constexpr int kTileBars = 5 + 2 * kPBuf;
+    static constexpr int kNumBars = 2 * kStages + MT * kTileBars + 1;
     static constexpr size_t kMaskOff = kBarOff + 8 * kNumBars;
     static constexpr size_t kSlotOff = kMaskOff + 4 * kStages;
     static constexpr size_t kSmem = kSlotOff + 16 + 1024;  // + alignment slack
-    static constexpr uint32_t kTmemCols = 256;             // S[2] (2 x 64) + O (D <= 128)
-    static constexpr uint32_t kSCol = 0;
-    static constexpr uint32_t kOCol = 2 * kN;
+    static constexpr uint32_t kTmemCols = 256 * MT;
+    static constexpr uint32_t kOCol = 128 * MT;            // S[u][b] at 128 u + 64 b; O[u] at kOCol + D u
     static_assert(D == 64 || D == 128, "head_dim");
-    static_assert(kOCol + D <= kTmemCols, "TMEM budget");
+    static_assert(MT == 1 || MT == 2, "tiles per CTA");
+    static_assert(kOCol + MT * D <= kTmemCols, "TMEM budget");
     static_assert(kPOff % 1024 == 0 && kKVOff % 1024 == 0, "swizzle atoms 1024-byte aligned");
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
@@ -84,13 +90,14 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
     return p;
 }
 
-template <typename T, int D, int B>
-__global__ void __launch_bounds__(256, 1)
+template <typename T, int D, int B, int MT>
+__global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
     chunk_umma_kernel(const ChunkArgs a, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv) {
-    using C = UmmaCfg<D>;
+    using C = UmmaCfg<D, MT>;
     using M = Mma16<T>;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    constexpr int kPB = C::kPBuf;
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -102,13 +109,14 @@ __global__ void __launch_bounds__(256, 1)
     const int s = blockIdx.z;
     const int kvh = blockIdx.y;
     const int G = a.Hq / a.Hkv;
-    const int r0 = blockIdx.x * C::kM;
+    const int r0 = blockIdx.x * C::kM * MT;
     const int qs = a.query_start[s];
     const int n = a.query_start[s + 1] - qs;
     if (n <= 0 || r0 >= n * G || a.tok_seq[qs] != s) return;  // nothing here, or a skipped sequence
     const int len = a.context_lens[s];
-    const int t_last = min(n - 1, (r0 + C::kM - 1) / G);
-    const int nch = (len - n + t_last) / C::kN + 1;           // 64-key steps up to the tile's last position
+    const int tiles = min(MT, (n * G - r0 + C::kM - 1) / C::kM);  // tiles with at least one row
+    const int t_last = min(n - 1, (r0 + C::kM * tiles - 1) / G);
+    const int nch = (len - n + t_last) / C::kN + 1;              // 64-key steps up to the last position
 
     const uint32_t qb = base + (uint32_t)C::kQOff;
     const uint32_t pb = base + (uint32_t)C::kPOff;
@@ -116,12 +124,17 @@ __global__ void __launch_bounds__(256, 1)
     const uint32_t bars = base + (uint32_t)C::kBarOff;
     auto kv_full = [&](int i) { return bars + 8u * (uint32_t)i; };
     auto kv_empty = [&](int i) { return bars + 8u * (uint32_t)(C::kStages + i); };
-    auto s_full = [&](int i) { return bars + 8u * (uint32_t)(2 * C::kStages + i); };
-    auto s_free = [&](int i) { return bars + 8u * (uint32_t)(2 * C::kStages + 2 + i); };
-    auto p_full = [&](int i) { return bars + 8u * (uint32_t)(2 * C::kStages + 4 + i); };
-    auto o_done = [&](int i) { return bars + 8u * (uint32_t)(2 * C::kStages + 6 + i); };
-    const uint32_t q_full = bars + 8u * (uint32_t)(2 * C::kStages + 8);
-    const uint32_t drain = bars + 8u * (uint32_t)(2 * C::kStages + 9);
+    auto tbar = [&](int u, int i) { return bars + 8u * (uint32_t)(2 * C::kStages + u * C::kTileBars + i); };
+    auto s_full = [&](int u, int b) { return tbar(u, b); };
+    auto s_free = [&](int u, int b) { return tbar(u, 2 + b); };
+    auto p_full = [&](int u, int b) { return tbar(u, 4 + b); };
+    auto o_done = [&](int u, int b) { return tbar(u, 4 + kPB + b); };
+    auto q_full = [&](int u) { return tbar(u, 4 + 2 * kPB); };
+    const uint32_t drain = bars + 8u * (uint32_t)(C::kNumBars - 1);
+    auto qtile = [&](int u) { return qb + (uint32_t)(u * C::kQTile); };
+    auto ptile = [&](int u, int b, int part) { return pb + (uint32_t)(((u * kPB + b) * 2 + part) * C::kPPart); };
+    auto s_col = [&](int u, int b) { return (uint32_t)(128 * u + 64 * b); };
+    auto o_col = [&](int u) { return C::kOCol + (uint32_t)(D * u); };
     int *vmask = reinterpret_cast<int *>(basep + C::kMaskOff);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(basep + C::kSlotOff);
 
@@ -130,13 +143,17 @@ __global__ void __launch_bounds__(256, 1)
             mbar_init(kv_full(i), 1);
             mbar_init(kv_empty(i), 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(s_full(i), 1);
-            mbar_init(s_free(i), 4);
-            mbar_init(p_full(i), 4);
-            mbar_init(o_done(i), 1);
+        for (int u = 0; u < MT; ++u) {
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(s_full(u, b), 1);
+                mbar_init(s_free(u, b), 4);
+            }
+            for (int b = 0; b < kPB; ++b) {
+                mbar_init(p_full(u, b), 4);
+                mbar_init(o_done(u, b), 1);
+            }
+            mbar_init(q_full(u), 4);
         }
-        mbar_init(q_full, 4);
         mbar_init(drain, 1);
         fence_mbar_init();
         prefetch_tmap(&tmk);
@@ -207,25 +224,30 @@ __global__ void __launch_bounds__(256, 1)
         // ------------------------------------------------------------ MMA issuer
         constexpr uint32_t idesc_s = tc::f16_idesc(kBf16, false, C::kM, C::kN);
         constexpr uint32_t idesc_o = tc::f16_idesc(kBf16, true, C::kM, D);
-        bool ok = mbar_wait_bounded(q_full, 0u, kWaitLimit);
+        bool ok = true;
+        for (int u = 0; u < tiles && ok; ++u) ok = mbar_wait_bounded(q_full(u), 0u, kWaitLimit);
         auto pv = [&](int c) {
-            if (!mbar_wait_bounded(p_full(c & 1), (uint32_t)(c >> 1) & 1u, kWaitLimit)) return false;
-            tc::fence_after_sync();
-            if (lane == 0) {
-                const uint32_t vst = kvb + (uint32_t)((c % C::kStages) * C::kStageBytes + C::kTile);
+            const int pbuf = c % kPB;
+            const uint32_t vst = kvb + (uint32_t)((c % C::kStages) * C::kStageBytes + C::kTile);
+            for (int u = 0; u < tiles; ++u) {
+                if (!mbar_wait_bounded(p_full(u, pbuf), (uint32_t)(c / kPB) & 1u, kWaitLimit)) return false;
+                tc::fence_after_sync();
+                if (lane == 0) {
 #pragma unroll
-                for (int part = 0; part < 2; ++part) {
-                    const uint32_t pa_ = pb + (uint32_t)(((c & 1) * 2 + part) * C::kPPart);
+                    for (int part = 0; part < 2; ++part) {
+                        const uint32_t pp = ptile(u, pbuf, part);
 #pragma unroll
-                    for (int k = 0; k < C::kN / 16; ++k) {
-                        const uint64_t ad = tc::sw128_desc(pa_ + 32u * k, 16u, 1024u);
-                        const uint64_t bd = tc::sw128_desc(vst + 2048u * k, (uint32_t)C::kHalf, 1024u);
-                        tc::mma_f16_ss(tbase + C::kOCol, ad, bd, idesc_o, (c > 0 || part > 0 || k > 0) ? 1u : 0u);
+                        for (int k = 0; k < C::kN / 16; ++k) {
+                            const uint64_t ad = tc::sw128_desc(pp + 32u * k, 16u, 1024u);
+                            const uint64_t bd = tc::sw128_desc(vst + 2048u * k, (uint32_t)C::kHalf, 1024u);
+                            tc::mma_f16_ss(tbase + o_col(u), ad, bd, idesc_o, (c > 0 || part > 0 || k > 0) ? 1u : 0u);
+                        }
                     }
+                    tc::mma_commit(o_done(u, pbuf));
                 }
-                tc::mma_commit(o_done(c & 1));
-                tc::mma_commit(kv_empty(c % C::kStages));
+                __syncwarp();
             }
+            if (lane == 0) tc::mma_commit(kv_empty(c % C::kStages));
             __syncwarp();
             return true;
         };
@@ -234,20 +256,25 @@ __global__ void __launch_bounds__(256, 1)
             const int st = j % C::kStages;
             const int b = j & 1;
             ok = mbar_wait_bounded(kv_full(st), (uint32_t)(j / C::kStages) & 1u, kWaitLimit);
-            if (ok && j >= 2) ok = mbar_wait_bounded(s_free(b), (uint32_t)((j >> 1) - 1) & 1u, kWaitLimit);
-            if (!ok) break;
-            tc::fence_after_sync();
-            if (lane == 0) {
-                const uint32_t kst = kvb + (uint32_t)(st * C::kStageBytes);
+            const uint32_t kst = kvb + (uint32_t)(st * C::kStageBytes);
+            for (int u = 0; u < tiles && ok; ++u) {
+                if (j >= 2) ok = mbar_wait_bounded(s_free(u, b), (uint32_t)((j >> 1) - 1) & 1u, kWaitLimit);
+                if (!ok) break;
+                tc::fence_after_sync();
+                if (lane == 0) {
 #pragma unroll
-                for (int k = 0; k < C::kKS; ++k) {
-                    const uint64_t ad = tc::sw128_desc(qb + (uint32_t)((k >> 2) * C::kQHalf) + 32u * (k & 3), 16u, 1024u);
-                    const uint64_t bd = tc::sw128_desc(kst + (uint32_t)((k >> 2) * C::kHalf) + 32u * (k & 3), 16u, 1024u);
-                    tc::mma_f16_ss(tbase + C::kSCol + (uint32_t)(b * C::kN), ad, bd, idesc_s, k > 0 ? 1u : 0u);
+                    for (int k = 0; k < C::kKS; ++k) {
+                        const uint64_t ad =
+                            tc::sw128_desc(qtile(u) + (uint32_t)((k >> 2) * C::kQHalf) + 32u * (k & 3), 16u, 1024u);
+                        const uint64_t bd =
+                            tc::sw128_desc(kst + (uint32_t)((k >> 2) * C::kHalf) + 32u * (k & 3), 16u, 1024u);
+                        tc::mma_f16_ss(tbase + s_col(u, b), ad, bd, idesc_s, k > 0 ? 1u : 0u);
+                    }
+                    tc::mma_commit(s_full(u, b));
                 }
-                tc::mma_commit(s_full(b));
+                __syncwarp();
             }
-            __syncwarp();
+            if (!ok) break;
             if (j >= 1 && !(ok = pv(j - 1))) break;
         }
         if (ok && nch >= 1) ok = pv(nch - 1);
@@ -256,11 +283,12 @@ __global__ void __launch_bounds__(256, 1)
         if (lane == 0) tc::mma_commit(drain);
         __syncwarp();
         mbar_wait_bounded(drain, 0u, kWaitLimit);
-    } else if (warp >= 4) {
+    } else if ((warp - 2) / 4 < tiles) {
         // ------------------------------------------------------------ softmax (one row per thread)
-        const int r = threadIdx.x - 128;
-        const int wq = warp - 4;  // TMEM lanes 32 * wq .. 32 * wq + 31
-        const int R = r0 + r;
+        const int u = (warp - 2) / 4;            // tile of this warpgroup
+        const int wq = warp & 3;                 // TMEM lanes 32 * wq .. 32 * wq + 31
+        const int r = 32 * wq + lane;            // row within the tile
+        const int R = r0 + C::kM * u + r;
         const int t = R / G;
         const bool valid = t < n;
         const int h = kvh * G + R % G;
@@ -273,14 +301,15 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
             for (int c = 0; c < D / 8; ++c) {
                 const uint4 v = valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-                const uint32_t addr = qb + (uint32_t)((c >> 3) * C::kQHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+                const uint32_t addr =
+                    qtile(u) + (uint32_t)((c >> 3) * C::kQHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4));
                 asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
                              "r"(v.w)
                              : "memory");
             }
             tc::fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(q_full);
+            if (lane == 0) mbar_arrive(q_full(u));
         }
         const uint32_t tl = tbase + ((uint32_t)(wq * 32) << 16);
         float m_used = -INFINITY, l = 0.f;
@@ -288,16 +317,17 @@ __global__ void __launch_bounds__(256, 1)
         for (int j = 0; j < nch; ++j) {
             const int b = j & 1;
             const int st = j % C::kStages;
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(s_full(b), (uint32_t)(j >> 1) & 1u, kWaitLimit));
+            const int pbuf = j % kPB;
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(s_full(u, b), (uint32_t)(j >> 1) & 1u, kWaitLimit));
             if (!ok) break;
             tc::fence_after_sync();
             uint32_t sv[2][32];
-            tc::tmem_ld32(tl + C::kSCol + (uint32_t)(b * C::kN), sv[0]);
-            tc::tmem_ld32(tl + C::kSCol + (uint32_t)(b * C::kN + 32), sv[1]);
+            tc::tmem_ld32(tl + s_col(u, b), sv[0]);
+            tc::tmem_ld32(tl + s_col(u, b) + 32u, sv[1]);
             tc::tmem_wait_ld();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(s_free(b));
+            if (lane == 0) mbar_arrive(s_free(u, b));
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(kv_full(st), (uint32_t)(j / C::kStages) & 1u, kWaitLimit));
             if (!ok) break;
             const int mask = vmask[st];
@@ -312,43 +342,44 @@ __global__ void __launch_bounds__(256, 1)
             }
             const bool need = mc > m_used + 8.f;
             if (j > 0 && __any_sync(0xffffffffu, need)) {
-                // move the row's maximum: every earlier P V must have landed in O
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait_bounded(o_done((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u, kWaitLimit));
+                // move the row's maximum: every earlier P V of this tile must have landed in O
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_done(u, (j - 1) % kPB),
+                                                                (uint32_t)((j - 1) / kPB) & 1u, kWaitLimit));
                 if (!ok) break;
                 tc::fence_after_sync();
                 const float alpha = need ? ex2(m_used - mc) : 1.f;
 #pragma unroll
                 for (int q = 0; q < D / 32; ++q) {
                     uint32_t ov[32];
-                    tc::tmem_ld32(tl + C::kOCol + 32u * q, ov);
+                    tc::tmem_ld32(tl + o_col(u) + 32u * q, ov);
                     tc::tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                    tc::tmem_st32(tl + C::kOCol + 32u * q, ov);
+                    tc::tmem_st32(tl + o_col(u) + 32u * q, ov);
                 }
                 tc::tmem_wait_st();
                 l *= alpha;
             }
             if (need) m_used = mc;
             const float mu = m_used == -INFINITY ? 0.f : m_used;
-            if (j >= 2) {  // P buffer b is free once the P V of step j - 2 has completed
-                ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_done(b), (uint32_t)((j - 2) >> 1) & 1u, kWaitLimit));
+            if (j >= kPB) {  // P buffer pbuf is free once the P V of step j - kPB has completed
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_done(u, pbuf), (uint32_t)((j - kPB) / kPB) & 1u,
+                                                                kWaitLimit));
                 if (!ok) break;
             }
-            const uint32_t ph = pb + (uint32_t)((b * 2) * C::kPPart) + (uint32_t)(r * 128);
+            const uint32_t ph = ptile(u, pbuf, 0) + (uint32_t)(r * 128);
             const uint32_t plo = ph + (uint32_t)C::kPPart;
 #pragma unroll
             for (int c8 = 0; c8 < C::kN / 8; ++c8) {
                 uint32_t hw[4], lw[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float p0 = ex2(x[c8 * 8 + 2 * u] - mu);
-                    const float p1 = ex2(x[c8 * 8 + 2 * u + 1] - mu);
+                for (int v = 0; v < 4; ++v) {
+                    const float p0 = ex2(x[c8 * 8 + 2 * v] - mu);
+                    const float p1 = ex2(x[c8 * 8 + 2 * v + 1] - mu);
                     l += p0 + p1;
-                    hw[u] = M::pack(p0, p1);
-                    const float2 f = M::unpack(hw[u]);
-                    lw[u] = M::pack(p0 - f.x, p1 - f.y);
+                    hw[v] = M::pack(p0, p1);
+                    const float2 f = M::unpack(hw[v]);
+                    lw[v] = M::pack(p0 - f.x, p1 - f.y);
                 }
                 const uint32_t off = (uint32_t)((c8 ^ (r & 7)) << 4);
                 asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(ph + off), "r"(hw[0]), "r"(hw[1]),
@@ -359,8 +390,10 @@ __global__ void __launch_bounds__(256, 1)
                              : "memory");
             }
             // V rows of keys that were not loaded or lie past the context hold
-            // anything: zero them (row r < 64 of this step's V), whole 128-byte rows
-            if (r < C::kN && (j * C::kN + r >= len || !(mask >> (r >> 4) & 1))) {
+            // anything: tile 0's warpgroup zeroes them (row r < 64 of this step's
+            // V, whole 128-byte rows) before its P is published; the MMA issues
+            // every tile's P V after tile 0's.
+            if (u == 0 && r < C::kN && (j * C::kN + r >= len || !(mask >> (r >> 4) & 1))) {
                 const uint32_t vrow = kvb + (uint32_t)(st * C::kStageBytes + C::kTile + r * 128);
 #pragma unroll
                 for (int sb = 0; sb < C::kSub; ++sb)
@@ -373,12 +406,13 @@ __global__ void __launch_bounds__(256, 1)
             tc::fence_async_smem();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full(b));
+            if (lane == 0) mbar_arrive(p_full(u, pbuf));
         }
+        const int last = nch - 1;
         if (!ok) {
             if (lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
-        } else if (__all_sync(0xffffffffu, mbar_wait_bounded(o_done((nch - 1) & 1),
-                                                              (uint32_t)((nch - 1) >> 1) & 1u, kWaitLimit))) {
+        } else if (__all_sync(0xffffffffu, mbar_wait_bounded(o_done(u, last % kPB), (uint32_t)(last / kPB) & 1u,
+                                                              kWaitLimit))) {
             // ---- epilogue: out = O / l for this row
             tc::fence_after_sync();
             const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -386,7 +420,7 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
             for (int q = 0; q < D / 32; ++q) {
                 uint32_t ov[32];
-                tc::tmem_ld32(tl + C::kOCol + 32u * q, ov);
+                tc::tmem_ld32(tl + o_col(u) + 32u * q, ov);
                 tc::tmem_wait_ld();
                 if (valid) {
 #pragma unroll
@@ -409,26 +443,27 @@ __global__ void __launch_bounds__(256, 1)
     }
 }
 
-template <typename T, int D, int B>
+template <typename T, int D, int B, int MT>
 cudaError_t launch_chunk_umma_t(const ChunkArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                 cudaStream_t st) {
-    using C = UmmaCfg<D>;
+    using C = UmmaCfg<D, MT>;
     static bool configured[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        e = cudaFuncSetAttribute(chunk_umma_kernel<T, D, B>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(chunk_umma_kernel<T, D, B, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)C::kSmem);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
     const int G = a.Hq / a.Hkv;
-    const int tiles = (int)(((long long)a.max_query_len * G + C::kM - 1) / C::kM);
+    const long long rows = (long long)a.max_query_len * G;
+    const int ctas = (int)((rows + C::kM * MT - 1) / (C::kM * MT));
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)tiles, (unsigned)a.Hkv, (unsigned)a.S);
-    cfg.blockDim = dim3(256);
+    cfg.gridDim = dim3((unsigned)ctas, (unsigned)a.Hkv, (unsigned)a.S);
+    cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -436,16 +471,29 @@ cudaError_t launch_chunk_umma_t(const ChunkArgs &a, const CUtensorMap &tmk, cons
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, chunk_umma_kernel<T, D, B>, a, tmk, tmv);
+    return cudaLaunchKernelEx(&cfg, chunk_umma_kernel<T, D, B, MT>, a, tmk, tmv);
+}
+
+// Two tiles per CTA once a sequence can fill them (256 rows per KV head).
+#ifndef PA_CHUNK_UMMA_PAIR_ROWS
+#define PA_CHUNK_UMMA_PAIR_ROWS 256
+#endif
+
+template <typename T, int D, int B>
+cudaError_t dispatch_chunk_umma_mt(const ChunkArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                                   cudaStream_t st) {
+    const long long rows = (long long)a.max_query_len * (a.Hq / a.Hkv);
+    return rows >= PA_CHUNK_UMMA_PAIR_ROWS ? launch_chunk_umma_t<T, D, B, 2>(a, tmk, tmv, st)
+                                           : launch_chunk_umma_t<T, D, B, 1>(a, tmk, tmv, st);
 }
 
 template <typename T>
 cudaError_t dispatch_chunk_umma(const ChunkArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                 cudaStream_t st) {
-    if (a.D == 64 && a.B == 16) return launch_chunk_umma_t<T, 64, 16>(a, tmk, tmv, st);
-    if (a.D == 64 && a.B == 32) return launch_chunk_umma_t<T, 64, 32>(a, tmk, tmv, st);
-    if (a.D == 128 && a.B == 16) return launch_chunk_umma_t<T, 128, 16>(a, tmk, tmv, st);
-    if (a.D == 128 && a.B == 32) return launch_chunk_umma_t<T, 128, 32>(a, tmk, tmv, st);
+    if (a.D == 64 && a.B == 16) return dispatch_chunk_umma_mt<T, 64, 16>(a, tmk, tmv, st);
+    if (a.D == 64 && a.B == 32) return dispatch_chunk_umma_mt<T, 64, 32>(a, tmk, tmv, st);
+    if (a.D == 128 && a.B == 16) return dispatch_chunk_umma_mt<T, 128, 16>(a, tmk, tmv, st);
+    if (a.D == 128 && a.B == 32) return dispatch_chunk_umma_mt<T, 128, 32>(a, tmk, tmv, st);
     return cudaErrorNotSupported;
 }
 

@@ -66,10 +66,14 @@ def test_chunk_small_shapes(gpu, dtype, D, B, G, path):
     assert pa.pa_device_errors(clear=True) == 0
 
 
-@pytest.mark.parametrize("nq,max_q", [(1, 1), (4, 4), (5, 5), (8, 8), (3, 16), (64, 64)])
+@pytest.mark.parametrize("nq,max_q", [(1, 1), (4, 4), (5, 5), (8, 8), (3, 16), (64, 64), (33, 33), (20, 64),
+                                      (40, 64)])
 def test_chunk_query_lengths_and_row_blocks(gpu, nq, max_q):
-    # G = 4: 4 rows per token; one tile (<= 4 tokens), one block of two tiles
-    # (5..8), a loose bound, and many row blocks (64 tokens = 256 rows)
+    # G = 4: 4 rows per token.  mma.sync path: one tile (<= 4 tokens), one block
+    # of two tiles (5..8), a loose bound (3 of 16).  tcgen05 path: one 128-row
+    # tile per CTA (33 tokens = 132 rows, two CTAs), two tiles per CTA (64
+    # tokens), a CTA whose second tile has no row (20 of 64) and one whose
+    # second tile is partly filled (40 of 64)
     torch, pa = gpu
     rng = synth.make_rng(3100 + nq)
     lens = [nq, nq + 1, 600, 1100, 64 + nq]
