@@ -12,17 +12,19 @@
 // steps, with no split across CTAs (a tile has enough rows to keep the tensor
 // cores busy), so there is no merge.  MT = 2 tiles share every K/V load and
 // give the softmax two warpgroups.  Warp roles:
-//   warp 0       producer: 16-row TMA boxes of K and V (one KV head, both
-//                128-byte halves of D) into a 3-stage ring; table entries
-//                outside the pool, or keys past the context, are not loaded
-//                and are marked in a per-stage mask;
+//   warps 0, 2   producers of K and of V: 16-row TMA boxes (one KV head, both
+//                128-byte halves of D) into two 3-stage rings, so that a K
+//                stage is refilled as soon as its S MMAs complete, well before
+//                the P V that frees the V stage; table entries outside the pool,
+//                or keys past the context, are not loaded and are marked in a
+//                per-stage mask;
 //   warp 1       allocates TMEM (256 columns per tile) and issues the MMAs
 //                (lane 0), per tile u:
 //                  S_u,j = Q_u K_j^T   M 128, N 64,  K = D    -> TMEM S[u][j % 2]
 //                  O_u  += P_u,j V_j   M 128, N = D, K 64     -> TMEM O[u]
 //                with P split into P_hi + P_lo (two bf16 / f16 operands) so
 //                the probabilities keep ~16 significant bits;
-//   warps 2..    one softmax warpgroup per tile, one thread per row (TMEM
+//   warps 3..    one softmax warpgroup per tile, one thread per row (TMEM
 //                lane 32 * (warp % 4) + lane): read S, mask (causal and
 //                not-loaded keys), online softmax in log2 units, write P_hi /
 //                P_lo to shared memory, zero the V rows of keys that must not
@@ -58,7 +60,7 @@ struct UmmaCfg {
     static constexpr int kKS = D / 16;                     // k-steps of S = Q K^T
     static constexpr int kStages = 3;
     static constexpr int kPBuf = MT == 1 ? 2 : 1;          // P buffers per tile (shared memory budget)
-    static constexpr int kThreads = 64 + 128 * MT;
+    static constexpr int kThreads = 96 + 128 * MT;         // K producer, MMA, V producer, MT warpgroups
     static constexpr int kHalf = kN * 128;                 // one half of K (or V) of a step
     static constexpr int kTile = kSub * kHalf;             // K (or V) of a step
     static constexpr int kStageBytes = 2 * kTile;
@@ -69,9 +71,10 @@ struct UmmaCfg {
     static constexpr size_t kPOff = kQOff + (size_t)MT * kQTile;
     static constexpr size_t kKVOff = kPOff + (size_t)MT * kPBuf * 2 * kPPart;
     static constexpr size_t kBarOff = kKVOff + (size_t)kStages * kStageBytes;
-    // kv_full[3] kv_empty[3] | per tile: s_full[2] s_free[2] p_full[kPBuf] o_done[kPBuf] q_full | drain
+    // k_full[3] k_empty[3] v_full[3] v_empty[3] | per tile: s_full[2] s_free[2] p_full[kPBuf]
+    // o_done[kPBuf] q_full | drain
     static constexpr int kTileBars = 5 + 2 * kPBuf;
-    static constexpr int kNumBars = 2 * kStages + MT * kTileBars + 1;
+    static constexpr int kNumBars = 4 * kStages + MT * kTileBars + 1;
     static constexpr size_t kMaskOff = kBarOff + 8 * kNumBars;
     static constexpr size_t kSlotOff = kMaskOff + 4 * kStages;
     static constexpr size_t kSmem = kSlotOff + 16 + 1024;  // + alignment slack
@@ -122,9 +125,11 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
     const uint32_t pb = base + (uint32_t)C::kPOff;
     const uint32_t kvb = base + (uint32_t)C::kKVOff;
     const uint32_t bars = base + (uint32_t)C::kBarOff;
-    auto kv_full = [&](int i) { return bars + 8u * (uint32_t)i; };
-    auto kv_empty = [&](int i) { return bars + 8u * (uint32_t)(C::kStages + i); };
-    auto tbar = [&](int u, int i) { return bars + 8u * (uint32_t)(2 * C::kStages + u * C::kTileBars + i); };
+    auto k_full = [&](int i) { return bars + 8u * (uint32_t)i; };
+    auto k_empty = [&](int i) { return bars + 8u * (uint32_t)(C::kStages + i); };
+    auto v_full = [&](int i) { return bars + 8u * (uint32_t)(2 * C::kStages + i); };
+    auto v_empty = [&](int i) { return bars + 8u * (uint32_t)(3 * C::kStages + i); };
+    auto tbar = [&](int u, int i) { return bars + 8u * (uint32_t)(4 * C::kStages + u * C::kTileBars + i); };
     auto s_full = [&](int u, int b) { return tbar(u, b); };
     auto s_free = [&](int u, int b) { return tbar(u, 2 + b); };
     auto p_full = [&](int u, int b) { return tbar(u, 4 + b); };
@@ -140,8 +145,10 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kStages; ++i) {
-            mbar_init(kv_full(i), 1);
-            mbar_init(kv_empty(i), 1);
+            mbar_init(k_full(i), 1);
+            mbar_init(k_empty(i), 1);
+            mbar_init(v_full(i), 1);
+            mbar_init(v_empty(i), 1);
         }
         for (int u = 0; u < MT; ++u) {
             for (int b = 0; b < 2; ++b) {
@@ -165,15 +172,19 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
     tc::fence_after_sync();
     const uint32_t tbase = *tslot;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
+    if (warp == 0 || warp == 2) {
+        // ------------------------------------------------------------ producers: K (warp 0), V (warp 2)
+        const bool is_v = warp == 2;
         const int32_t *row = a.block_tables + (size_t)s * a.max_blocks;
         const uint64_t pol = policy_evict_last();  // the other row tiles of this head reread these keys
+        const CUtensorMap *map = is_v ? &tmv : &tmk;
+        const uint32_t ring = kvb + (is_v ? (uint32_t)C::kTile : 0u);
         int j = 0;
         for (; j < nch; ++j) {
             const int st = j % C::kStages;
             if (j >= C::kStages &&
-                !mbar_wait_bounded(kv_empty(st), (uint32_t)((j / C::kStages) - 1) & 1u, kWaitLimit)) {
+                !mbar_wait_bounded(is_v ? v_empty(st) : k_empty(st), (uint32_t)((j / C::kStages) - 1) & 1u,
+                                   kWaitLimit)) {
                 if (lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
                 break;
             }
@@ -188,30 +199,27 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
                         if (pbk >= 0 && pbk < a.N) {
                             blk[i] = pbk;
                             mask |= 1 << i;
-                        } else {
+                        } else if (!is_v) {
                             set_error(a.err, PA_DEVERR_BAD_BLOCK);
                         }
                     }
                 }
-                vmask[st] = mask;
-                const uint32_t bar = kv_full(st);
-                const uint32_t bytes = (uint32_t)__popc(mask) * 2u * C::kSub * 2048u;
+                if (is_v) vmask[st] = mask;  // read by the softmax after v_full (released with v_empty)
+                const uint32_t bar = is_v ? v_full(st) : k_full(st);
+                const uint32_t bytes = (uint32_t)__popc(mask) * C::kSub * 2048u;
                 if (bytes == 0) {
                     mbar_arrive(bar);
                 } else {
                     mbar_arrive_expect_tx(bar, bytes);
-                    const uint32_t kst = kvb + (uint32_t)(st * C::kStageBytes);
+                    const uint32_t dst = ring + (uint32_t)(st * C::kStageBytes);
 #pragma unroll
                     for (int i = 0; i < C::kBoxes; ++i) {
                         if (!(mask >> i & 1)) continue;
                         const int y = (j * C::kN + 16 * i) % B;
                         const int z = blk[i] * a.Hkv + kvh;
 #pragma unroll
-                        for (int sb = 0; sb < C::kSub; ++sb) {
-                            const uint32_t off = (uint32_t)(sb * C::kHalf + i * 2048);
-                            tma_load_3d(kst + off, &tmk, sb * 64, y, z, bar, pol);
-                            tma_load_3d(kst + C::kTile + off, &tmv, sb * 64, y, z, bar, pol);
-                        }
+                        for (int sb = 0; sb < C::kSub; ++sb)
+                            tma_load_3d(dst + (uint32_t)(sb * C::kHalf + i * 2048), map, sb * 64, y, z, bar, pol);
                     }
                 }
             }
@@ -219,7 +227,8 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
         }
         // copies still in flight must land before the CTA's shared memory is released
         for (int k = max(0, j - C::kStages); k < j; ++k)
-            mbar_wait_bounded(kv_full(k % C::kStages), (uint32_t)(k / C::kStages) & 1u, kWaitLimit);
+            mbar_wait_bounded(is_v ? v_full(k % C::kStages) : k_full(k % C::kStages), (uint32_t)(k / C::kStages) & 1u,
+                              kWaitLimit);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         constexpr uint32_t idesc_s = tc::f16_idesc(kBf16, false, C::kM, C::kN);
@@ -229,6 +238,7 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
         auto pv = [&](int c) {
             const int pbuf = c % kPB;
             const uint32_t vst = kvb + (uint32_t)((c % C::kStages) * C::kStageBytes + C::kTile);
+            if (!mbar_wait_bounded(v_full(c % C::kStages), (uint32_t)(c / C::kStages) & 1u, kWaitLimit)) return false;
             for (int u = 0; u < tiles; ++u) {
                 if (!mbar_wait_bounded(p_full(u, pbuf), (uint32_t)(c / kPB) & 1u, kWaitLimit)) return false;
                 tc::fence_after_sync();
@@ -247,7 +257,7 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
                 }
                 __syncwarp();
             }
-            if (lane == 0) tc::mma_commit(kv_empty(c % C::kStages));
+            if (lane == 0) tc::mma_commit(v_empty(c % C::kStages));
             __syncwarp();
             return true;
         };
@@ -255,7 +265,7 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
         for (; ok && j < nch; ++j) {
             const int st = j % C::kStages;
             const int b = j & 1;
-            ok = mbar_wait_bounded(kv_full(st), (uint32_t)(j / C::kStages) & 1u, kWaitLimit);
+            ok = mbar_wait_bounded(k_full(st), (uint32_t)(j / C::kStages) & 1u, kWaitLimit);
             const uint32_t kst = kvb + (uint32_t)(st * C::kStageBytes);
             for (int u = 0; u < tiles && ok; ++u) {
                 if (j >= 2) ok = mbar_wait_bounded(s_free(u, b), (uint32_t)((j >> 1) - 1) & 1u, kWaitLimit);
@@ -275,6 +285,8 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
                 __syncwarp();
             }
             if (!ok) break;
+            if (lane == 0) tc::mma_commit(k_empty(st));  // the K stage is free once these S MMAs complete
+            __syncwarp();
             if (j >= 1 && !(ok = pv(j - 1))) break;
         }
         if (ok && nch >= 1) ok = pv(nch - 1);
@@ -283,9 +295,9 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
         if (lane == 0) tc::mma_commit(drain);
         __syncwarp();
         mbar_wait_bounded(drain, 0u, kWaitLimit);
-    } else if ((warp - 2) / 4 < tiles) {
+    } else if (warp >= 3 && (warp - 3) / 4 < tiles) {
         // ------------------------------------------------------------ softmax (one row per thread)
-        const int u = (warp - 2) / 4;            // tile of this warpgroup
+        const int u = (warp - 3) / 4;            // tile of this warpgroup
         const int wq = warp & 3;                 // TMEM lanes 32 * wq .. 32 * wq + 31
         const int r = 32 * wq + lane;            // row within the tile
         const int R = r0 + C::kM * u + r;
@@ -328,65 +340,87 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(s_free(u, b));
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(kv_full(st), (uint32_t)(j / C::kStages) & 1u, kWaitLimit));
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(v_full(st), (uint32_t)(j / C::kStages) & 1u, kWaitLimit));
             if (!ok) break;
             const int mask = vmask[st];
             const int lim = valid ? pos - j * C::kN : -1;  // last visible key of this step
-            float x[C::kN];
-            float mc = -INFINITY;
+            // raw logits; the softmax scale is folded into the exponent's FFMA
+            float f[C::kN];
 #pragma unroll
-            for (int c = 0; c < C::kN; ++c) {
-                const bool vis = c <= lim && (mask >> (c >> 4) & 1);
-                x[c] = vis ? __uint_as_float(sv[c >> 5][c & 31]) * sl : -INFINITY;
-                mc = fmaxf(mc, x[c]);
+            for (int c = 0; c < C::kN; ++c) f[c] = __uint_as_float(sv[c >> 5][c & 31]);
+            float mul = sl;
+            if (!(sl > 0.f)) {
+                // a non-positive scale: scale first, mask to -inf
+#pragma unroll
+                for (int c = 0; c < C::kN; ++c) f[c] = (c <= lim && (mask >> (c >> 4) & 1)) ? f[c] * sl : -INFINITY;
+                mul = 1.f;
+            } else if (!(__all_sync(0xffffffffu, lim >= C::kN - 1) && mask == (1 << C::kBoxes) - 1)) {
+                // a step on the diagonal, past the context or over a block not loaded
+#pragma unroll
+                for (int c = 0; c < C::kN; ++c)
+                    if (!(c <= lim && (mask >> (c >> 4) & 1))) f[c] = -INFINITY;
             }
+            // row maximum as 8 independent chains (a single 64-long chain of
+            // dependent max operations would sit on the critical path)
+            float mx[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx[i] = f[i];
+#pragma unroll
+            for (int c = 8; c < C::kN; ++c) mx[c & 7] = fmaxf(mx[c & 7], f[c]);
+            const float mr = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            const float mc = mr * mul;  // -inf when nothing is visible
             const bool need = mc > m_used + 8.f;
-            if (j > 0 && __any_sync(0xffffffffu, need)) {
-                // move the row's maximum: every earlier P V of this tile must have landed in O
-                ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_done(u, (j - 1) % kPB),
-                                                                (uint32_t)((j - 1) / kPB) & 1u, kWaitLimit));
-                if (!ok) break;
-                tc::fence_after_sync();
-                const float alpha = need ? ex2(m_used - mc) : 1.f;
-#pragma unroll
-                for (int q = 0; q < D / 32; ++q) {
-                    uint32_t ov[32];
-                    tc::tmem_ld32(tl + o_col(u) + 32u * q, ov);
-                    tc::tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                    tc::tmem_st32(tl + o_col(u) + 32u * q, ov);
-                }
-                tc::tmem_wait_st();
-                l *= alpha;
-            }
+            const float alpha = (need && j > 0) ? ex2(m_used - mc) : 1.f;
             if (need) m_used = mc;
             const float mu = m_used == -INFINITY ? 0.f : m_used;
-            if (j >= kPB) {  // P buffer pbuf is free once the P V of step j - kPB has completed
-                ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_done(u, pbuf), (uint32_t)((j - kPB) / kPB) & 1u,
-                                                                kWaitLimit));
+            // P = exp2(x - m) split into P_hi + P_lo, in registers before waiting;
+            // the row sum in 8 independent partial sums
+            uint32_t hw[C::kN / 2], lw[C::kN / 2];
+            float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int v = 0; v < C::kN / 2; ++v) {
+                const float p0 = ex2(fmaf(f[2 * v], mul, -mu));
+                const float p1 = ex2(fmaf(f[2 * v + 1], mul, -mu));
+                ls[v & 7] += p0 + p1;
+                hw[v] = M::pack(p0, p1);
+                const float2 hf = M::unpack(hw[v]);
+                lw[v] = M::pack(p0 - hf.x, p1 - hf.y);
+            }
+            l = l * alpha + (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
+            // O may be rescaled, and the P buffer rewritten, only once the P V
+            // MMAs that read them have completed: step j - 1 for a rescale, step
+            // j - kPB for the buffer (completion is in issue order)
+            const bool rescale = j > 0 && __any_sync(0xffffffffu, need);
+            const int wait_step = rescale ? j - 1 : j - kPB;
+            if (wait_step >= 0) {
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_done(u, wait_step % kPB),
+                                                                (uint32_t)(wait_step / kPB) & 1u, kWaitLimit));
                 if (!ok) break;
+            }
+            if (rescale) {
+                tc::fence_after_sync();
+#pragma unroll 1
+                for (int q = 0; q < D / 16; ++q) {
+                    uint32_t ov[16];
+                    tc::tmem_ld16(tl + o_col(u) + 16u * q, ov);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                    tc::tmem_st16(tl + o_col(u) + 16u * q, ov);
+                }
+                tc::tmem_wait_st();
             }
             const uint32_t ph = ptile(u, pbuf, 0) + (uint32_t)(r * 128);
             const uint32_t plo = ph + (uint32_t)C::kPPart;
 #pragma unroll
             for (int c8 = 0; c8 < C::kN / 8; ++c8) {
-                uint32_t hw[4], lw[4];
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    const float p0 = ex2(x[c8 * 8 + 2 * v] - mu);
-                    const float p1 = ex2(x[c8 * 8 + 2 * v + 1] - mu);
-                    l += p0 + p1;
-                    hw[v] = M::pack(p0, p1);
-                    const float2 f = M::unpack(hw[v]);
-                    lw[v] = M::pack(p0 - f.x, p1 - f.y);
-                }
                 const uint32_t off = (uint32_t)((c8 ^ (r & 7)) << 4);
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(ph + off), "r"(hw[0]), "r"(hw[1]),
-                             "r"(hw[2]), "r"(hw[3])
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(ph + off), "r"(hw[4 * c8]),
+                             "r"(hw[4 * c8 + 1]), "r"(hw[4 * c8 + 2]), "r"(hw[4 * c8 + 3])
                              : "memory");
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(plo + off), "r"(lw[0]), "r"(lw[1]),
-                             "r"(lw[2]), "r"(lw[3])
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(plo + off), "r"(lw[4 * c8]),
+                             "r"(lw[4 * c8 + 1]), "r"(lw[4 * c8 + 2]), "r"(lw[4 * c8 + 3])
                              : "memory");
             }
             // V rows of keys that were not loaded or lie past the context hold
