@@ -18,13 +18,13 @@
 //                the P V that frees the V stage; table entries outside the pool,
 //                or keys past the context, are not loaded and are marked in a
 //                per-stage mask;
-//   warp 1       allocates TMEM (256 columns per tile) and issues the MMAs
-//                (lane 0), per tile u:
+//   warps 1, 3   issue the MMAs (lane 0), S in warp 1 (which also allocates
+//                TMEM, 256 columns per tile), P V in warp 3, per tile u:
 //                  S_u,j = Q_u K_j^T   M 128, N 64,  K = D    -> TMEM S[u][j % 2]
 //                  O_u  += P_u,j V_j   M 128, N = D, K 64     -> TMEM O[u]
 //                with P split into P_hi + P_lo (two bf16 / f16 operands) so
 //                the probabilities keep ~16 significant bits;
-//   warps 3..    one softmax warpgroup per tile, one thread per row (TMEM
+//   warps 4..    one softmax warpgroup per tile, one thread per row (TMEM
 //                lane 32 * (warp % 4) + lane): read S, mask (causal and
 //                not-loaded keys), online softmax in log2 units, write P_hi /
 //                P_lo to shared memory, zero the V rows of keys that must not
@@ -60,7 +60,7 @@ struct UmmaCfg {
     static constexpr int kKS = D / 16;                     // k-steps of S = Q K^T
     static constexpr int kStages = 3;
     static constexpr int kPBuf = MT == 1 ? 2 : 1;          // P buffers per tile (shared memory budget)
-    static constexpr int kThreads = 96 + 128 * MT;         // K producer, MMA, V producer, MT warpgroups
+    static constexpr int kThreads = 128 + 128 * MT;        // K producer, S issuer, V producer, P V issuer, MT warpgroups
     static constexpr int kHalf = kN * 128;                 // one half of K (or V) of a step
     static constexpr int kTile = kSub * kHalf;             // K (or V) of a step
     static constexpr int kStageBytes = 2 * kTile;
@@ -72,9 +72,9 @@ struct UmmaCfg {
     static constexpr size_t kKVOff = kPOff + (size_t)MT * kPBuf * 2 * kPPart;
     static constexpr size_t kBarOff = kKVOff + (size_t)kStages * kStageBytes;
     // k_full[3] k_empty[3] v_full[3] v_empty[3] | per tile: s_full[2] s_free[2] p_full[kPBuf]
-    // o_done[kPBuf] q_full | drain
+    // o_done[kPBuf] q_full | drain_s drain_p
     static constexpr int kTileBars = 5 + 2 * kPBuf;
-    static constexpr int kNumBars = 4 * kStages + MT * kTileBars + 1;
+    static constexpr int kNumBars = 4 * kStages + MT * kTileBars + 2;
     static constexpr size_t kMaskOff = kBarOff + 8 * kNumBars;
     static constexpr size_t kSlotOff = kMaskOff + 4 * kStages;
     static constexpr size_t kSmem = kSlotOff + 16 + 1024;  // + alignment slack
@@ -135,7 +135,8 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
     auto p_full = [&](int u, int b) { return tbar(u, 4 + b); };
     auto o_done = [&](int u, int b) { return tbar(u, 4 + kPB + b); };
     auto q_full = [&](int u) { return tbar(u, 4 + 2 * kPB); };
-    const uint32_t drain = bars + 8u * (uint32_t)(C::kNumBars - 1);
+    const uint32_t drain_s = bars + 8u * (uint32_t)(C::kNumBars - 2);
+    const uint32_t drain_p = bars + 8u * (uint32_t)(C::kNumBars - 1);
     auto qtile = [&](int u) { return qb + (uint32_t)(u * C::kQTile); };
     auto ptile = [&](int u, int b, int part) { return pb + (uint32_t)(((u * kPB + b) * 2 + part) * C::kPPart); };
     auto s_col = [&](int u, int b) { return (uint32_t)(128 * u + 64 * b); };
@@ -161,7 +162,8 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
             }
             mbar_init(q_full(u), 4);
         }
-        mbar_init(drain, 1);
+        mbar_init(drain_s, 1);
+        mbar_init(drain_p, 1);
         fence_mbar_init();
         prefetch_tmap(&tmk);
         prefetch_tmap(&tmv);
@@ -230,39 +232,11 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
             mbar_wait_bounded(is_v ? v_full(k % C::kStages) : k_full(k % C::kStages), (uint32_t)(k / C::kStages) & 1u,
                               kWaitLimit);
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------ S = Q K^T issuer
         constexpr uint32_t idesc_s = tc::f16_idesc(kBf16, false, C::kM, C::kN);
-        constexpr uint32_t idesc_o = tc::f16_idesc(kBf16, true, C::kM, D);
         bool ok = true;
         for (int u = 0; u < tiles && ok; ++u) ok = mbar_wait_bounded(q_full(u), 0u, kWaitLimit);
-        auto pv = [&](int c) {
-            const int pbuf = c % kPB;
-            const uint32_t vst = kvb + (uint32_t)((c % C::kStages) * C::kStageBytes + C::kTile);
-            if (!mbar_wait_bounded(v_full(c % C::kStages), (uint32_t)(c / C::kStages) & 1u, kWaitLimit)) return false;
-            for (int u = 0; u < tiles; ++u) {
-                if (!mbar_wait_bounded(p_full(u, pbuf), (uint32_t)(c / kPB) & 1u, kWaitLimit)) return false;
-                tc::fence_after_sync();
-                if (lane == 0) {
-#pragma unroll
-                    for (int part = 0; part < 2; ++part) {
-                        const uint32_t pp = ptile(u, pbuf, part);
-#pragma unroll
-                        for (int k = 0; k < C::kN / 16; ++k) {
-                            const uint64_t ad = tc::sw128_desc(pp + 32u * k, 16u, 1024u);
-                            const uint64_t bd = tc::sw128_desc(vst + 2048u * k, (uint32_t)C::kHalf, 1024u);
-                            tc::mma_f16_ss(tbase + o_col(u), ad, bd, idesc_o, (c > 0 || part > 0 || k > 0) ? 1u : 0u);
-                        }
-                    }
-                    tc::mma_commit(o_done(u, pbuf));
-                }
-                __syncwarp();
-            }
-            if (lane == 0) tc::mma_commit(v_empty(c % C::kStages));
-            __syncwarp();
-            return true;
-        };
-        int j = 0;
-        for (; ok && j < nch; ++j) {
+        for (int j = 0; ok && j < nch; ++j) {
             const int st = j % C::kStages;
             const int b = j & 1;
             ok = mbar_wait_bounded(k_full(st), (uint32_t)(j / C::kStages) & 1u, kWaitLimit);
@@ -287,17 +261,53 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
             if (!ok) break;
             if (lane == 0) tc::mma_commit(k_empty(st));  // the K stage is free once these S MMAs complete
             __syncwarp();
-            if (j >= 1 && !(ok = pv(j - 1))) break;
         }
-        if (ok && nch >= 1) ok = pv(nch - 1);
         if (!ok && lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
         // every MMA issued by this thread has completed before TMEM is freed
-        if (lane == 0) tc::mma_commit(drain);
+        if (lane == 0) tc::mma_commit(drain_s);
         __syncwarp();
-        mbar_wait_bounded(drain, 0u, kWaitLimit);
-    } else if (warp >= 3 && (warp - 3) / 4 < tiles) {
+        mbar_wait_bounded(drain_s, 0u, kWaitLimit);
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ O += P V issuer
+        // A thread of its own: issuing the next step's S MMAs may block while the
+        // tensor pipe is busy, and must not hold back a P V whose P is ready.
+        constexpr uint32_t idesc_o = tc::f16_idesc(kBf16, true, C::kM, D);
+        bool ok = true;
+        for (int c = 0; ok && c < nch; ++c) {
+            const int pbuf = c % kPB;
+            const int st = c % C::kStages;
+            const uint32_t vst = kvb + (uint32_t)(st * C::kStageBytes + C::kTile);
+            ok = mbar_wait_bounded(v_full(st), (uint32_t)(c / C::kStages) & 1u, kWaitLimit);
+            for (int u = 0; u < tiles && ok; ++u) {
+                ok = mbar_wait_bounded(p_full(u, pbuf), (uint32_t)(c / kPB) & 1u, kWaitLimit);
+                if (!ok) break;
+                tc::fence_after_sync();
+                if (lane == 0) {
+#pragma unroll
+                    for (int part = 0; part < 2; ++part) {
+                        const uint32_t pp = ptile(u, pbuf, part);
+#pragma unroll
+                        for (int k = 0; k < C::kN / 16; ++k) {
+                            const uint64_t ad = tc::sw128_desc(pp + 32u * k, 16u, 1024u);
+                            const uint64_t bd = tc::sw128_desc(vst + 2048u * k, (uint32_t)C::kHalf, 1024u);
+                            tc::mma_f16_ss(tbase + o_col(u), ad, bd, idesc_o, (c > 0 || part > 0 || k > 0) ? 1u : 0u);
+                        }
+                    }
+                    tc::mma_commit(o_done(u, pbuf));
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (lane == 0) tc::mma_commit(v_empty(st));
+            __syncwarp();
+        }
+        if (!ok && lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
+        if (lane == 0) tc::mma_commit(drain_p);
+        __syncwarp();
+        mbar_wait_bounded(drain_p, 0u, kWaitLimit);
+    } else if (warp >= 4 && (warp - 4) / 4 < tiles) {
         // ------------------------------------------------------------ softmax (one row per thread)
-        const int u = (warp - 3) / 4;            // tile of this warpgroup
+        const int u = (warp - 4) / 4;            // tile of this warpgroup
         const int wq = warp & 3;                 // TMEM lanes 32 * wq .. 32 * wq + 31
         const int r = 32 * wq + lane;            // row within the tile
         const int R = r0 + C::kM * u + r;
