@@ -27,7 +27,8 @@
 //   warps 4..    one softmax warpgroup per tile, one thread per row (TMEM
 //                lane 32 * (warp % 4) + lane): read S, mask (causal and
 //                not-loaded keys), online softmax in log2 units, write P_hi /
-//                P_lo to shared memory, zero the V rows of keys that must not
+//                P_lo into TMEM over the S just read (the P V MMA takes its A
+//                operand from TMEM), zero the V rows of keys that must not
 //                contribute (their slots may hold anything); epilogue O / l.
 // The running maximum is only moved when a row's new maximum exceeds it by
 // more than 2^8 (exp2 units): until then the weights are exp2(x - m) <= 256,
@@ -58,32 +59,31 @@ struct UmmaCfg {
     static constexpr int kBoxes = kN / 16;                 // 16-row TMA boxes per step
     static constexpr int kSub = D / 64;                    // 128-byte halves of a row
     static constexpr int kKS = D / 16;                     // k-steps of S = Q K^T
-    static constexpr int kStages = 3;
-    static constexpr int kPBuf = MT == 1 ? 2 : 1;          // P buffers per tile (shared memory budget)
+    static constexpr int kStages = 4;
     static constexpr int kThreads = 128 + 128 * MT;        // K producer, S issuer, V producer, P V issuer, MT warpgroups
     static constexpr int kHalf = kN * 128;                 // one half of K (or V) of a step
     static constexpr int kTile = kSub * kHalf;             // K (or V) of a step
     static constexpr int kStageBytes = 2 * kTile;
     static constexpr int kQTile = kSub * kM * 128;         // Q of one tile (kSub halves of kM x 128 bytes)
     static constexpr int kQHalf = kM * 128;
-    static constexpr int kPPart = kM * kN * 2;             // one of P_hi / P_lo of one tile
     static constexpr size_t kQOff = 0;
-    static constexpr size_t kPOff = kQOff + (size_t)MT * kQTile;
-    static constexpr size_t kKVOff = kPOff + (size_t)MT * kPBuf * 2 * kPPart;
+    static constexpr size_t kKVOff = kQOff + (size_t)MT * kQTile;
     static constexpr size_t kBarOff = kKVOff + (size_t)kStages * kStageBytes;
-    // k_full[3] k_empty[3] v_full[3] v_empty[3] | per tile: s_full[2] s_free[2] p_full[kPBuf]
-    // o_done[kPBuf] q_full | drain_s drain_p
-    static constexpr int kTileBars = 5 + 2 * kPBuf;
+    // k_full, k_empty, v_full, v_empty [kStages] | per tile: s_full[2] p_full[2] o_done[2] q_full |
+    // drain_s drain_p
+    static constexpr int kTileBars = 7;
     static constexpr int kNumBars = 4 * kStages + MT * kTileBars + 2;
     static constexpr size_t kMaskOff = kBarOff + 8 * kNumBars;
     static constexpr size_t kSlotOff = kMaskOff + 4 * kStages;
     static constexpr size_t kSmem = kSlotOff + 16 + 1024;  // + alignment slack
     static constexpr uint32_t kTmemCols = 256 * MT;
     static constexpr uint32_t kOCol = 128 * MT;            // S[u][b] at 128 u + 64 b; O[u] at kOCol + D u
+    // P[u][b] aliases S[u][b]: P_hi in its first 32 columns, P_lo in the next 32
+    // (two 16-bit values per column)
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(MT == 1 || MT == 2, "tiles per CTA");
     static_assert(kOCol + MT * D <= kTmemCols, "TMEM budget");
-    static_assert(kPOff % 1024 == 0 && kKVOff % 1024 == 0, "swizzle atoms 1024-byte aligned");
+    static_assert(kKVOff % 1024 == 0, "swizzle atoms 1024-byte aligned");
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
 
@@ -100,7 +100,6 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
     using C = UmmaCfg<D, MT>;
     using M = Mma16<T>;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
-    constexpr int kPB = C::kPBuf;
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -122,7 +121,6 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
     const int nch = (len - n + t_last) / C::kN + 1;              // 64-key steps up to the last position
 
     const uint32_t qb = base + (uint32_t)C::kQOff;
-    const uint32_t pb = base + (uint32_t)C::kPOff;
     const uint32_t kvb = base + (uint32_t)C::kKVOff;
     const uint32_t bars = base + (uint32_t)C::kBarOff;
     auto k_full = [&](int i) { return bars + 8u * (uint32_t)i; };
@@ -131,14 +129,13 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
     auto v_empty = [&](int i) { return bars + 8u * (uint32_t)(3 * C::kStages + i); };
     auto tbar = [&](int u, int i) { return bars + 8u * (uint32_t)(4 * C::kStages + u * C::kTileBars + i); };
     auto s_full = [&](int u, int b) { return tbar(u, b); };
-    auto s_free = [&](int u, int b) { return tbar(u, 2 + b); };
-    auto p_full = [&](int u, int b) { return tbar(u, 4 + b); };
-    auto o_done = [&](int u, int b) { return tbar(u, 4 + kPB + b); };
-    auto q_full = [&](int u) { return tbar(u, 4 + 2 * kPB); };
+    auto p_full = [&](int u, int b) { return tbar(u, 2 + b); };
+    // P V of a step on buffer b complete: O is up to date and S/P[u][b] may be rewritten
+    auto o_done = [&](int u, int b) { return tbar(u, 4 + b); };
+    auto q_full = [&](int u) { return tbar(u, 6); };
     const uint32_t drain_s = bars + 8u * (uint32_t)(C::kNumBars - 2);
     const uint32_t drain_p = bars + 8u * (uint32_t)(C::kNumBars - 1);
     auto qtile = [&](int u) { return qb + (uint32_t)(u * C::kQTile); };
-    auto ptile = [&](int u, int b, int part) { return pb + (uint32_t)(((u * kPB + b) * 2 + part) * C::kPPart); };
     auto s_col = [&](int u, int b) { return (uint32_t)(128 * u + 64 * b); };
     auto o_col = [&](int u) { return C::kOCol + (uint32_t)(D * u); };
     int *vmask = reinterpret_cast<int *>(basep + C::kMaskOff);
@@ -154,9 +151,6 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
         for (int u = 0; u < MT; ++u) {
             for (int b = 0; b < 2; ++b) {
                 mbar_init(s_full(u, b), 1);
-                mbar_init(s_free(u, b), 4);
-            }
-            for (int b = 0; b < kPB; ++b) {
                 mbar_init(p_full(u, b), 4);
                 mbar_init(o_done(u, b), 1);
             }
@@ -242,7 +236,8 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
             ok = mbar_wait_bounded(k_full(st), (uint32_t)(j / C::kStages) & 1u, kWaitLimit);
             const uint32_t kst = kvb + (uint32_t)(st * C::kStageBytes);
             for (int u = 0; u < tiles && ok; ++u) {
-                if (j >= 2) ok = mbar_wait_bounded(s_free(u, b), (uint32_t)((j >> 1) - 1) & 1u, kWaitLimit);
+                // S/P[u][b] is free once the P V of step j - 2 has read P from it
+                if (j >= 2) ok = mbar_wait_bounded(o_done(u, b), (uint32_t)((j >> 1) - 1) & 1u, kWaitLimit);
                 if (!ok) break;
                 tc::fence_after_sync();
                 if (lane == 0) {
@@ -274,26 +269,25 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
         constexpr uint32_t idesc_o = tc::f16_idesc(kBf16, true, C::kM, D);
         bool ok = true;
         for (int c = 0; ok && c < nch; ++c) {
-            const int pbuf = c % kPB;
+            const int b = c & 1;
             const int st = c % C::kStages;
             const uint32_t vst = kvb + (uint32_t)(st * C::kStageBytes + C::kTile);
             ok = mbar_wait_bounded(v_full(st), (uint32_t)(c / C::kStages) & 1u, kWaitLimit);
             for (int u = 0; u < tiles && ok; ++u) {
-                ok = mbar_wait_bounded(p_full(u, pbuf), (uint32_t)(c / kPB) & 1u, kWaitLimit);
+                ok = mbar_wait_bounded(p_full(u, b), (uint32_t)(c >> 1) & 1u, kWaitLimit);
                 if (!ok) break;
                 tc::fence_after_sync();
                 if (lane == 0) {
 #pragma unroll
                     for (int part = 0; part < 2; ++part) {
-                        const uint32_t pp = ptile(u, pbuf, part);
 #pragma unroll
                         for (int k = 0; k < C::kN / 16; ++k) {
-                            const uint64_t ad = tc::sw128_desc(pp + 32u * k, 16u, 1024u);
+                            const uint32_t at = tbase + s_col(u, b) + (uint32_t)(32 * part + 8 * k);
                             const uint64_t bd = tc::sw128_desc(vst + 2048u * k, (uint32_t)C::kHalf, 1024u);
-                            tc::mma_f16_ss(tbase + o_col(u), ad, bd, idesc_o, (c > 0 || part > 0 || k > 0) ? 1u : 0u);
+                            tc::mma_f16_ts(tbase + o_col(u), at, bd, idesc_o, (c > 0 || part > 0 || k > 0) ? 1u : 0u);
                         }
                     }
-                    tc::mma_commit(o_done(u, pbuf));
+                    tc::mma_commit(o_done(u, b));
                 }
                 __syncwarp();
             }
@@ -339,7 +333,6 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
         for (int j = 0; j < nch; ++j) {
             const int b = j & 1;
             const int st = j % C::kStages;
-            const int pbuf = j % kPB;
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(s_full(u, b), (uint32_t)(j >> 1) & 1u, kWaitLimit));
             if (!ok) break;
             tc::fence_after_sync();
@@ -347,9 +340,6 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
             tc::tmem_ld32(tl + s_col(u, b), sv[0]);
             tc::tmem_ld32(tl + s_col(u, b) + 32u, sv[1]);
             tc::tmem_wait_ld();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_free(u, b));
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(v_full(st), (uint32_t)(j / C::kStages) & 1u, kWaitLimit));
             if (!ok) break;
             const int mask = vmask[st];
@@ -398,17 +388,12 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
                 lw[v] = M::pack(p0 - hf.x, p1 - hf.y);
             }
             l = l * alpha + (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
-            // O may be rescaled, and the P buffer rewritten, only once the P V
-            // MMAs that read them have completed: step j - 1 for a rescale, step
-            // j - kPB for the buffer (completion is in issue order)
+            // O may be rescaled only once the P V of step j - 1 has landed in it
             const bool rescale = j > 0 && __any_sync(0xffffffffu, need);
-            const int wait_step = rescale ? j - 1 : j - kPB;
-            if (wait_step >= 0) {
-                ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_done(u, wait_step % kPB),
-                                                                (uint32_t)(wait_step / kPB) & 1u, kWaitLimit));
-                if (!ok) break;
-            }
             if (rescale) {
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait_bounded(o_done(u, (j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u, kWaitLimit));
+                if (!ok) break;
                 tc::fence_after_sync();
 #pragma unroll 1
                 for (int q = 0; q < D / 16; ++q) {
@@ -421,18 +406,10 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
                 }
                 tc::tmem_wait_st();
             }
-            const uint32_t ph = ptile(u, pbuf, 0) + (uint32_t)(r * 128);
-            const uint32_t plo = ph + (uint32_t)C::kPPart;
-#pragma unroll
-            for (int c8 = 0; c8 < C::kN / 8; ++c8) {
-                const uint32_t off = (uint32_t)((c8 ^ (r & 7)) << 4);
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(ph + off), "r"(hw[4 * c8]),
-                             "r"(hw[4 * c8 + 1]), "r"(hw[4 * c8 + 2]), "r"(hw[4 * c8 + 3])
-                             : "memory");
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(plo + off), "r"(lw[4 * c8]),
-                             "r"(lw[4 * c8 + 1]), "r"(lw[4 * c8 + 2]), "r"(lw[4 * c8 + 3])
-                             : "memory");
-            }
+            // P into TMEM over this step's S (already read): P_hi, then P_lo
+            tc::tmem_st32(tl + s_col(u, b), hw);
+            tc::tmem_st32(tl + s_col(u, b) + 32u, lw);
+            tc::tmem_wait_st();
             // V rows of keys that were not loaded or lie past the context hold
             // anything: tile 0's warpgroup zeroes them (row r < 64 of this step's
             // V, whole 128-byte rows) before its P is published; the MMA issues
@@ -450,12 +427,12 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
             tc::fence_async_smem();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full(u, pbuf));
+            if (lane == 0) mbar_arrive(p_full(u, b));
         }
         const int last = nch - 1;
         if (!ok) {
             if (lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
-        } else if (__all_sync(0xffffffffu, mbar_wait_bounded(o_done(u, last % kPB), (uint32_t)(last / kPB) & 1u,
+        } else if (__all_sync(0xffffffffu, mbar_wait_bounded(o_done(u, last & 1), (uint32_t)(last >> 1) & 1u,
                                                               kWaitLimit))) {
             // ---- epilogue: out = O / l for this row
             tc::fence_after_sync();
