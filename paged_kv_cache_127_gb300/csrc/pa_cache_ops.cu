@@ -52,6 +52,30 @@ __global__ void write_kv_kernel(const uint4 *__restrict__ k, const uint4 *__rest
     }
 }
 
+// Copy `chunks` 16-byte chunks of one block (source and destination blocks
+// are distinct, so the ranges do not overlap).  The CTA's slice (blockIdx.z
+// of gridDim.z) is copied kCopyUnroll chunks per thread at a time: all loads
+// first, then all stores, so each thread keeps kCopyUnroll reads in flight
+// (a read of pinned host memory crosses the CPU-GPU link, with a long latency).
+constexpr int kCopyUnroll = 8;
+
+__device__ __forceinline__ void copy_chunks(const uint4 *__restrict__ from, uint4 *__restrict__ to, int64_t chunks) {
+    const int64_t stride = (int64_t)blockDim.x * gridDim.z;
+    for (int64_t i0 = threadIdx.x + (int64_t)blockIdx.z * blockDim.x; i0 < chunks; i0 += stride * kCopyUnroll) {
+        uint4 v[kCopyUnroll];
+#pragma unroll
+        for (int u = 0; u < kCopyUnroll; ++u) {
+            const int64_t i = i0 + u * stride;
+            if (i < chunks) v[u] = from[i];
+        }
+#pragma unroll
+        for (int u = 0; u < kCopyUnroll; ++u) {
+            const int64_t i = i0 + u * stride;
+            if (i < chunks) to[i] = v[u];
+        }
+    }
+}
+
 // grid: (pair, 2 * layer + {0: K, 1: V}, slice of the block)
 __global__ void copy_blocks_kernel(uint4 *kc, uint4 *vc, const int64_t *__restrict__ pairs,
                                    int64_t chunks, int64_t layer_chunks, int N, unsigned int *err) {
@@ -65,11 +89,7 @@ __global__ void copy_blocks_kernel(uint4 *kc, uint4 *vc, const int64_t *__restri
         return;
     }
     uint4 *base = ((blockIdx.y & 1) ? vc : kc) + (int64_t)(blockIdx.y >> 1) * layer_chunks;
-    const uint4 *from = base + src * chunks;
-    uint4 *to = base + dst * chunks;
-    for (int64_t i = threadIdx.x + (int64_t)blockIdx.z * blockDim.x; i < chunks;
-         i += (int64_t)blockDim.x * gridDim.z)
-        to[i] = from[i];
+    copy_chunks(base + src * chunks, base + dst * chunks, chunks);
 }
 
 // Block swap between a device pool and a host pool (pinned host memory the
@@ -91,9 +111,7 @@ __global__ void swap_blocks_kernel(const uint4 *from_k, const uint4 *from_v, uin
     const int64_t layer = blockIdx.y >> 1;
     const uint4 *from = ((blockIdx.y & 1) ? from_v : from_k) + layer * from_layer + src * chunks;
     uint4 *to = ((blockIdx.y & 1) ? to_v : to_k) + layer * to_layer + dst * chunks;
-    for (int64_t i = threadIdx.x + (int64_t)blockIdx.z * blockDim.x; i < chunks;
-         i += (int64_t)blockDim.x * gridDim.z)
-        to[i] = from[i];
+    copy_chunks(from, to, chunks);
 }
 
 cudaError_t launch_swap_blocks(const void *from_k, const void *from_v, void *to_k, void *to_v,
