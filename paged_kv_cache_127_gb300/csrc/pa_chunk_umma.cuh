@@ -8,8 +8,8 @@
 // for chunks whose (query token, query head) rows fill 128-row tiles.
 //
 // Work: one CTA per (MT 128-row tiles, KV head, sequence); the rows of a KV
-// head are r = t * G + gq.  The CTA walks the visible context in 64-key
-// steps, with no split across CTAs (a tile has enough rows to keep the tensor
+// head are r = t * G + gq.  The CTA walks the visible context in steps of
+// PA_CHUNK_UMMA_KEYS keys, with no split across CTAs (a tile has enough rows to keep the tensor
 // cores busy), so there is no merge.  MT = 2 tiles share every K/V load and
 // give the softmax two warpgroups.  Warp roles:
 //   warps 0, 2   producers of K and of V: 16-row TMA boxes (one KV head, both
@@ -20,8 +20,8 @@
 //                per-stage mask;
 //   warps 1, 3   issue the MMAs (lane 0), S in warp 1 (which also allocates
 //                TMEM, 256 columns per tile), P V in warp 3, per tile u:
-//                  S_u,j = Q_u K_j^T   M 128, N 64,  K = D    -> TMEM S[u][j % 2]
-//                  O_u  += P_u,j V_j   M 128, N = D, K 64     -> TMEM O[u]
+//                  S_u,j = Q_u K_j^T   M 128, N = keys, K = D     -> TMEM S[u][j % kSB]
+//                  O_u  += P_u,j V_j   M 128, N = D,    K = keys  -> TMEM O[u]
 //                with P split into P_hi + P_lo (two bf16 / f16 operands) so
 //                the probabilities keep ~16 significant bits;
 //   warps 4..    one softmax warpgroup per tile, one thread per row (TMEM
@@ -52,14 +52,22 @@
 
 namespace pa {
 
+// Keys per step: each tile has 128 TMEM columns for S/P buffers, so 128 / keys
+// of them (a step's S may run that many steps minus one ahead of the P V that
+// frees its buffer).
+#ifndef PA_CHUNK_UMMA_KEYS
+#define PA_CHUNK_UMMA_KEYS 64
+#endif
+
 template <int D, int MT>
 struct UmmaCfg {
     static constexpr int kM = 128;                         // rows per tile (TMEM lanes)
-    static constexpr int kN = 64;                          // keys per step
+    static constexpr int kN = PA_CHUNK_UMMA_KEYS;          // keys per step
+    static constexpr int kSB = 128 / kN;                   // S/P buffers per tile
     static constexpr int kBoxes = kN / 16;                 // 16-row TMA boxes per step
     static constexpr int kSub = D / 64;                    // 128-byte halves of a row
     static constexpr int kKS = D / 16;                     // k-steps of S = Q K^T
-    static constexpr int kStages = 4;
+    static constexpr int kStages = kN == 64 ? 4 : 8;
     static constexpr int kThreads = 128 + 128 * MT;        // K producer, S issuer, V producer, P V issuer, MT warpgroups
     static constexpr int kHalf = kN * 128;                 // one half of K (or V) of a step
     static constexpr int kTile = kSub * kHalf;             // K (or V) of a step
@@ -69,19 +77,20 @@ struct UmmaCfg {
     static constexpr size_t kQOff = 0;
     static constexpr size_t kKVOff = kQOff + (size_t)MT * kQTile;
     static constexpr size_t kBarOff = kKVOff + (size_t)kStages * kStageBytes;
-    // k_full, k_empty, v_full, v_empty [kStages] | per tile: s_full[2] p_full[2] o_done[2] q_full |
+    // k_full, k_empty, v_full, v_empty [kStages] | per tile: s_full, p_full, o_done [kSB], q_full |
     // drain_s drain_p
-    static constexpr int kTileBars = 7;
+    static constexpr int kTileBars = 3 * kSB + 1;
     static constexpr int kNumBars = 4 * kStages + MT * kTileBars + 2;
     static constexpr size_t kMaskOff = kBarOff + 8 * kNumBars;
     static constexpr size_t kSlotOff = kMaskOff + 4 * kStages;
     static constexpr size_t kSmem = kSlotOff + 16 + 1024;  // + alignment slack
     static constexpr uint32_t kTmemCols = 256 * MT;
-    static constexpr uint32_t kOCol = 128 * MT;            // S[u][b] at 128 u + 64 b; O[u] at kOCol + D u
-    // P[u][b] aliases S[u][b]: P_hi in its first 32 columns, P_lo in the next 32
-    // (two 16-bit values per column)
+    static constexpr uint32_t kOCol = 128 * MT;            // S[u][b] at 128 u + kN b; O[u] at kOCol + D u
+    // P[u][b] aliases S[u][b]: P_hi in its first kN / 2 columns, P_lo in the next
+    // kN / 2 (two 16-bit values per column)
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(MT == 1 || MT == 2, "tiles per CTA");
+    static_assert(kN == 32 || kN == 64, "keys per step");
     static_assert(kOCol + MT * D <= kTmemCols, "TMEM budget");
     static_assert(kKVOff % 1024 == 0, "swizzle atoms 1024-byte aligned");
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
@@ -118,7 +127,7 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
     const int len = a.context_lens[s];
     const int tiles = min(MT, (n * G - r0 + C::kM - 1) / C::kM);  // tiles with at least one row
     const int t_last = min(n - 1, (r0 + C::kM * tiles - 1) / G);
-    const int nch = (len - n + t_last) / C::kN + 1;              // 64-key steps up to the last position
+    const int nch = (len - n + t_last) / C::kN + 1;              // kN-key steps up to the last position
 
     const uint32_t qb = base + (uint32_t)C::kQOff;
     const uint32_t kvb = base + (uint32_t)C::kKVOff;
@@ -128,15 +137,16 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
     auto v_full = [&](int i) { return bars + 8u * (uint32_t)(2 * C::kStages + i); };
     auto v_empty = [&](int i) { return bars + 8u * (uint32_t)(3 * C::kStages + i); };
     auto tbar = [&](int u, int i) { return bars + 8u * (uint32_t)(4 * C::kStages + u * C::kTileBars + i); };
+    constexpr int kSB = C::kSB;
     auto s_full = [&](int u, int b) { return tbar(u, b); };
-    auto p_full = [&](int u, int b) { return tbar(u, 2 + b); };
+    auto p_full = [&](int u, int b) { return tbar(u, kSB + b); };
     // P V of a step on buffer b complete: O is up to date and S/P[u][b] may be rewritten
-    auto o_done = [&](int u, int b) { return tbar(u, 4 + b); };
-    auto q_full = [&](int u) { return tbar(u, 6); };
+    auto o_done = [&](int u, int b) { return tbar(u, 2 * kSB + b); };
+    auto q_full = [&](int u) { return tbar(u, 3 * kSB); };
     const uint32_t drain_s = bars + 8u * (uint32_t)(C::kNumBars - 2);
     const uint32_t drain_p = bars + 8u * (uint32_t)(C::kNumBars - 1);
     auto qtile = [&](int u) { return qb + (uint32_t)(u * C::kQTile); };
-    auto s_col = [&](int u, int b) { return (uint32_t)(128 * u + 64 * b); };
+    auto s_col = [&](int u, int b) { return (uint32_t)(128 * u + C::kN * b); };
     auto o_col = [&](int u) { return C::kOCol + (uint32_t)(D * u); };
     int *vmask = reinterpret_cast<int *>(basep + C::kMaskOff);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(basep + C::kSlotOff);
@@ -149,7 +159,7 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
             mbar_init(v_empty(i), 1);
         }
         for (int u = 0; u < MT; ++u) {
-            for (int b = 0; b < 2; ++b) {
+            for (int b = 0; b < kSB; ++b) {
                 mbar_init(s_full(u, b), 1);
                 mbar_init(p_full(u, b), 4);
                 mbar_init(o_done(u, b), 1);
@@ -232,12 +242,12 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
         for (int u = 0; u < tiles && ok; ++u) ok = mbar_wait_bounded(q_full(u), 0u, kWaitLimit);
         for (int j = 0; ok && j < nch; ++j) {
             const int st = j % C::kStages;
-            const int b = j & 1;
+            const int b = j % kSB;
             ok = mbar_wait_bounded(k_full(st), (uint32_t)(j / C::kStages) & 1u, kWaitLimit);
             const uint32_t kst = kvb + (uint32_t)(st * C::kStageBytes);
             for (int u = 0; u < tiles && ok; ++u) {
-                // S/P[u][b] is free once the P V of step j - 2 has read P from it
-                if (j >= 2) ok = mbar_wait_bounded(o_done(u, b), (uint32_t)((j >> 1) - 1) & 1u, kWaitLimit);
+                // S/P[u][b] is free once the P V of step j - kSB has read P from it
+                if (j >= kSB) ok = mbar_wait_bounded(o_done(u, b), (uint32_t)((j / kSB) - 1) & 1u, kWaitLimit);
                 if (!ok) break;
                 tc::fence_after_sync();
                 if (lane == 0) {
@@ -269,12 +279,12 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
         constexpr uint32_t idesc_o = tc::f16_idesc(kBf16, true, C::kM, D);
         bool ok = true;
         for (int c = 0; ok && c < nch; ++c) {
-            const int b = c & 1;
+            const int b = c % kSB;
             const int st = c % C::kStages;
             const uint32_t vst = kvb + (uint32_t)(st * C::kStageBytes + C::kTile);
             ok = mbar_wait_bounded(v_full(st), (uint32_t)(c / C::kStages) & 1u, kWaitLimit);
             for (int u = 0; u < tiles && ok; ++u) {
-                ok = mbar_wait_bounded(p_full(u, b), (uint32_t)(c >> 1) & 1u, kWaitLimit);
+                ok = mbar_wait_bounded(p_full(u, b), (uint32_t)(c / kSB) & 1u, kWaitLimit);
                 if (!ok) break;
                 tc::fence_after_sync();
                 if (lane == 0) {
@@ -282,7 +292,7 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
                     for (int part = 0; part < 2; ++part) {
 #pragma unroll
                         for (int k = 0; k < C::kN / 16; ++k) {
-                            const uint32_t at = tbase + s_col(u, b) + (uint32_t)(32 * part + 8 * k);
+                            const uint32_t at = tbase + s_col(u, b) + (uint32_t)((C::kN / 2) * part + 8 * k);
                             const uint64_t bd = tc::sw128_desc(vst + 2048u * k, (uint32_t)C::kHalf, 1024u);
                             tc::mma_f16_ts(tbase + o_col(u), at, bd, idesc_o, (c > 0 || part > 0 || k > 0) ? 1u : 0u);
                         }
@@ -331,14 +341,14 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nch; ++j) {
-            const int b = j & 1;
+            const int b = j % kSB;
             const int st = j % C::kStages;
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(s_full(u, b), (uint32_t)(j >> 1) & 1u, kWaitLimit));
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(s_full(u, b), (uint32_t)(j / kSB) & 1u, kWaitLimit));
             if (!ok) break;
             tc::fence_after_sync();
-            uint32_t sv[2][32];
-            tc::tmem_ld32(tl + s_col(u, b), sv[0]);
-            tc::tmem_ld32(tl + s_col(u, b) + 32u, sv[1]);
+            uint32_t sv[C::kN / 32][32];
+#pragma unroll
+            for (int q = 0; q < C::kN / 32; ++q) tc::tmem_ld32(tl + s_col(u, b) + 32u * q, sv[q]);
             tc::tmem_wait_ld();
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(v_full(st), (uint32_t)(j / C::kStages) & 1u, kWaitLimit));
             if (!ok) break;
@@ -392,7 +402,7 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
             const bool rescale = j > 0 && __any_sync(0xffffffffu, need);
             if (rescale) {
                 ok = __all_sync(0xffffffffu,
-                                mbar_wait_bounded(o_done(u, (j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u, kWaitLimit));
+                                mbar_wait_bounded(o_done(u, (j - 1) % kSB), (uint32_t)((j - 1) / kSB) & 1u, kWaitLimit));
                 if (!ok) break;
                 tc::fence_after_sync();
 #pragma unroll 1
@@ -407,8 +417,13 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
                 tc::tmem_wait_st();
             }
             // P into TMEM over this step's S (already read): P_hi, then P_lo
-            tc::tmem_st32(tl + s_col(u, b), hw);
-            tc::tmem_st32(tl + s_col(u, b) + 32u, lw);
+            if constexpr (C::kN == 64) {
+                tc::tmem_st32(tl + s_col(u, b), hw);
+                tc::tmem_st32(tl + s_col(u, b) + 32u, lw);
+            } else {
+                tc::tmem_st16(tl + s_col(u, b), hw);
+                tc::tmem_st16(tl + s_col(u, b) + 16u, lw);
+            }
             tc::tmem_wait_st();
             // V rows of keys that were not loaded or lie past the context hold
             // anything: tile 0's warpgroup zeroes them (row r < 64 of this step's
@@ -432,7 +447,7 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
         const int last = nch - 1;
         if (!ok) {
             if (lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
-        } else if (__all_sync(0xffffffffu, mbar_wait_bounded(o_done(u, last & 1), (uint32_t)(last >> 1) & 1u,
+        } else if (__all_sync(0xffffffffu, mbar_wait_bounded(o_done(u, last % kSB), (uint32_t)(last / kSB) & 1u,
                                                               kWaitLimit))) {
             // ---- epilogue: out = O / l for this row
             tc::fence_after_sync();
