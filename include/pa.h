@@ -71,7 +71,11 @@ typedef struct pa_dims {
     int32_t num_blocks;          /* N: physical blocks in the pool                   */
     int32_t max_blocks_per_seq;  /* columns of block_tables                          */
     int32_t partition_size;      /* context tokens per split-K partition; a multiple */
-                                 /* of B, at most 256 * B; 0 selects 512             */
+                                 /* of B, at most 256 * B.  0 chooses by batch: with */
+                                 /* W = num_seqs * num_kv_heads / 4 (work items per  */
+                                 /* partition), 512 if W >= 256, 256 if W >= 32,     */
+                                 /* else 128 (smaller partitions give a small batch  */
+                                 /* enough parallel work)                            */
     int32_t kv_dtype;            /* pa_dtype of q, k, v, k_cache and v_cache         */
 } pa_dims;
 

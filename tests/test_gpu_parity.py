@@ -42,7 +42,7 @@ def test_decode_small_shapes(gpu, dtype, D, B, G):
     q, K, V, kc, vc, tables, lens = random_case(rng, dtype, len(lens), G * Hkv, Hkv, D, B, lens)
     scale = 1.0 / math.sqrt(D)
     ref = oracle.decode(q, kc, vc, tables, lens, scale, dtype)
-    for psize in (0, B, 4 * B):   # default 512 (one partition for most), and split-K
+    for psize in (0, B, 4 * B):   # the automatic size (128 tokens at this batch), and split-K
         got = run_decode(torch, pa, dtype, q, kc, vc, tables, lens, scale, psize)
         assert_attention_close(got, ref)
         if dtype == "f32":
