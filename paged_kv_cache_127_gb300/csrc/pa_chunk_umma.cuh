@@ -384,20 +384,24 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
             const float alpha = (need && j > 0) ? ex2(m_used - mc) : 1.f;
             if (need) m_used = mc;
             const float mu = m_used == -INFINITY ? 0.f : m_used;
-            // P = exp2(x - m) split into P_hi + P_lo, in registers before waiting;
-            // the row sum in 8 independent partial sums
+            // P = exp2(x - m) split into P_hi + P_lo, in registers before waiting,
+            // two keys per packed f32x2 operation; the row sum in 4 pair accumulators
             uint32_t hw[C::kN / 2], lw[C::kN / 2];
-            float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            uint64_t ls[4] = {0ull, 0ull, 0ull, 0ull};
+            const uint64_t mul2 = tc::f2(mul, mul), nmu2 = tc::f2(-mu, -mu);
 #pragma unroll
             for (int v = 0; v < C::kN / 2; ++v) {
-                const float p0 = ex2(fmaf(f[2 * v], mul, -mu));
-                const float p1 = ex2(fmaf(f[2 * v + 1], mul, -mu));
-                ls[v & 7] += p0 + p1;
+                const float2 xa = tc::f2split(tc::fma2(tc::f2(f[2 * v], f[2 * v + 1]), mul2, nmu2));
+                const float p0 = ex2(xa.x), p1 = ex2(xa.y);
+                const uint64_t pp = tc::f2(p0, p1);
+                ls[v & 3] = tc::add2(ls[v & 3], pp);
                 hw[v] = M::pack(p0, p1);
                 const float2 hf = M::unpack(hw[v]);
-                lw[v] = M::pack(p0 - hf.x, p1 - hf.y);
+                const float2 d = tc::f2split(tc::sub2(pp, tc::f2(hf.x, hf.y)));
+                lw[v] = M::pack(d.x, d.y);
             }
-            l = l * alpha + (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
+            const float2 s01 = tc::f2split(tc::add2(ls[0], ls[1])), s23 = tc::f2split(tc::add2(ls[2], ls[3]));
+            l = l * alpha + ((s01.x + s01.y) + (s23.x + s23.y));
             // O may be rescaled only once the P V of step j - 1 has landed in it
             const bool rescale = j > 0 && __any_sync(0xffffffffu, need);
             if (rescale) {
