@@ -260,14 +260,16 @@ PA_API int32_t pa_copy_blocks_layers(const pa_dims *dims, void *k_caches, void *
 
 /*
  * Step graph -- one decode step over num_layers layers, captured once into a
- * CUDA graph: for l = 0 .. L-1, pa_write_kv then pa_decode of layer l.  Every
+ * CUDA graph: for l = 0 .. L-1, pa_write_kv then pa_decode of layer l (the
+ * decode work list, which depends only on the shared tables and lengths, is
+ * built once per launch rather than per layer).  Every
  * pointer is a fixed device buffer read at each launch (update the buffers,
  * then launch); layer l uses
  *     k_caches + l * cache_layer_stride      (and v_caches)
  *     q        + l * q_layer_stride          [S, Hq, D]
  *     k_new    + l * kv_new_layer_stride     [num_tokens, Hkv, D] (and v_new)
  *     out      + l * out_layer_stride        [S, Hq, D] fp32
- * (strides in bytes); slot_mapping, block_tables, context_lens and the
+ * (strides in bytes; out_layer_stride a multiple of 16); slot_mapping, block_tables, context_lens and the
  * workspace are shared by all layers (layers run in order).  Arguments are
  * validated as by the two calls; on failure NULL is returned and *status
  * (nullable) holds the pa_status.  Copy-on-write copies, which are rare and

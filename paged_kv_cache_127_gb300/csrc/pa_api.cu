@@ -204,9 +204,14 @@ size_t pa_decode_workspace_bytes(const pa_dims *dims) {
     return workspace_bytes_for(dims, parts);
 }
 
-int32_t pa_decode(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
-                  const int32_t *block_tables, const int32_t *context_lens, float scale, float *out,
-                  void *workspace, size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace pa {
+
+int32_t decode_call(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *block_tables, const int32_t *context_lens, float scale, float *out,
+                    void *workspace, size_t workspace_bytes, void *stream, DecodePhase phase, int zero_layers,
+                    long long out_layer_floats) {
     int32_t parts = 0;
     int32_t rc = check_decode_dims(dims, &parts);
     if (rc != PA_OK) return rc;
@@ -244,10 +249,13 @@ int32_t pa_decode(const pa_dims *dims, const void *q, const void *k_cache, const
     a.max_parts = parts;
     a.head_group = pa::decode_head_group(dims->num_kv_heads);
     a.scale = scale;
+    a.zero_layers = zero_layers;
+    a.out_layer_floats = out_layer_floats;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (dims->kv_dtype == PA_F32) {
+        if (phase == DecodePhase::kPlanOnly) return PA_OK;  // the CUDA-core path has no plan
         // fp32 caches: CUDA-core kernel, then the merge kernel for split-K
         e = pa::launch_decode_f32(a, st);
         if (e != cudaSuccess) return to_status(e);
@@ -266,12 +274,26 @@ int32_t pa_decode(const pa_dims *dims, const void *q, const void *k_cache, const
     if (e == cudaSuccess)
         e = cache_tensor_map(v_cache, bf16, dims->head_dim, dims->block_size, block_heads, a.head_group, &tmv);
     if (e != cudaSuccess) return PA_ERR_CUDA;
-    e = pa::launch_decode_plan(a, st);
-    if (e != cudaSuccess) return to_status(e);
+    if (phase != DecodePhase::kRunOnly) {
+        e = pa::launch_decode_plan(a, st);
+        if (e != cudaSuccess) return to_status(e);
+        if (phase == DecodePhase::kPlanOnly) return PA_OK;
+    }
     e = bf16 ? pa::launch_decode_mma_bf16(a, tmk, tmv, st) : pa::launch_decode_mma_f16(a, tmk, tmv, st);
     if (e != cudaSuccess) return to_status(e);
     if (parts > 1) e = pa::launch_decode_merge(a, st);
     return to_status(e);
+}
+
+}  // namespace pa
+
+extern "C" {
+
+int32_t pa_decode(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
+                  const int32_t *block_tables, const int32_t *context_lens, float scale, float *out,
+                  void *workspace, size_t workspace_bytes, void *stream) {
+    return pa::decode_call(dims, q, k_cache, v_cache, block_tables, context_lens, scale, out, workspace,
+                           workspace_bytes, stream, pa::DecodePhase::kPlanAndRun, 1, 0);
 }
 
 size_t pa_chunk_workspace_bytes(const pa_dims *dims, int32_t num_tokens, int32_t max_query_len) {

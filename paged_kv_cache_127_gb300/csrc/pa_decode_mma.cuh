@@ -406,6 +406,15 @@ __global__ void __launch_bounds__(MmaCfg<D, HG>::kThreads, 2)
     if (warp == 0) {
         for (int k = cons; k < iss; ++k)
             mbar_wait_bounded(full0 + 8 * (k % C::kStages), (uint32_t)(k / C::kStages) & 1u, kWaitLimit);
+        // Warp 0's lane 0 made every claim of this CTA.  The last CTA to get
+        // here resets the counters, so the plan's list can serve the next launch.
+        if (lane == 0) {
+            __threadfence();
+            if (atomicAdd(a.plan_hdr + 2, 1) == (int)gridDim.x - 1) {
+                a.plan_hdr[1] = 0;
+                a.plan_hdr[2] = 0;
+            }
+        }
     }
 }
 

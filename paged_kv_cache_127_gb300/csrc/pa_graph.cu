@@ -5,7 +5,10 @@
 // agnostic: block p is the same slot range in every layer's cache).  Capturing
 // the L x (pa_write_kv, pa_decode) launches into one graph and replaying it
 // removes the host's per-launch cost from the step; the launches keep their
-// programmatic-dependent edges inside the graph.  ("Paged Attention and vLLM",
+// programmatic-dependent edges inside the graph.  The decode work list depends
+// only on the tables and lengths, which all layers share, so the graph runs the
+// plan kernel once per step and each layer only its decode and merge kernels.
+// ("Paged Attention and vLLM",
 // "Continuous Batching and Scheduler": a new batch decision every iteration;
 // "KV Cache Optimization and Management", recap: the cache grows by one token
 // per layer per generated token.)
@@ -15,6 +18,7 @@
 #include <new>
 
 #include "../../include/pa.h"
+#include "pa_internal.h"
 
 struct pa_step_graph {
     cudaGraph_t graph = nullptr;
@@ -52,16 +56,20 @@ pa_step_graph *pa_step_graph_create(const pa_dims *dims, int32_t num_layers, voi
     // Relaxed mode: the launch paths may make first-use set-up calls (kernel
     // attributes, symbol lookups, tensor-map encoding) that are not stream work.
     int32_t rc = PA_OK;
-    if (cudaStreamBeginCapture(st, cudaStreamCaptureModeRelaxed) != cudaSuccess) rc = PA_ERR_CUDA;
+    if (out_layer_stride % 16 != 0) rc = PA_ERR_INVALID;
+    if (rc == PA_OK && cudaStreamBeginCapture(st, cudaStreamCaptureModeRelaxed) != cudaSuccess) rc = PA_ERR_CUDA;
+    auto out_l = [&](int32_t l) { return reinterpret_cast<float *>(const_cast<char *>(at(out, l * out_layer_stride))); };
+    if (rc == PA_OK)  // the work list (and every layer's zero rows) once for the step
+        rc = pa::decode_call(dims, q, k_caches, v_caches, block_tables, context_lens, scale, out_l(0), workspace,
+                             workspace_bytes, st, pa::DecodePhase::kPlanOnly, num_layers, out_layer_stride / 4);
     for (int32_t l = 0; l < num_layers && rc == PA_OK; ++l) {
         void *kc = const_cast<char *>(at(k_caches, l * cache_layer_stride));
         void *vc = const_cast<char *>(at(v_caches, l * cache_layer_stride));
         rc = pa_write_kv(dims, at(k_new, l * kv_new_layer_stride), at(v_new, l * kv_new_layer_stride),
                          slot_mapping, num_tokens, kc, vc, st);
         if (rc != PA_OK) break;
-        rc = pa_decode(dims, at(q, l * q_layer_stride), kc, vc, block_tables, context_lens, scale,
-                       reinterpret_cast<float *>(const_cast<char *>(at(out, l * out_layer_stride))), workspace,
-                       workspace_bytes, st);
+        rc = pa::decode_call(dims, at(q, l * q_layer_stride), kc, vc, block_tables, context_lens, scale, out_l(l),
+                             workspace, workspace_bytes, st, pa::DecodePhase::kRunOnly, 1, 0);
     }
     cudaGraph_t graph = nullptr;
     const cudaError_t end = cudaStreamEndCapture(st, &graph);

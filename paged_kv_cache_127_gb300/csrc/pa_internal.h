@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
+#include "../../include/pa.h"
+
 namespace pa {
 
 // Everything a decode launch needs, already validated by the entry point.
@@ -18,12 +20,17 @@ struct DecodeArgs {
     float *out;
     float *ws_ml;    // [S, Hq, P, 2]  (m in log2 units, l)
     float *ws_acc;   // [S, Hq, P, D]
-    int *plan_hdr;   // [0] work items, [1] claim counter
+    int *plan_hdr;   // [0] work items, [1] claim counter, [2] CTAs done claiming
     int4 *plan_list; // (sequence, partition, tokens, partitions of the sequence) per item, largest first
     unsigned int *err;
     int S, Hq, Hkv, D, B, N, max_blocks, partition_size, max_parts;
     int head_group;  // KV heads per tensor-core work item (decode_head_group)
     float scale;
+    // The plan writes the zero rows of empty contexts into `zero_layers`
+    // outputs, out + l * out_layer_floats (a step over several layers runs the
+    // plan once: the work list depends only on the tables and lengths).
+    int zero_layers;
+    long long out_layer_floats;
 };
 
 // Everything a chunk-attention launch needs (several query tokens per sequence).
@@ -87,7 +94,10 @@ cudaError_t launch_decode_f32(const DecodeArgs &a, cudaStream_t st);
 // Cross-partition merge of the split-K partials (dtype independent).
 cudaError_t launch_decode_merge(const DecodeArgs &a, cudaStream_t st);
 
-// Work list for the tensor-core decode (f16 / bf16 path).
+// Work list for the tensor-core decode (f16 / bf16 path).  The decode kernel
+// leaves the claim counters as the plan set them (the last CTA to finish
+// claiming resets them), so one plan serves several launches over the same
+// tables and lengths, in stream order.
 cudaError_t launch_decode_plan(const DecodeArgs &a, cudaStream_t st);
 
 // Tensor-core decode: f16 / bf16 caches, K and V read through 2-D tensor maps
@@ -96,6 +106,17 @@ cudaError_t launch_decode_mma_f16(const DecodeArgs &a, const CUtensorMap &tmk, c
                                   cudaStream_t st);
 cudaError_t launch_decode_mma_bf16(const DecodeArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                    cudaStream_t st);
+
+// pa_decode with its launches split: kPlanAndRun is pa_decode; kPlanOnly
+// writes the work list (and the zero rows of `zero_layers` outputs spaced
+// out_layer_floats apart); kRunOnly runs the decode and merge kernels on a list
+// an earlier kPlanOnly / kPlanAndRun left in the same workspace, for the same
+// tables and lengths.  Validation and statuses as for pa_decode.
+enum class DecodePhase { kPlanAndRun, kPlanOnly, kRunOnly };
+int32_t decode_call(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *block_tables, const int32_t *context_lens, float scale, float *out,
+                    void *workspace, size_t workspace_bytes, void *stream, DecodePhase phase, int zero_layers,
+                    long long out_layer_floats);
 
 // Encode the tensor map of one cache [N, Hkv, B, D] of 16-bit elements as a
 // 3-D tensor {D, B, N*Hkv}; a box is 64 columns x kChunkRows rows x head_group

@@ -4,9 +4,9 @@
 // partition's token count and the sequence's partition count -- largest
 // partition first (a counting sort on the partition's block count), so the
 // persistent decode kernel hands out big items before small ones and its
-// tail is short.  It also resets the claim counter, writes the all-zero
-// output rows of empty contexts, and flags context lengths outside
-// [0, max_blocks * B].
+// tail is short.  It also resets the claim counters, writes the all-zero
+// output rows of empty contexts (of every layer the list will serve), and
+// flags context lengths outside [0, max_blocks * B].
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -26,7 +26,10 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeArgs a) {
     const int cap = a.max_blocks * B;
     const int maxpb = Pt / B;
     for (int i = tid; i <= maxpb; i += blockDim.x) hist[i] = 0;
-    if (tid == 0) a.plan_hdr[1] = 0;
+    if (tid == 0) {
+        a.plan_hdr[1] = 0;
+        a.plan_hdr[2] = 0;
+    }
     __syncthreads();
     for (int s = tid; s < a.S; s += blockDim.x) {
         int len = a.context_lens[s];
@@ -35,8 +38,10 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeArgs a) {
             len = len < 0 ? 0 : cap;
         }
         if (len == 0) {
-            float4 *row = reinterpret_cast<float4 *>(a.out + (size_t)s * a.Hq * a.D);
-            for (int i = 0; i < a.Hq * a.D / 4; ++i) row[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int l = 0; l < a.zero_layers; ++l) {
+                float4 *row = reinterpret_cast<float4 *>(a.out + l * a.out_layer_floats + (size_t)s * a.Hq * a.D);
+                for (int i = 0; i < a.Hq * a.D / 4; ++i) row[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
             continue;
         }
         const int np = (len + Pt - 1) / Pt;

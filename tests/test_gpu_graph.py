@@ -94,3 +94,46 @@ def test_step_graph_equals_eager_launches_and_oracle(gpu):
         assert_attention_close(g_out[L - 1].cpu().numpy(), ref)
     graph.close()
     assert pa.pa_device_errors(clear=True) == 0
+
+
+@pytest.mark.parametrize("psize", [0, 64])
+def test_step_graph_plan_serves_every_layer(gpu, psize):
+    """One work list per step: every layer matches the oracle, empty contexts
+    give zero rows in every layer, and a second launch (counters reset by the
+    decode kernel itself) gives the same bits."""
+    torch, pa = gpu
+    dtype, L, Hkv, G, D, B = "f16", 4, 4, 2, 64, 16
+    rng = synth.make_rng(63)
+    lens = [0, 40, 1, 333, 0, 129]
+    S = len(lens)
+    _, _, _, kc0, _, tables, lens = random_case(rng, dtype, S, G * Hkv, Hkv, D, B, lens, extra_blocks=4)
+    N = kc0.shape[0]
+    kc = synth.normal(rng, (L, N, Hkv, B, D), 1.0, dtype)
+    vc = synth.normal(rng, (L, N, Hkv, B, D), 1.0, dtype)
+    slots = oracle.slot_mapping(tables, B, np.arange(S, dtype=np.int32), lens - 1)   # -1: empty, skipped
+    dims = pa.make_dims(S, G * Hkv, Hkv, D, B, N, tables.shape[1], psize, dtype)
+    q = synth.normal(rng, (L, S, G * Hkv, D), 1.0, dtype)
+    kn = synth.normal(rng, (L, S, Hkv, D), 1.0, dtype)
+    vn = synth.normal(rng, (L, S, Hkv, D), 1.0, dtype)
+    d_kc, d_vc = to_dev(torch, kc, dtype), to_dev(torch, vc, dtype)
+    out = torch.full((L, S, G * Hkv, D), float("nan"), device="cuda")
+    ws = torch.empty(max(pa.pa_decode_workspace_bytes(dims), 16), dtype=torch.uint8, device="cuda")
+    graph = pa.pa_step_graph_create(dims, d_kc, d_vc, to_dev(torch, q, dtype), to_dev(torch, kn, dtype),
+                                    to_dev(torch, vn, dtype), torch.from_numpy(slots).cuda(),
+                                    torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(), 0.125, out, ws)
+    graph.launch()
+    torch.cuda.synchronize()
+    first = out.clone()
+    out.fill_(float("nan"))
+    graph.launch()                                     # rewrites the same slots with the same rows
+    torch.cuda.synchronize()
+    assert torch.equal(out, first)
+    got = first.cpu().numpy().astype(np.float64)
+    for layer in range(L):
+        k_l, v_l = kc[layer].copy(), vc[layer].copy()
+        oracle.write_kv(kn[layer], vn[layer], slots, k_l, v_l, dtype)
+        ref = oracle.decode(q[layer], k_l, v_l, tables, lens, 0.125, dtype)
+        assert_attention_close(got[layer], ref)
+        np.testing.assert_array_equal(got[layer][lens == 0], 0.0)
+    graph.close()
+    assert pa.pa_device_errors(clear=True) == 0
