@@ -350,6 +350,7 @@ int32_t pa_chunk_attention(const pa_dims *dims, const void *q, const void *k_cac
 
     const bool bf16 = dims->kv_dtype == PA_BF16;
     const bool umma = pa::chunk_uses_umma(max_query_len, dims->num_q_heads / dims->num_kv_heads);
+    a.umma_rows = umma ? pa::chunk_umma_rows(max_query_len, dims->num_q_heads / dims->num_kv_heads) : 0;
     const int box_heads = umma ? 1 : a.head_group;
     const long long block_heads = (long long)dims->num_blocks * dims->num_kv_heads;
     CUtensorMap tmk, tmv;

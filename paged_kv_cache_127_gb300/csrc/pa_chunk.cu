@@ -4,9 +4,11 @@
 // The plan (one CTA) checks that query_start is non-decreasing within [0, T],
 // maps every query row to its sequence (-1 where none, or where the sequence
 // is skipped because n_s > context length or n_s > max_query_len), and lists
-// every (sequence, partition, row block) whose rows see at least one key of
-// the partition, with the partition's token count up to the block's last row
-// position, largest first (a counting sort on the block count).  The merge
+// the work: on the mma.sync path every (sequence, partition, row block) whose
+// rows see at least one key of the partition, with the partition's token count
+// up to the block's last row position, largest first (a counting sort on the
+// block count); on the tcgen05 path every (sequence, group of 128-row tiles)
+// with its step count, longest first.  The merge
 // combines, for each query row, the partitions 0 .. pos / partition_size it
 // sees ("Paged Attention and vLLM", "Paged Attention CUDA Kernel", the merge
 // equation).
@@ -31,9 +33,17 @@ __device__ __forceinline__ int block_tokens(int n, int len, int G, int rows_per_
 
 }  // namespace
 
+// tcgen05 path: steps of the CTA that serves tile group g of a sequence with n
+// queries and context len (up to its last row's position), kN keys per step.
+__device__ __forceinline__ int umma_steps(int n, int len, int G, int rows_cta, int g) {
+    const int t_last = min(n - 1, (g * rows_cta + rows_cta - 1) / G);
+    return (len - n + t_last) / PA_CHUNK_UMMA_KEYS + 1;
+}
+
 __global__ void __launch_bounds__(1024) chunk_plan_kernel(const ChunkArgs a) {
-    __shared__ int hist[kMaxPartitionBlocks + 1];
-    __shared__ int start[kMaxPartitionBlocks + 1];
+    constexpr int kBins = kUmmaStepBins > kMaxPartitionBlocks + 1 ? kUmmaStepBins : kMaxPartitionBlocks + 1;
+    __shared__ int hist[kBins];
+    __shared__ int start[kBins];
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int tid = threadIdx.x;
@@ -43,7 +53,7 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const ChunkArgs a) {
     const int maxpb = Pt / B;
     const int G = a.Hq / a.Hkv;
     const int rpb = a.row_warps * 16;
-    for (int i = tid; i <= maxpb; i += blockDim.x) hist[i] = 0;
+    for (int i = tid; i < kBins; i += blockDim.x) hist[i] = 0;
     int my_bad = 0;
     if (tid == 0) {
         a.plan_hdr[1] = 0;
@@ -73,6 +83,43 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const ChunkArgs a) {
             if (len >= 0 && len <= cap && n <= len && n <= a.max_query_len) s = lo;
         }
         a.tok_seq[i] = s;
+    }
+    if (a.umma_rows > 0) {
+        // tcgen05 path: one entry per (sequence, tile group), by step count, longest first
+        const int R = a.umma_rows;
+        for (int s = tid; s < a.S; s += blockDim.x) {
+            const int raw = a.context_lens[s];
+            const int len = clamp_len(raw, cap);
+            const int n = a.query_start[s + 1] - a.query_start[s];
+            if (raw != len || n > len || n > a.max_query_len) {
+                set_error(a.err, PA_DEVERR_BAD_LEN);
+                continue;
+            }
+            for (int g = 0; g * R < n * G; ++g)
+                atomicAdd(&hist[min(umma_steps(n, len, G, R, g), kBins - 1)], 1);
+        }
+        __syncthreads();
+        if (tid == 0) {
+            int acc = 0;
+            for (int z = kBins - 1; z >= 0; --z) {
+                start[z] = acc;
+                acc += hist[z];
+            }
+            a.plan_hdr[0] = acc;
+        }
+        __syncthreads();
+        for (int s = tid; s < a.S; s += blockDim.x) {
+            const int raw = a.context_lens[s];
+            const int len = clamp_len(raw, cap);
+            const int n = a.query_start[s + 1] - a.query_start[s];
+            if (raw != len || n > len || n > a.max_query_len) continue;
+            for (int g = 0; g * R < n * G; ++g) {
+                const int steps = umma_steps(n, len, G, R, g);
+                const int pos = atomicAdd(&start[min(steps, kBins - 1)], 1);
+                a.plan_list[pos] = make_int4(s, g, steps, 0);
+            }
+        }
+        return;
     }
     for (int s = tid; s < a.S; s += blockDim.x) {
         const int raw = a.context_lens[s];

@@ -7,8 +7,9 @@
 // "KV Cache Fundamentals" and "Block Table and Logical-to-Physical Mapping"),
 // for chunks whose (query token, query head) rows fill 128-row tiles.
 //
-// Work: one CTA per (MT 128-row tiles, KV head, sequence); the rows of a KV
-// head are r = t * G + gq.  The CTA walks the visible context in steps of
+// Work: one CTA per (MT 128-row tiles, KV head, sequence), taken from the plan
+// kernel's list, longest first (so the longest CTAs do not form the tail); the
+// rows of a KV head are r = t * G + gq.  The CTA walks the visible context in steps of
 // PA_CHUNK_UMMA_KEYS keys, with no split across CTAs (a tile has enough rows to keep the tensor
 // cores busy), so there is no merge.  MT = 2 tiles share every K/V load and
 // give the softmax two warpgroups.  Warp roles:
@@ -18,13 +19,14 @@
 //                the P V that frees the V stage; table entries outside the pool,
 //                or keys past the context, are not loaded and are marked in a
 //                per-stage mask;
-//   warps 1, 3   issue the MMAs (lane 0), S in warp 1 (which also allocates
-//                TMEM, 256 columns per tile), P V in warp 3, per tile u:
+//   warps 1, 3   issue tile 0's MMAs (lane 0), S in warp 1 (which also
+//   (4, 5)       allocates TMEM, 256 columns per tile), P V in warp 3; warps 4
+//                and 5 do the same for tile 1, so a tile waits only on itself:
 //                  S_u,j = Q_u K_j^T   M 128, N = keys, K = D     -> TMEM S[u][j % kSB]
 //                  O_u  += P_u,j V_j   M 128, N = D,    K = keys  -> TMEM O[u]
 //                with P split into P_hi + P_lo (two bf16 / f16 operands) so
 //                the probabilities keep ~16 significant bits;
-//   warps 4..    one softmax warpgroup per tile, one thread per row (TMEM
+//   warps 4.. (6.. with two tiles)  one softmax warpgroup per tile, one thread per row (TMEM
 //                lane 32 * (warp % 4) + lane): read S, mask (causal and
 //                not-loaded keys), online softmax in log2 units, write P_hi /
 //                P_lo into TMEM over the S just read (the P V MMA takes its A
@@ -52,12 +54,9 @@
 
 namespace pa {
 
-// Keys per step: each tile has 128 TMEM columns for S/P buffers, so 128 / keys
-// of them (a step's S may run that many steps minus one ahead of the P V that
-// frees its buffer).
-#ifndef PA_CHUNK_UMMA_KEYS
-#define PA_CHUNK_UMMA_KEYS 64
-#endif
+// Keys per step (PA_CHUNK_UMMA_KEYS): each tile has 128 TMEM columns for S/P
+// buffers, so 128 / keys of them (a step's S may run that many steps minus one
+// ahead of the P V that frees its buffer).
 
 template <int D, int MT>
 struct UmmaCfg {
@@ -68,7 +67,10 @@ struct UmmaCfg {
     static constexpr int kSub = D / 64;                    // 128-byte halves of a row
     static constexpr int kKS = D / 16;                     // k-steps of S = Q K^T
     static constexpr int kStages = kN == 64 ? 4 : 8;
-    static constexpr int kThreads = 128 + 128 * MT;        // K producer, S issuer, V producer, P V issuer, MT warpgroups
+    // warps: 0 K producer, 2 V producer; per tile u an S issuer (warp 1, 4) and a
+    // P V issuer (warp 3, 5); then one softmax warpgroup per tile
+    static constexpr int kSoftWarp0 = MT == 2 ? 6 : 4;
+    static constexpr int kThreads = 32 * (kSoftWarp0 + 4 * MT);
     static constexpr int kHalf = kN * 128;                 // one half of K (or V) of a step
     static constexpr int kTile = kSub * kHalf;             // K (or V) of a step
     static constexpr int kStageBytes = 2 * kTile;
@@ -77,10 +79,10 @@ struct UmmaCfg {
     static constexpr size_t kQOff = 0;
     static constexpr size_t kKVOff = kQOff + (size_t)MT * kQTile;
     static constexpr size_t kBarOff = kKVOff + (size_t)kStages * kStageBytes;
-    // k_full, k_empty, v_full, v_empty [kStages] | per tile: s_full, p_full, o_done [kSB], q_full |
-    // drain_s drain_p
-    static constexpr int kTileBars = 3 * kSB + 1;
-    static constexpr int kNumBars = 4 * kStages + MT * kTileBars + 2;
+    // k_full, k_empty, v_full, v_empty, v_zeroed [kStages] | per tile: s_full, p_full, o_done [kSB],
+    // q_full, drain_s, drain_p
+    static constexpr int kTileBars = 3 * kSB + 3;
+    static constexpr int kNumBars = 5 * kStages + MT * kTileBars;
     static constexpr size_t kMaskOff = kBarOff + 8 * kNumBars;
     static constexpr size_t kSlotOff = kMaskOff + 4 * kStages;
     static constexpr size_t kSmem = kSlotOff + 16 + 1024;  // + alignment slack
@@ -116,14 +118,17 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    griddep_wait();  // the plan kernel has validated the query ranges (tok_seq)
-    const int s = blockIdx.z;
-    const int kvh = blockIdx.y;
+    griddep_wait();  // the plan kernel's list of (sequence, tile group), longest first
+    const int item = blockIdx.x / a.Hkv;
+    if (item >= a.plan_hdr[0]) return;
+    const int4 e = a.plan_list[item];
+    const int s = e.x;
+    const int kvh = blockIdx.x % a.Hkv;
     const int G = a.Hq / a.Hkv;
-    const int r0 = blockIdx.x * C::kM * MT;
+    const int r0 = e.y * C::kM * MT;
     const int qs = a.query_start[s];
     const int n = a.query_start[s + 1] - qs;
-    if (n <= 0 || r0 >= n * G || a.tok_seq[qs] != s) return;  // nothing here, or a skipped sequence
+    if (n <= 0 || r0 >= n * G) return;
     const int len = a.context_lens[s];
     const int tiles = min(MT, (n * G - r0 + C::kM - 1) / C::kM);  // tiles with at least one row
     const int t_last = min(n - 1, (r0 + C::kM * tiles - 1) / G);
@@ -136,15 +141,17 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
     auto k_empty = [&](int i) { return bars + 8u * (uint32_t)(C::kStages + i); };
     auto v_full = [&](int i) { return bars + 8u * (uint32_t)(2 * C::kStages + i); };
     auto v_empty = [&](int i) { return bars + 8u * (uint32_t)(3 * C::kStages + i); };
-    auto tbar = [&](int u, int i) { return bars + 8u * (uint32_t)(4 * C::kStages + u * C::kTileBars + i); };
+    // tile 0's softmax has zeroed this step's V rows that must not contribute
+    auto v_zeroed = [&](int i) { return bars + 8u * (uint32_t)(4 * C::kStages + i); };
+    auto tbar = [&](int u, int i) { return bars + 8u * (uint32_t)(5 * C::kStages + u * C::kTileBars + i); };
     constexpr int kSB = C::kSB;
     auto s_full = [&](int u, int b) { return tbar(u, b); };
     auto p_full = [&](int u, int b) { return tbar(u, kSB + b); };
     // P V of a step on buffer b complete: O is up to date and S/P[u][b] may be rewritten
     auto o_done = [&](int u, int b) { return tbar(u, 2 * kSB + b); };
     auto q_full = [&](int u) { return tbar(u, 3 * kSB); };
-    const uint32_t drain_s = bars + 8u * (uint32_t)(C::kNumBars - 2);
-    const uint32_t drain_p = bars + 8u * (uint32_t)(C::kNumBars - 1);
+    auto drain_s = [&](int u) { return tbar(u, 3 * kSB + 1); };
+    auto drain_p = [&](int u) { return tbar(u, 3 * kSB + 2); };
     auto qtile = [&](int u) { return qb + (uint32_t)(u * C::kQTile); };
     auto s_col = [&](int u, int b) { return (uint32_t)(128 * u + C::kN * b); };
     auto o_col = [&](int u) { return C::kOCol + (uint32_t)(D * u); };
@@ -154,9 +161,10 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kStages; ++i) {
             mbar_init(k_full(i), 1);
-            mbar_init(k_empty(i), 1);
+            mbar_init(k_empty(i), tiles);  // one commit per tile's S issuer
             mbar_init(v_full(i), 1);
-            mbar_init(v_empty(i), 1);
+            mbar_init(v_empty(i), tiles);  // one commit per tile's P V issuer
+            mbar_init(v_zeroed(i), 4);
         }
         for (int u = 0; u < MT; ++u) {
             for (int b = 0; b < kSB; ++b) {
@@ -165,9 +173,9 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
                 mbar_init(o_done(u, b), 1);
             }
             mbar_init(q_full(u), 4);
+            mbar_init(drain_s(u), 1);
+            mbar_init(drain_p(u), 1);
         }
-        mbar_init(drain_s, 1);
-        mbar_init(drain_p, 1);
         fence_mbar_init();
         prefetch_tmap(&tmk);
         prefetch_tmap(&tmv);
@@ -235,22 +243,23 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
         for (int k = max(0, j - C::kStages); k < j; ++k)
             mbar_wait_bounded(is_v ? v_full(k % C::kStages) : k_full(k % C::kStages), (uint32_t)(k / C::kStages) & 1u,
                               kWaitLimit);
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ S = Q K^T issuer
-        constexpr uint32_t idesc_s = tc::f16_idesc(kBf16, false, C::kM, C::kN);
-        bool ok = true;
-        for (int u = 0; u < tiles && ok; ++u) ok = mbar_wait_bounded(q_full(u), 0u, kWaitLimit);
-        for (int j = 0; ok && j < nch; ++j) {
-            const int st = j % C::kStages;
-            const int b = j % kSB;
-            ok = mbar_wait_bounded(k_full(st), (uint32_t)(j / C::kStages) & 1u, kWaitLimit);
-            const uint32_t kst = kvb + (uint32_t)(st * C::kStageBytes);
-            for (int u = 0; u < tiles && ok; ++u) {
+    } else if (warp == 1 || (MT == 2 && warp == 4)) {
+        // ------------------------------------------------------------ S = Q K^T issuer of tile u
+        // One issuer per tile: a tile waits for its own P V, not the other tile's.
+        const int u = warp == 1 ? 0 : 1;
+        if (u < tiles) {
+            constexpr uint32_t idesc_s = tc::f16_idesc(kBf16, false, C::kM, C::kN);
+            bool ok = mbar_wait_bounded(q_full(u), 0u, kWaitLimit);
+            for (int j = 0; ok && j < nch; ++j) {
+                const int st = j % C::kStages;
+                const int b = j % kSB;
+                ok = mbar_wait_bounded(k_full(st), (uint32_t)(j / C::kStages) & 1u, kWaitLimit);
                 // S/P[u][b] is free once the P V of step j - kSB has read P from it
-                if (j >= kSB) ok = mbar_wait_bounded(o_done(u, b), (uint32_t)((j / kSB) - 1) & 1u, kWaitLimit);
+                if (ok && j >= kSB) ok = mbar_wait_bounded(o_done(u, b), (uint32_t)((j / kSB) - 1) & 1u, kWaitLimit);
                 if (!ok) break;
                 tc::fence_after_sync();
                 if (lane == 0) {
+                    const uint32_t kst = kvb + (uint32_t)(st * C::kStageBytes);
 #pragma unroll
                     for (int k = 0; k < C::kKS; ++k) {
                         const uint64_t ad =
@@ -260,31 +269,33 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
                         tc::mma_f16_ss(tbase + s_col(u, b), ad, bd, idesc_s, k > 0 ? 1u : 0u);
                     }
                     tc::mma_commit(s_full(u, b));
+                    tc::mma_commit(k_empty(st));  // the K stage is free once every tile's S MMAs complete
                 }
                 __syncwarp();
             }
-            if (!ok) break;
-            if (lane == 0) tc::mma_commit(k_empty(st));  // the K stage is free once these S MMAs complete
+            if (!ok && lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
+            // every MMA issued by this thread has completed before TMEM is freed
+            if (lane == 0) tc::mma_commit(drain_s(u));
             __syncwarp();
+            mbar_wait_bounded(drain_s(u), 0u, kWaitLimit);
         }
-        if (!ok && lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
-        // every MMA issued by this thread has completed before TMEM is freed
-        if (lane == 0) tc::mma_commit(drain_s);
-        __syncwarp();
-        mbar_wait_bounded(drain_s, 0u, kWaitLimit);
-    } else if (warp == 3) {
-        // ------------------------------------------------------------ O += P V issuer
-        // A thread of its own: issuing the next step's S MMAs may block while the
-        // tensor pipe is busy, and must not hold back a P V whose P is ready.
-        constexpr uint32_t idesc_o = tc::f16_idesc(kBf16, true, C::kM, D);
-        bool ok = true;
-        for (int c = 0; ok && c < nch; ++c) {
-            const int b = c % kSB;
-            const int st = c % C::kStages;
-            const uint32_t vst = kvb + (uint32_t)(st * C::kStageBytes + C::kTile);
-            ok = mbar_wait_bounded(v_full(st), (uint32_t)(c / C::kStages) & 1u, kWaitLimit);
-            for (int u = 0; u < tiles && ok; ++u) {
-                ok = mbar_wait_bounded(p_full(u, b), (uint32_t)(c / kSB) & 1u, kWaitLimit);
+    } else if (warp == 3 || (MT == 2 && warp == 5)) {
+        // ------------------------------------------------------------ O += P V issuer of tile u
+        // Threads of their own: issuing S MMAs may block while the tensor pipe is
+        // busy, and must not hold back a P V whose P is ready.
+        const int u = warp == 3 ? 0 : 1;
+        if (u < tiles) {
+            constexpr uint32_t idesc_o = tc::f16_idesc(kBf16, true, C::kM, D);
+            bool ok = true;
+            for (int c = 0; ok && c < nch; ++c) {
+                const int b = c % kSB;
+                const int st = c % C::kStages;
+                const uint32_t vst = kvb + (uint32_t)(st * C::kStageBytes + C::kTile);
+                ok = mbar_wait_bounded(v_full(st), (uint32_t)(c / C::kStages) & 1u, kWaitLimit);
+                // tile 0's softmax zeroes the V rows that must not contribute; tile 0's own
+                // P V is issued after that (its P is published after the zeroing)
+                if (ok && u > 0) ok = mbar_wait_bounded(v_zeroed(st), (uint32_t)(c / C::kStages) & 1u, kWaitLimit);
+                if (ok) ok = mbar_wait_bounded(p_full(u, b), (uint32_t)(c / kSB) & 1u, kWaitLimit);
                 if (!ok) break;
                 tc::fence_after_sync();
                 if (lane == 0) {
@@ -298,20 +309,18 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
                         }
                     }
                     tc::mma_commit(o_done(u, b));
+                    tc::mma_commit(v_empty(st));
                 }
                 __syncwarp();
             }
-            if (!ok) break;
-            if (lane == 0) tc::mma_commit(v_empty(st));
+            if (!ok && lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
+            if (lane == 0) tc::mma_commit(drain_p(u));
             __syncwarp();
+            mbar_wait_bounded(drain_p(u), 0u, kWaitLimit);
         }
-        if (!ok && lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
-        if (lane == 0) tc::mma_commit(drain_p);
-        __syncwarp();
-        mbar_wait_bounded(drain_p, 0u, kWaitLimit);
-    } else if (warp >= 4 && (warp - 4) / 4 < tiles) {
+    } else if (warp >= C::kSoftWarp0 && (warp - C::kSoftWarp0) / 4 < tiles) {
         // ------------------------------------------------------------ softmax (one row per thread)
-        const int u = (warp - 4) / 4;            // tile of this warpgroup
+        const int u = (warp - C::kSoftWarp0) / 4;  // tile of this warpgroup
         const int wq = warp & 3;                 // TMEM lanes 32 * wq .. 32 * wq + 31
         const int r = 32 * wq + lane;            // row within the tile
         const int R = r0 + C::kM * u + r;
@@ -430,9 +439,9 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
             }
             tc::tmem_wait_st();
             // V rows of keys that were not loaded or lie past the context hold
-            // anything: tile 0's warpgroup zeroes them (row r < 64 of this step's
-            // V, whole 128-byte rows) before its P is published; the MMA issues
-            // every tile's P V after tile 0's.
+            // anything: tile 0's warpgroup zeroes them (row r < kN of this step's
+            // V, whole 128-byte rows) before it publishes its P and v_zeroed, which
+            // the other tile's P V issuer waits for.
             if (u == 0 && r < C::kN && (j * C::kN + r >= len || !(mask >> (r >> 4) & 1))) {
                 const uint32_t vrow = kvb + (uint32_t)(st * C::kStageBytes + C::kTile + r * 128);
 #pragma unroll
@@ -446,7 +455,10 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
             tc::fence_async_smem();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full(u, b));
+            if (lane == 0) {
+                mbar_arrive(p_full(u, b));
+                if (u == 0) mbar_arrive(v_zeroed(st));
+            }
         }
         const int last = nch - 1;
         if (!ok) {
@@ -500,9 +512,11 @@ cudaError_t launch_chunk_umma_t(const ChunkArgs &a, const CUtensorMap &tmk, cons
     }
     const int G = a.Hq / a.Hkv;
     const long long rows = (long long)a.max_query_len * G;
-    const int ctas = (int)((rows + C::kM * MT - 1) / (C::kM * MT));
+    const long long groups = (rows + C::kM * MT - 1) / (C::kM * MT);  // tile groups per sequence, at most
+    const long long ctas = groups * a.S * a.Hkv;                       // one per list entry and KV head
+    if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)ctas, (unsigned)a.Hkv, (unsigned)a.S);
+    cfg.gridDim = dim3((unsigned)ctas);
     cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = st;
@@ -514,17 +528,12 @@ cudaError_t launch_chunk_umma_t(const ChunkArgs &a, const CUtensorMap &tmk, cons
     return cudaLaunchKernelEx(&cfg, chunk_umma_kernel<T, D, B, MT>, a, tmk, tmv);
 }
 
-// Two tiles per CTA once a sequence can fill them (256 rows per KV head).
-#ifndef PA_CHUNK_UMMA_PAIR_ROWS
-#define PA_CHUNK_UMMA_PAIR_ROWS 256
-#endif
-
+// Two tiles per CTA once a sequence can fill them (chunk_umma_rows).
 template <typename T, int D, int B>
 cudaError_t dispatch_chunk_umma_mt(const ChunkArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                    cudaStream_t st) {
-    const long long rows = (long long)a.max_query_len * (a.Hq / a.Hkv);
-    return rows >= PA_CHUNK_UMMA_PAIR_ROWS ? launch_chunk_umma_t<T, D, B, 2>(a, tmk, tmv, st)
-                                           : launch_chunk_umma_t<T, D, B, 1>(a, tmk, tmv, st);
+    return a.umma_rows == 256 ? launch_chunk_umma_t<T, D, B, 2>(a, tmk, tmv, st)
+                              : launch_chunk_umma_t<T, D, B, 1>(a, tmk, tmv, st);
 }
 
 template <typename T>

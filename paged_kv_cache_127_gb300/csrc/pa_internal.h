@@ -51,6 +51,7 @@ struct ChunkArgs {
     int S, T, Hq, Hkv, D, B, N, max_blocks, partition_size, max_parts, max_query_len;
     int head_group;                 // KV heads per work item
     int row_warps;                  // 16-row query tiles per KV head per work item (1 or 2)
+    int umma_rows;                  // tcgen05 path: query rows per CTA (128 or 256); 0 on the mma.sync path
     float scale;
 };
 
@@ -67,6 +68,19 @@ inline int chunk_row_warps(int max_query_len, int G) { return (long long)max_que
 inline bool chunk_uses_umma(int max_query_len, int G) {
     return (long long)max_query_len * G >= PA_CHUNK_UMMA_MIN_ROWS;
 }
+// Keys per step of the tcgen05 kernel, and its rows per CTA: two 128-row tiles
+// once a sequence can fill them.
+#ifndef PA_CHUNK_UMMA_KEYS
+#define PA_CHUNK_UMMA_KEYS 64
+#endif
+#ifndef PA_CHUNK_UMMA_PAIR_ROWS
+#define PA_CHUNK_UMMA_PAIR_ROWS 256
+#endif
+inline int chunk_umma_rows(int max_query_len, int G) {
+    return (long long)max_query_len * G >= PA_CHUNK_UMMA_PAIR_ROWS ? 256 : 128;
+}
+// Step-count bins of the tcgen05 work list (longer CTAs are binned together).
+constexpr int kUmmaStepBins = 1024;
 
 // KV heads that one tensor-core work item (one CTA) covers: PA_MMA_HEAD_GROUP
 // (4 by default) when they divide Hkv, else the largest power of two that does.
