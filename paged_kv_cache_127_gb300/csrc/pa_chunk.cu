@@ -42,8 +42,10 @@ __device__ __forceinline__ int umma_steps(int n, int len, int G, int rows_cta, i
 
 __global__ void __launch_bounds__(1024) chunk_plan_kernel(const ChunkArgs a) {
     constexpr int kBins = kUmmaStepBins > kMaxPartitionBlocks + 1 ? kUmmaStepBins : kMaxPartitionBlocks + 1;
+    constexpr int kQsCache = 4096;
     __shared__ int hist[kBins];
     __shared__ int start[kBins];
+    __shared__ int qs_cache[kQsCache];
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int tid = threadIdx.x;
@@ -69,20 +71,29 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const ChunkArgs a) {
         for (int i = tid; i < a.T; i += blockDim.x) a.tok_seq[i] = -1;
         return;
     }
-    // query row -> sequence: the last s with query_start[s] <= i, if i is inside its range
-    for (int i = tid; i < a.T; i += blockDim.x) {
-        int lo = 0, hi = a.S;  // invariant: query_start[lo] <= i (or lo == 0), answer in [lo, hi)
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (a.query_start[mid] <= i) lo = mid; else hi = mid;
+    // query row -> sequence (read by the split-K merge; the tcgen05 path has
+    // none): the last s with query_start[s] <= i, if i is inside its range.  The
+    // binary search runs over a shared-memory copy of query_start when it fits.
+    if (a.umma_rows == 0) {
+        const bool cached = a.S + 1 <= kQsCache;
+        if (cached)
+            for (int i = tid; i <= a.S; i += blockDim.x) qs_cache[i] = a.query_start[i];
+        __syncthreads();
+        const int *qsv = cached ? qs_cache : a.query_start;
+        for (int i = tid; i < a.T; i += blockDim.x) {
+            int lo = 0, hi = a.S;  // invariant: query_start[lo] <= i (or lo == 0), answer in [lo, hi)
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (qsv[mid] <= i) lo = mid; else hi = mid;
+            }
+            int s = -1;
+            if (a.S > 0 && qsv[lo] <= i && i < qsv[lo + 1]) {
+                const int n = qsv[lo + 1] - qsv[lo];
+                const int len = a.context_lens[lo];
+                if (len >= 0 && len <= cap && n <= len && n <= a.max_query_len) s = lo;
+            }
+            a.tok_seq[i] = s;
         }
-        int s = -1;
-        if (a.S > 0 && a.query_start[lo] <= i && i < a.query_start[lo + 1]) {
-            const int n = a.query_start[lo + 1] - a.query_start[lo];
-            const int len = a.context_lens[lo];
-            if (len >= 0 && len <= cap && n <= len && n <= a.max_query_len) s = lo;
-        }
-        a.tok_seq[i] = s;
     }
     if (a.umma_rows > 0) {
         // tcgen05 path: one entry per (sequence, tile group), by step count, longest first
