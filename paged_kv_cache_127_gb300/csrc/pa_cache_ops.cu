@@ -146,6 +146,7 @@ template <int D>
 __global__ void decode_merge_kernel(const DecodeArgs a) {
     constexpr int kPer = D / 32;
     constexpr int kU = 4;
+    constexpr int kFastParts = 8;  // rows with at most this many partitions merge in one round trip
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int gw = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
@@ -159,6 +160,43 @@ __global__ void decode_merge_kernel(const DecodeArgs a) {
     const size_t r0 = (size_t)gw * a.max_parts;
     const float *ml = a.ws_ml + 2 * r0;
     const float *acc = a.ws_acc + r0 * D;
+    if (np <= kFastParts) {
+        // one round trip: every lane loads all (m, l) pairs (broadcast) and its
+        // slice of every partial sum together, then combines them in registers
+        float2 w[kFastParts];
+        float x[kFastParts][kPer];
+#pragma unroll
+        for (int p = 0; p < kFastParts; ++p) {
+            if (p < np) {
+                w[p] = *reinterpret_cast<const float2 *>(ml + 2 * p);
+#pragma unroll
+                for (int i = 0; i < kPer; ++i) x[p][i] = acc[(size_t)p * D + lane * kPer + i];
+            }
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int p = 0; p < kFastParts; ++p)
+            if (p < np) M = fmaxf(M, w[p].x);
+        float L = 0.f, o[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) o[i] = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int p = 0; p < kFastParts; ++p) {
+                if (p < np) {
+                    const float wt = ex2(w[p].x - M);
+                    L += wt * w[p].y;
+#pragma unroll
+                    for (int i = 0; i < kPer; ++i) o[i] += wt * x[p][i];
+                }
+            }
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        float *dst = a.out + (size_t)gw * D + lane * kPer;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) dst[i] = o[i] * inv;
+        return;
+    }
     float M = -INFINITY;
     for (int p = lane; p < np; p += 32) M = fmaxf(M, ml[2 * p]);
 #pragma unroll
