@@ -20,12 +20,11 @@
 //
 // Every operation is O(1) amortised per block touched.  Not thread-safe.
 
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <deque>
 #include <new>
-#include <unordered_map>
-#include <unordered_set>
 #include <vector>
 
 #include "../../include/pa.h"
@@ -96,6 +95,7 @@ pa_pool *pa_pool_create(int32_t num_blocks, int32_t block_size, const int32_t *f
     p->num_blocks = num_blocks;
     p->B = block_size;
     p->ref.assign(num_blocks, 0);
+    p->given_up.assign(num_blocks, 0);
     if (free_order) {
         std::vector<char> seen(num_blocks, 0);
         for (int32_t i = 0; i < num_blocks; ++i) {
@@ -152,27 +152,36 @@ int32_t pa_seq_append_batch(pa_pool *pool, const int32_t *seqs, int32_t n, int32
     if (!pool || n < 0 || tokens_each < 0 || !n_cow || (n > 0 && (!seqs || !cow_pairs_out)) ||
         (n > 0 && tokens_each > 0 && !slots_out))
         return PA_ERR_INVALID;
-    std::unordered_set<int32_t> seen;
+    // each sequence at most once: mark it with this call's epoch
+    if (++pool->batch_epoch == 0) {  // the counter wrapped: forget every old mark
+        for (auto &rec : pool->seqs) rec.batch_mark = 0;
+        pool->batch_epoch = 1;
+    }
+    const uint32_t epoch = pool->batch_epoch;
     for (int32_t i = 0; i < n; ++i) {
         if (!valid_seq(pool, seqs[i])) return PA_ERR_BAD_INDEX;
-        if (!seen.insert(seqs[i]).second) return PA_ERR_INVALID;
+        pa_seq_rec &s = pool->seqs[seqs[i]];
+        if (s.batch_mark == epoch) return PA_ERR_INVALID;
+        s.batch_mark = epoch;
     }
     // Dry run: copies made earlier in the batch lower the count of the block
     // they left, which can spare a later sharer its own copy.
-    std::unordered_map<int32_t, int32_t> given_up;
     int64_t need = 0;
     for (int32_t i = 0; i < n; ++i) {
         const pa_seq_rec &s = pool->seqs[seqs[i]];
         int32_t ref_last = 0;
         if (!s.table.empty()) {
-            int32_t last = s.table.back();
-            auto it = given_up.find(last);
-            ref_last = pool->ref[last] - (it == given_up.end() ? 0 : it->second);
+            const int32_t last = s.table.back();
+            ref_last = pool->ref[last] - pool->given_up[last];
         }
-        int64_t k = need_for(pool, s, tokens_each, ref_last);
-        need += k;
-        if (tokens_each > 0 && s.len % pool->B != 0 && ref_last > 1) ++given_up[s.table.back()];
+        need += need_for(pool, s, tokens_each, ref_last);
+        if (tokens_each > 0 && s.len % pool->B != 0 && ref_last > 1) {
+            const int32_t last = s.table.back();
+            if (pool->given_up[last]++ == 0) pool->touched.push_back(last);
+        }
     }
+    for (int32_t b : pool->touched) pool->given_up[b] = 0;
+    pool->touched.clear();
     if (need > available(pool)) return PA_ERR_OOM;
     int32_t pairs = 0;
     for (int32_t i = 0; i < n; ++i) {
@@ -224,9 +233,9 @@ int32_t pa_pool_export(const pa_pool *pool, const int32_t *seqs, int32_t n, int3
     for (int32_t i = 0; i < n; ++i) {
         const auto &s = pool->seqs[seqs[i]];
         int32_t *row = tables_out + (int64_t)i * max_blocks;
-        int32_t k = 0;
-        for (; k < (int32_t)s.table.size(); ++k) row[k] = s.table[k];
-        for (; k < max_blocks; ++k) row[k] = pad;
+        const size_t k = s.table.size();
+        if (k) std::memcpy(row, s.table.data(), k * sizeof(int32_t));
+        std::fill(row + k, row + max_blocks, pad);
         lens_out[i] = (int32_t)s.len;
     }
     return PA_OK;

@@ -12,6 +12,7 @@ struct pa_seq_rec {
     std::vector<int32_t> table;
     int64_t len = 0;
     bool live = false;
+    uint32_t batch_mark = 0;  // batch calls: the call that last listed this sequence
 };
 
 struct pa_pool {
@@ -23,6 +24,10 @@ struct pa_pool {
     int32_t live = 0;
     int64_t cow_copies = 0;
     int64_t fail_budget = -1;  // < 0: unlimited
+    // scratch of pa_seq_append_batch, kept between calls so a call allocates nothing
+    uint32_t batch_epoch = 0;
+    std::vector<int32_t> given_up;   // per block: copies made earlier in the batch (zero outside a call)
+    std::vector<int32_t> touched;    // blocks whose given_up count is nonzero
 };
 
 
