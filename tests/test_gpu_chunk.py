@@ -179,3 +179,36 @@ def test_chunk_full_size_workloads_on_sampled_sequences(gpu, name, k):
                                          np.array([cut], np.int32), np.array([0, b0 - a0], np.int32),
                                          st.scale, st.dtype)
             assert_attention_close(got[s * n + a0:s * n + b0], ref)
+
+
+@pytest.mark.parametrize("path,nq", [("mma", 6), ("umma", 40)])
+def test_chunk_bad_block_entry_is_flagged_and_skipped(gpu, path, nq):
+    # a table entry outside the pool inside the context: its keys are skipped
+    # (every query attends to the remaining keys), PA_DEVERR_BAD_BLOCK is raised
+    # and the other sequence is untouched
+    from scipy.special import softmax
+    from paged_helpers import widen
+    torch, pa = gpu
+    rng = synth.make_rng(3500 + nq)
+    B, Hq, Hkv, D = 16, 16, 4, 128
+    q, kc, vc, tables, lens, qs = chunk_case(rng, "bf16", Hq, Hkv, D, B, [300, 300], [nq, nq])
+    bad = tables.copy()
+    bad[1, 10] = kc.shape[0] + 7                        # block 10 of sequence 1: tokens 160..175
+    got = run_chunk(torch, pa, "bf16", q, kc, vc, bad, lens, qs, 0.1)
+    assert pa.pa_device_errors(clear=True) & pa.PA_DEVERR_BAD_BLOCK
+    ref = oracle.chunk_attention(q, kc, vc, tables, lens, qs, 0.1, "bf16")
+    assert_attention_close(got[:nq], ref[:nq])          # sequence 0 is untouched
+    # sequence 1: unpaged attention with tokens 160..175 removed
+    K = widen(np.stack([kc[tables[1, t // B], :, t % B] for t in range(300)]), "bf16")
+    V = widen(np.stack([vc[tables[1, t // B], :, t % B] for t in range(300)]), "bf16")
+    q64 = widen(q[nq:], "bf16")
+    keep = np.ones(300, bool)
+    keep[160:176] = False
+    want = np.zeros((nq, Hq, D))
+    G = Hq // Hkv
+    for t in range(nq):
+        vis = keep & (np.arange(300) <= 300 - nq + t)
+        for h in range(Hq):
+            w = softmax(0.1 * (K[vis, h // G] @ q64[t, h]))
+            want[t, h] = w @ V[vis, h // G]
+    assert_attention_close(got[nq:], want)
