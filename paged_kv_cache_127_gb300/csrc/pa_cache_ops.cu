@@ -146,7 +146,10 @@ template <int D>
 __global__ void decode_merge_kernel(const DecodeArgs a) {
     constexpr int kPer = D / 32;
     constexpr int kU = 4;
-    constexpr int kFastParts = 8;  // rows with at most this many partitions merge in one round trip
+#ifndef PA_MERGE_FAST_PARTS
+#define PA_MERGE_FAST_PARTS 8
+#endif
+    constexpr int kFastParts = PA_MERGE_FAST_PARTS;  // rows with at most this many partitions merge in one round trip
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int gw = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
@@ -160,11 +163,11 @@ __global__ void decode_merge_kernel(const DecodeArgs a) {
     const size_t r0 = (size_t)gw * a.max_parts;
     const float *ml = a.ws_ml + 2 * r0;
     const float *acc = a.ws_acc + r0 * D;
-    if (np <= kFastParts) {
+    if (kFastParts > 0 && np <= kFastParts) {
         // one round trip: every lane loads all (m, l) pairs (broadcast) and its
         // slice of every partial sum together, then combines them in registers
-        float2 w[kFastParts];
-        float x[kFastParts][kPer];
+        float2 w[kFastParts > 0 ? kFastParts : 1];
+        float x[kFastParts > 0 ? kFastParts : 1][kPer];
 #pragma unroll
         for (int p = 0; p < kFastParts; ++p) {
             if (p < np) {
