@@ -238,24 +238,27 @@ def run_ours(args):
     for name, arr in parts:
         b = as_bytes(arr)
         h_in[offs[name]:offs[name] + b.size] = torch.from_numpy(b)
-    d_in = h_in.to(device)
-
-    def view(name, arr, tdtype, shape):
-        n = np.ascontiguousarray(arr).nbytes
-        return d_in[offs[name]:offs[name] + n].view(tdtype).view(shape)
-
+    # two device mirrors of the inputs and two outputs: the end-to-end leg
+    # double-buffers them so a step's copies overlap its neighbours' compute
+    d_ins = [h_in.to(device), h_in.to(device)]
     kvt = torch.bfloat16 if step.dtype == "bf16" else (torch.float16 if step.dtype == "f16" else torch.float32)
-    d_q = view("q", step.q, kvt, step.q.shape)
-    d_k = view("k", step.k_new, kvt, step.k_new.shape)
-    d_v = view("v", step.v_new, kvt, step.v_new.shape)
-    d_slots = view("slots", step.slots, torch.int64, step.slots.shape)
-    d_tables = view("tables", step.tables, torch.int32, step.tables.shape)
-    d_lens = view("lens", step.lens, torch.int32, step.lens.shape)
-    d_pairs = view("pairs", step.pairs, torch.int64, step.pairs.shape)
-    h_out = torch.empty((S, Hq, D), dtype=torch.float32).pin_memory()
 
+    def views(d_in):
+        def view(name, arr, tdtype, shape):
+            n = np.ascontiguousarray(arr).nbytes
+            return d_in[offs[name]:offs[name] + n].view(tdtype).view(shape)
+        return {"q": view("q", step.q, kvt, step.q.shape), "k": view("k", step.k_new, kvt, step.k_new.shape),
+                "v": view("v", step.v_new, kvt, step.v_new.shape),
+                "slots": view("slots", step.slots, torch.int64, step.slots.shape),
+                "tables": view("tables", step.tables, torch.int32, step.tables.shape),
+                "lens": view("lens", step.lens, torch.int32, step.lens.shape),
+                "pairs": view("pairs", step.pairs, torch.int64, step.pairs.shape)}
+
+    bufs = [views(d) for d in d_ins]
+    h_outs = [torch.empty((S, Hq, D), dtype=torch.float32).pin_memory() for _ in range(2)]
     d_kc, d_vc = bf(step.k_cache).to(device), bf(step.v_cache).to(device)
-    d_out = torch.empty((S, Hq, D), dtype=torch.float32, device=device)
+    d_outs = [torch.empty((S, Hq, D), dtype=torch.float32, device=device) for _ in range(2)]
+    d_out = d_outs[0]
     ws_bytes = pa.pa_decode_workspace_bytes(dims)
     d_ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
@@ -271,17 +274,19 @@ def run_ours(args):
 
     dec_ev = []
 
-    def device_step(record=False):
+    def device_step(record=False, b=0, st=None):
+        st = stream if st is None else st
+        v = bufs[b]
         if npairs:
-            pa.pa_copy_blocks(dims, d_kc, d_vc, d_pairs, stream)
-        pa.pa_write_kv(dims, d_k, d_v, d_slots, d_kc, d_vc, stream)
+            pa.pa_copy_blocks(dims, d_kc, d_vc, v["pairs"], st)
+        pa.pa_write_kv(dims, v["k"], v["v"], v["slots"], d_kc, d_vc, st)
         if record:
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-        pa.pa_decode(dims, d_q, d_kc, d_vc, d_tables, d_lens, step.scale, d_out, d_ws, stream)
+            e0.record(st)
+        pa.pa_decode(dims, v["q"], d_kc, d_vc, v["tables"], v["lens"], step.scale, d_outs[b], d_ws, st)
         if record:
-            e1.record(stream)
+            e1.record(st)
             dec_ev.append((e0, e1))
 
     pa.pa_device_errors(clear=True)
@@ -297,8 +302,11 @@ def run_ours(args):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for _ in range(args.steps):
-        device_step(record=True)
+    # the decode call is bracketed by CUDA events on every 8th step (an event pair
+    # on every step would cost the step ~2 % by breaking the overlap of the
+    # programmatically dependent launches)
+    for i in range(args.steps):
+        device_step(record=(i % 8 == 0))
     t1.record(stream)
     torch.cuda.synchronize(device)
     barrier(dist, device)
@@ -306,20 +314,43 @@ def run_ours(args):
     dec_ms = float(np.mean([a.elapsed_time(b) for a, b in dec_ev]))
     ms_total = reduce_scalar(dist, ms_local, "max", device)
 
-    # ---- end to end through the binding with host buffers
+    # ---- end to end through the binding with host buffers.  Every step copies
+    # all of its inputs host -> device (one packed copy) and its output device ->
+    # host; steps are double-buffered over three streams, so step i's copies
+    # overlap the compute of steps i - 1 and i + 1, and the host collects step
+    # i - 1's result before enqueueing step i + 1.
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
-    for _ in range(3):
-        d_in.copy_(h_in, non_blocking=True)
-        device_step()
-        h_out.copy_(d_out, non_blocking=True)
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_cmp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def e2e_loop(n):
+        for i in range(n):
+            b = i & 1
+            if i >= 2:
+                s_in.wait_event(ev_cmp[b])      # step i - 2 has read input buffer b
+            with torch.cuda.stream(s_in):
+                d_ins[b].copy_(h_in, non_blocking=True)
+            ev_in[b].record(s_in)
+            stream.wait_event(ev_in[b])
+            if i >= 2:
+                stream.wait_event(ev_out[b])    # step i - 2's output has reached the host
+            device_step(b=b)
+            ev_cmp[b].record(stream)
+            s_out.wait_event(ev_cmp[b])
+            with torch.cuda.stream(s_out):
+                h_outs[b].copy_(d_outs[b], non_blocking=True)
+            ev_out[b].record(s_out)
+            if i >= 1:
+                ev_out[b ^ 1].synchronize()     # the host has step i - 1's result
+        torch.cuda.synchronize(device)
+
+    e2e_loop(3)
     barrier(dist, device)
     torch.cuda.synchronize(device)
     w0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        d_in.copy_(h_in, non_blocking=True)  # all of the step's inputs, one copy
-        device_step()
-        h_out.copy_(d_out, non_blocking=True)
-        stream.synchronize()
+    e2e_loop(e2e_steps)
     e2e_s = time.perf_counter() - w0
     barrier(dist, device)
     e2e_s = reduce_scalar(dist, e2e_s, "max", device)
@@ -332,7 +363,7 @@ def run_ours(args):
     seqs_all = reduce_scalar(dist, S, "sum", device)
     step_s = ms_total / 1e3 / args.steps
     h2d = h_in.numel()
-    d2h = h_out.numel() * h_out.element_size()
+    d2h = h_outs[0].numel() * h_outs[0].element_size()
 
     if rank != 0:
         return None
@@ -459,8 +490,11 @@ def run_chunk(args):
     barrier(dist, device)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for _ in range(args.steps):
-        device_step(record=True)
+    # the decode call is bracketed by CUDA events on every 8th step (an event pair
+    # on every step would cost the step ~2 % by breaking the overlap of the
+    # programmatically dependent launches)
+    for i in range(args.steps):
+        device_step(record=(i % 8 == 0))
     t1.record(stream)
     torch.cuda.synchronize(device)
     barrier(dist, device)
