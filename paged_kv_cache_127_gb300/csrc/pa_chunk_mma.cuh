@@ -146,8 +146,9 @@ __global__ void __launch_bounds__(ChunkCfg<D, HG, RW>::kThreads, ChunkCfg<D, HG,
     const int tile_of = warp / HG;   // row tile within the item's row block
 
     // ------------------------------------------------------------ producer (warp 0)
-    int ticket = 0;
-    if (warp == 0 && lane == 0) ticket = atomicAdd(a.plan_hdr + 1, 1);
+    // First item: list entry blockIdx.x; later ones are claimed from the counter
+    // when the issue cursor reaches them, not earlier, so each CTA's last item is
+    // taken as late as possible and the largest-first order bounds the tail.
     int p_item = 0;
     int p_chunk = 0;
     int p_claimed = 0;
@@ -158,8 +159,9 @@ __global__ void __launch_bounds__(ChunkCfg<D, HG, RW>::kThreads, ChunkCfg<D, HG,
         const int slot = seq % C::kSlots;
         if (seq >= C::kSlots)
             mbar_wait_bounded(iempty0 + 8 * slot, (uint32_t)((seq / C::kSlots) - 1) & 1u, kWaitLimit);
-        const int idx = __shfl_sync(0xffffffffu, ticket, 0);
-        if (lane == 0) ticket = atomicAdd(a.plan_hdr + 1, 1);
+        int idx = 0;
+        if (lane == 0) idx = seq == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(a.plan_hdr + 1, 1);
+        idx = __shfl_sync(0xffffffffu, idx, 0);
         int4 e0 = make_int4(0, 0, 0, 0), e1 = make_int4(0, 0, 0, 0), e2 = make_int4(0, 0, 0, 0);
         if (idx < n_items) {
             const int4 e = a.plan_list[idx / ngroups];

@@ -144,11 +144,13 @@ __global__ void __launch_bounds__(MmaCfg<D, HG>::kThreads, 2)
     const uint64_t pol = policy_evict_first();
 
     // ------------------------------------------------------------ producer (warp 0)
-    // Warp 0 claims work items (one ticket ahead, hiding the atomic), fills the
-    // item slots, and lane 0 issues the TMA loads, running up to kStages chunks
-    // ahead of warp 0's own consumption and across item boundaries.
-    int ticket = 0;
-    if (warp == 0 && lane == 0) ticket = atomicAdd(a.plan_hdr + 1, 1);
+    // Warp 0 claims work items, fills the item slots, and lane 0 issues the TMA
+    // loads, running up to kStages chunks ahead of warp 0's own consumption and
+    // across item boundaries.  A CTA's first item is list entry blockIdx.x; every
+    // later one is claimed from the counter only when the issue cursor reaches
+    // it (a few chunks before it is consumed, which hides the atomic).  Claiming
+    // any earlier would fix each CTA's last item while the list still holds
+    // bigger ones, and the largest-first order would no longer bound the tail.
     int p_item = 0;    // item sequence number the issue cursor is in
     int p_chunk = 0;   // next chunk of it
     int p_claimed = 0; // items claimed (slots filled) so far
@@ -159,8 +161,9 @@ __global__ void __launch_bounds__(MmaCfg<D, HG>::kThreads, 2)
         const int slot = seq % C::kSlots;
         if (seq >= C::kSlots)  // all warps must be done with the item that used this slot
             mbar_wait_bounded(iempty0 + 8 * slot, (uint32_t)((seq / C::kSlots) - 1) & 1u, kWaitLimit);
-        const int idx = __shfl_sync(0xffffffffu, ticket, 0);
-        if (lane == 0) ticket = atomicAdd(a.plan_hdr + 1, 1);
+        int idx = 0;
+        if (lane == 0) idx = seq == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(a.plan_hdr + 1, 1);
+        idx = __shfl_sync(0xffffffffu, idx, 0);
         int4 e0 = make_int4(0, 0, 0, 0), e1 = make_int4(0, 0, 0, 0);
         if (idx < n_items) {
             const int4 e = a.plan_list[idx / ngroups];
