@@ -16,12 +16,12 @@
 // Work: an item is (sequence, context partition, group of HG KV heads, row
 // block).  For one KV head the query rows are the (query token, query head of
 // the group) pairs r = t * G + gq, cut into 16-row tiles; a row block is RW
-// tiles.  A CTA has HG x RW warps: warp w takes KV head g0 + w % HG and tile
-// w / HG of the block.  The producer is the decode kernel's: warp 0 claims
-// items from the plan's list and lane 0 streams 16-token chunks of the HG heads
-// into a shared-memory ring with 3-D TMA copies; here all HG x RW warps consume
-// each stage, so a partition's K/V is read once per row block, not once per
-// query.
+// tiles.  A CTA has HG x RW consumer warps: warp w takes KV head g0 + w % HG
+// and tile w / HG of the block.  The producer is the decode kernel's: one more
+// warp claims items from the plan's list and streams 16-token chunks of the HG
+// heads into a shared-memory ring with 3-D TMA copies; here all HG x RW
+// consumer warps read each stage, so a partition's K/V is read once per row
+// block, not once per query.
 //
 // Per chunk and warp:
 //   S = Q K^T    mma.m16n8k16, A = the tile's 16 query rows (rows g and g + 8
@@ -67,8 +67,8 @@ struct ChunkCfg {
     static constexpr int kBoxBytes = HG * kHeadSub;      // one TMA box: that, for HG heads
     static constexpr int kTileBytes = kSub * kBoxBytes;  // K (or V) of a chunk, all HG heads
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kWarps = HG * RW;
-    static constexpr int kThreads = kWarps * 32;
+    static constexpr int kConsumers = HG * RW;              // warp w < HG * RW: head w % HG, row tile w / HG
+    static constexpr int kThreads = (kConsumers + 1) * 32;  // + one producer warp
     static constexpr int kMinBlocks = RW == 1 ? 2 : 1;
     static constexpr int kStagesRaw = PA_CHUNK_STAGE_BUDGET / kMinBlocks / kStageBytes;
     static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
@@ -118,11 +118,11 @@ __global__ void __launch_bounds__(ChunkCfg<D, HG, RW>::kThreads, ChunkCfg<D, HG,
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kStages; ++i) {
             mbar_init(full0 + 8 * i, 1);
-            mbar_init(empty0 + 8 * i, C::kWarps);
+            mbar_init(empty0 + 8 * i, C::kConsumers);
         }
         for (int i = 0; i < C::kSlots; ++i) {
             mbar_init(ifull0 + 8 * i, 1);
-            mbar_init(iempty0 + 8 * i, C::kWarps);
+            mbar_init(iempty0 + 8 * i, C::kConsumers);
         }
         fence_mbar_init();
         prefetch_tmap(&tmk);
@@ -141,110 +141,106 @@ __global__ void __launch_bounds__(ChunkCfg<D, HG, RW>::kThreads, ChunkCfg<D, HG,
     const uint32_t kx = (uint32_t)(lm ^ lr);          // swizzled chunk bits for K reads
     const uint32_t vx = (uint32_t)((lm >> 1) ^ lr);   // and for V reads
     const float sl = a.scale * 1.4426950408889634f;   // logits in log2 units
-    const uint64_t pol = policy_evict_first();
     const int head = warp % HG;      // KV head of the item's group
     const int tile_of = warp / HG;   // row tile within the item's row block
 
-    // ------------------------------------------------------------ producer (warp 0)
-    // First item: list entry blockIdx.x; later ones are claimed from the counter
-    // when the issue cursor reaches them, not earlier, so each CTA's last item is
-    // taken as late as possible and the largest-first order bounds the tail.
-    int p_item = 0;
-    int p_chunk = 0;
-    int p_claimed = 0;
-    int iss = 0;
-    bool p_done = false;
-
-    auto claim_into_slot = [&](int seq) {  // warp 0, uniform
-        const int slot = seq % C::kSlots;
-        if (seq >= C::kSlots)
-            mbar_wait_bounded(iempty0 + 8 * slot, (uint32_t)((seq / C::kSlots) - 1) & 1u, kWaitLimit);
-        int idx = 0;
-        if (lane == 0) idx = seq == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(a.plan_hdr + 1, 1);
-        idx = __shfl_sync(0xffffffffu, idx, 0);
-        int4 e0 = make_int4(0, 0, 0, 0), e1 = make_int4(0, 0, 0, 0), e2 = make_int4(0, 0, 0, 0);
-        if (idx < n_items) {
-            const int4 e = a.plan_list[idx / ngroups];
-            e0 = e;
-            const int qs = a.query_start[e.x];
-            const int n = a.query_start[e.x + 1] - qs;
-            int len = a.context_lens[e.x];
-            len = len < 0 ? 0 : (len > cap ? cap : len);
-            e1 = make_int4((idx % ngroups) * HG, (e.z + 15) >> 4, 1, qs);
-            e2 = make_int4(n, len, 0, 0);
-            const int nblk = (e.z + B - 1) / B;
-            const int32_t *row = a.block_tables + (size_t)e.x * a.max_blocks + (size_t)e.y * (Pt / B);
-            int32_t *tb = tbl + slot * C::kTblCap;
-            for (int i = lane; i < nblk; i += 32) {
-                int pb = row[i];
-                if (pb < 0 || pb >= a.N) {
-                    set_error(a.err, PA_DEVERR_BAD_BLOCK);
-                    pb = -1;
-                }
-                tb[i] = pb;
+    // ------------------------------------------------------------ producer warp
+    // The last warp claims items, fills the item slots and issues the TMA loads,
+    // up to kStages chunks ahead of the consumer warps and across item
+    // boundaries; it never consumes, so a claim overlaps the chunks already in
+    // the ring instead of stalling it.  First item: list entry blockIdx.x; later
+    // ones are claimed from the counter when the issue cursor reaches them, not
+    // earlier, so each CTA's last item is taken as late as possible and the
+    // largest-first order bounds the tail.
+    if (warp == C::kConsumers) {
+        const uint64_t pol = policy_evict_first();
+        int iss = 0;  // chunks issued
+        bool ok = true;
+        for (int seq = 0; ok; ++seq) {
+            const int slot = seq % C::kSlots;
+            // every consumer warp must be done with the item that used this slot
+            if (seq >= C::kSlots &&
+                !mbar_wait_bounded(iempty0 + 8 * slot, (uint32_t)((seq / C::kSlots) - 1) & 1u, kWaitLimit)) {
+                if (lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
+                break;
             }
-        }
-        if (lane == 0) {
-            info[3 * slot] = e0;
-            info[3 * slot + 1] = e1;
-            info[3 * slot + 2] = e2;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(ifull0 + 8 * slot);  // release: info and table visible
-        p_claimed = seq + 1;
-        return idx < n_items;
-    };
-
-    int cons = 0;  // chunks consumed by this warp
-    int seq = 0;   // item this warp is working on (the same item sequence in every warp)
-    auto top_up = [&]() {  // warp 0, uniform
-        while (!p_done && iss - cons < C::kStages) {
-            const int slot = p_item % C::kSlots;
-            if (p_item >= p_claimed) {
-                if (p_item >= seq + C::kSlots) break;
-                if (!claim_into_slot(p_item)) {
-                    p_done = true;
+            int idx = 0;
+            if (lane == 0) idx = seq == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(a.plan_hdr + 1, 1);
+            idx = __shfl_sync(0xffffffffu, idx, 0);
+            int4 e0 = make_int4(0, 0, 0, 0), e1 = make_int4(0, 0, 0, 0), e2 = make_int4(0, 0, 0, 0);
+            int32_t *tb = tbl + slot * C::kTblCap;
+            if (idx < n_items) {
+                const int4 e = a.plan_list[idx / ngroups];
+                e0 = e;
+                const int qs = a.query_start[e.x];
+                const int n = a.query_start[e.x + 1] - qs;
+                int len = a.context_lens[e.x];
+                len = len < 0 ? 0 : (len > cap ? cap : len);
+                e1 = make_int4((idx % ngroups) * HG, (e.z + 15) >> 4, 1, qs);
+                e2 = make_int4(n, len, 0, 0);
+                const int nblk = (e.z + B - 1) / B;
+                const int32_t *row = a.block_tables + (size_t)e.x * a.max_blocks + (size_t)e.y * (Pt / B);
+                for (int i = lane; i < nblk; i += 32) {
+                    int pb = row[i];
+                    if (pb < 0 || pb >= a.N) {
+                        set_error(a.err, PA_DEVERR_BAD_BLOCK);
+                        pb = -1;
+                    }
+                    tb[i] = pb;
+                }
+            }
+            if (lane == 0) {
+                info[3 * slot] = e0;
+                info[3 * slot + 1] = e1;
+                info[3 * slot + 2] = e2;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ifull0 + 8 * slot);  // release: info and table visible
+            if (idx >= n_items) break;
+            for (int c = 0; c < e1.y; ++c) {
+                const int st = iss % C::kStages;
+                // every consumer warp has released this stage's previous chunk
+                if (iss >= C::kStages &&
+                    !mbar_wait_bounded(empty0 + 8 * st, (uint32_t)((iss / C::kStages) - 1) & 1u, kWaitLimit)) {
+                    if (lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
+                    ok = false;
                     break;
                 }
-            }
-            const int4 e1 = info[3 * slot + 1];
-            if (p_chunk >= e1.y) {
-                ++p_item;
-                p_chunk = 0;
-                continue;
-            }
-            const int st = iss % C::kStages;
-            if (iss >= C::kStages)
-                mbar_wait_bounded(empty0 + 8 * st, (uint32_t)((iss / C::kStages) - 1) & 1u, kWaitLimit);
-            if (lane == 0) {
-                const uint32_t bar = full0 + 8 * st;
-                const int pb = tbl[slot * C::kTblCap + p_chunk / kCPB];
-                if (pb < 0) {
-                    mbar_arrive(bar);  // bad table entry: complete the phase without data
-                } else {
-                    const uint32_t dst = base + (uint32_t)(st * C::kStageBytes);
-                    const int y = (p_chunk % kCPB) * kChunkRows;
-                    const int z = pb * a.Hkv + e1.x;
-                    mbar_arrive_expect_tx(bar, C::kStageBytes);
+                if (lane == 0) {
+                    const uint32_t bar = full0 + 8 * st;
+                    const int pb = tb[c / kCPB];
+                    if (pb < 0) {
+                        mbar_arrive(bar);  // bad table entry: complete the phase without data
+                    } else {
+                        const uint32_t dst = base + (uint32_t)(st * C::kStageBytes);
+                        const int y = (c % kCPB) * kChunkRows;
+                        const int z = pb * a.Hkv + e1.x;
+                        mbar_arrive_expect_tx(bar, C::kStageBytes);
 #pragma unroll
-                    for (int sb = 0; sb < C::kSub; ++sb) {
-                        tma_load_3d(dst + sb * C::kBoxBytes, &tmk, sb * 64, y, z, bar, pol);
-                        tma_load_3d(dst + C::kTileBytes + sb * C::kBoxBytes, &tmv, sb * 64, y, z, bar, pol);
+                        for (int sb = 0; sb < C::kSub; ++sb) {
+                            tma_load_3d(dst + sb * C::kBoxBytes, &tmk, sb * 64, y, z, bar, pol);
+                            tma_load_3d(dst + C::kTileBytes + sb * C::kBoxBytes, &tmv, sb * 64, y, z, bar, pol);
+                        }
                     }
                 }
+                ++iss;
             }
-            ++iss;
-            ++p_chunk;
         }
-    };
+        // The CTA's shared memory outlives its copies: wait for the last
+        // kStages chunks issued (one pending phase per stage at most, so the
+        // parities are unambiguous); they have normally landed long ago.
+        for (int k = iss > C::kStages ? iss - C::kStages : 0; k < iss; ++k)
+            mbar_wait_bounded(full0 + 8 * (k % C::kStages), (uint32_t)(k / C::kStages) & 1u, kWaitLimit);
+        return;
+    }
 
-    // ------------------------------------------------------------ consumers (all warps)
+    // ------------------------------------------------------------ consumer warps
+    // Every consumer warp walks the same items (slot by slot) and chunks
+    // (stage by stage).
     uint32_t qa[C::kKS][4];
-    for (;; ++seq) {
+    int cons = 0;  // chunks consumed by this warp
+    for (int seq = 0;; ++seq) {
         const int slot = seq % C::kSlots;
-        if (warp == 0 && !p_done && seq >= p_claimed) {
-            if (!claim_into_slot(seq)) p_done = true;
-        }
         if (!mbar_wait_bounded(ifull0 + 8 * slot, (uint32_t)(seq / C::kSlots) & 1u, kWaitLimit)) {
             if (lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
             break;
@@ -289,7 +285,6 @@ __global__ void __launch_bounds__(ChunkCfg<D, HG, RW>::kThreads, ChunkCfg<D, HG,
         bool timed_out = false;
 
         for (int j = 0; j < nchunk; ++j) {
-            if (warp == 0) top_up();
             const int st = cons % C::kStages;
             const uint32_t parity = (uint32_t)(cons / C::kStages) & 1u;
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(full0 + 8 * st, parity, kWaitLimit))) {
@@ -452,12 +447,6 @@ __global__ void __launch_bounds__(ChunkCfg<D, HG, RW>::kThreads, ChunkCfg<D, HG,
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(iempty0 + 8 * slot);  // this warp is done with the item slot
-    }
-    // Drain: warp 0 waits for any copies it issued that were never consumed
-    // (only after a timeout) before the CTA's shared memory is released.
-    if (warp == 0) {
-        for (int k = cons; k < iss; ++k)
-            mbar_wait_bounded(full0 + 8 * (k % C::kStages), (uint32_t)(k / C::kStages) & 1u, kWaitLimit);
     }
 }
 

@@ -11,13 +11,13 @@
 //
 // Work: a work item is one (sequence, context partition, group of HG KV heads).
 // A small plan kernel lists the (sequence, partition) pairs, largest first, in
-// the workspace.  The kernel is persistent: each CTA claims items from a global
-// counter and gives warp w the item's KV head g0 + w.  Warp 0's lane 0 is also
-// the producer: it streams the item's 16-token chunks into a ring of
+// the workspace.  The kernel is persistent: in each CTA a producer warp claims
+// items from a global counter and streams their 16-token chunks into a ring of
 // shared-memory stages with TMA tensor copies (cp.async.bulk.tensor, 128-byte
 // swizzle) -- one 3-D box covers 16 rows of all HG heads, so a copy is 8 KB
-// rather than one head's 2 KB -- and runs ahead across item boundaries.  Full
-// barriers (transaction counts) signal data; empty barriers (one arrival per
+// rather than one head's 2 KB -- running ahead across item boundaries, and
+// consumer warp w computes the item's KV head g0 + w.  Full barriers
+// (transaction counts) signal data; empty barriers (one arrival per consumer
 // warp) return stages to the producer.
 //
 // Per 16-token chunk, with G = Hq / Hkv query heads sharing the KV head:
@@ -69,8 +69,8 @@ struct MmaCfg {
     static constexpr int kBoxBytes = HG * kHeadSub;      // one TMA box: that, for HG heads
     static constexpr int kTileBytes = kSub * kBoxBytes;  // K (or V) of a chunk, all HG heads
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kWarps = HG;
-    static constexpr int kThreads = kWarps * 32;
+    static constexpr int kConsumers = HG;                   // warp w < HG computes head g0 + w of an item
+    static constexpr int kThreads = (kConsumers + 1) * 32;  // + one producer warp
     static constexpr int kStagesRaw = PA_MMA_STAGE_BUDGET / kStageBytes;
     static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
     static constexpr int kSlots = 3;                     // work items in flight per CTA
@@ -103,7 +103,6 @@ __global__ void __launch_bounds__(MmaCfg<D, HG>::kThreads, 2)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int G = a.Hq / a.Hkv;
-    const int Pt = a.partition_size;
     const int ngroups = a.Hkv / HG;
 
     const uint32_t full0 = base + (uint32_t)C::kFullOff;
@@ -116,11 +115,11 @@ __global__ void __launch_bounds__(MmaCfg<D, HG>::kThreads, 2)
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kStages; ++i) {
             mbar_init(full0 + 8 * i, 1);
-            mbar_init(empty0 + 8 * i, C::kWarps);
+            mbar_init(empty0 + 8 * i, C::kConsumers);
         }
         for (int i = 0; i < C::kSlots; ++i) {
             mbar_init(ifull0 + 8 * i, 1);
-            mbar_init(iempty0 + 8 * i, C::kWarps);
+            mbar_init(iempty0 + 8 * i, C::kConsumers);
         }
         fence_mbar_init();
         prefetch_tmap(&tmk);
@@ -141,110 +140,109 @@ __global__ void __launch_bounds__(MmaCfg<D, HG>::kThreads, 2)
     const uint32_t kx = (uint32_t)(lm ^ lr);          // swizzled chunk bits for K reads
     const uint32_t vx = (uint32_t)((lm >> 1) ^ lr);   // and for V reads
     const float sl = a.scale * 1.4426950408889634f;   // logits in log2 units
-    const uint64_t pol = policy_evict_first();
 
-    // ------------------------------------------------------------ producer (warp 0)
-    // Warp 0 claims work items, fills the item slots, and lane 0 issues the TMA
-    // loads, running up to kStages chunks ahead of warp 0's own consumption and
-    // across item boundaries.  A CTA's first item is list entry blockIdx.x; every
-    // later one is claimed from the counter only when the issue cursor reaches
-    // it (a few chunks before it is consumed, which hides the atomic).  Claiming
-    // any earlier would fix each CTA's last item while the list still holds
-    // bigger ones, and the largest-first order would no longer bound the tail.
-    int p_item = 0;    // item sequence number the issue cursor is in
-    int p_chunk = 0;   // next chunk of it
-    int p_claimed = 0; // items claimed (slots filled) so far
-    int iss = 0;       // chunks issued
-    bool p_done = false;
-
-    auto claim_into_slot = [&](int seq) {  // warp 0, uniform
-        const int slot = seq % C::kSlots;
-        if (seq >= C::kSlots)  // all warps must be done with the item that used this slot
-            mbar_wait_bounded(iempty0 + 8 * slot, (uint32_t)((seq / C::kSlots) - 1) & 1u, kWaitLimit);
-        int idx = 0;
-        if (lane == 0) idx = seq == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(a.plan_hdr + 1, 1);
-        idx = __shfl_sync(0xffffffffu, idx, 0);
-        int4 e0 = make_int4(0, 0, 0, 0), e1 = make_int4(0, 0, 0, 0);
-        if (idx < n_items) {
-            const int4 e = a.plan_list[idx / ngroups];
-            e0 = e;
-            const int nchunk = (e.z + 15) >> 4;
-            e1 = make_int4((idx % ngroups) * HG, nchunk, 1, 0);
-            const int nblk = (e.z + B - 1) / B;
-            const int32_t *row = a.block_tables + (size_t)e.x * a.max_blocks + (size_t)e.y * (Pt / B);
-            int32_t *tb = tbl + slot * C::kTblCap;
-            for (int i = lane; i < nblk; i += 32) {
-                int pb = row[i];
-                if (pb < 0 || pb >= a.N) {
-                    set_error(a.err, PA_DEVERR_BAD_BLOCK);
-                    pb = -1;
-                }
-                tb[i] = pb;
+    // ------------------------------------------------------------ producer warp
+    // The last warp claims work items, fills the item slots, and issues the TMA
+    // loads, up to kStages chunks ahead of the consumer warps and across item
+    // boundaries; it never consumes, so a claim (an atomic, the list entry and
+    // the item's table slice) overlaps the chunks already in the ring instead
+    // of stalling it.  A CTA's first item is list entry blockIdx.x; every later
+    // one is claimed from the counter only when the issue cursor reaches it (a
+    // few chunks before it is consumed).  Claiming any earlier would fix each
+    // CTA's last item while the list still holds bigger ones, and the
+    // largest-first order would no longer bound the tail.
+    if (warp == C::kConsumers) {
+        const uint64_t pol = policy_evict_first();
+        int iss = 0;  // chunks issued
+        bool ok = true;
+        for (int seq = 0; ok; ++seq) {
+            const int slot = seq % C::kSlots;
+            // every consumer warp must be done with the item that used this slot
+            if (seq >= C::kSlots &&
+                !mbar_wait_bounded(iempty0 + 8 * slot, (uint32_t)((seq / C::kSlots) - 1) & 1u, kWaitLimit)) {
+                if (lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
+                break;
             }
-        }
-        if (lane == 0) {
-            info[2 * slot] = e0;
-            info[2 * slot + 1] = e1;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(ifull0 + 8 * slot);  // release: info and table visible
-        p_claimed = seq + 1;
-        return idx < n_items;
-    };
-
-    int cons = 0;  // chunks consumed by this warp
-    int seq = 0;   // item this warp is working on (same sequence of items in every warp)
-    // Issue chunks while fewer than kStages are ahead of warp 0's consumption.
-    // The cursor never enters an item whose slot is still held by warp 0's
-    // current item (claiming it would wait on warp 0 itself).
-    auto top_up = [&]() {  // warp 0, uniform
-        while (!p_done && iss - cons < C::kStages) {
-            const int slot = p_item % C::kSlots;
-            if (p_item >= p_claimed) {
-                if (p_item >= seq + C::kSlots) break;
-                if (!claim_into_slot(p_item)) {
-                    p_done = true;
+            int idx = 0;
+            if (lane == 0) idx = seq == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(a.plan_hdr + 1, 1);
+            idx = __shfl_sync(0xffffffffu, idx, 0);
+            int4 e0 = make_int4(0, 0, 0, 0), e1 = make_int4(0, 0, 0, 0);
+            int32_t *tb = tbl + slot * C::kTblCap;
+            if (idx < n_items) {
+                const int4 e = a.plan_list[idx / ngroups];
+                e0 = e;
+                e1 = make_int4((idx % ngroups) * HG, (e.z + 15) >> 4, 1, 0);
+                const int nblk = (e.z + B - 1) / B;
+                const int32_t *row = a.block_tables + (size_t)e.x * a.max_blocks + (size_t)e.y * (a.partition_size / B);
+                for (int i = lane; i < nblk; i += 32) {
+                    int pb = row[i];
+                    if (pb < 0 || pb >= a.N) {
+                        set_error(a.err, PA_DEVERR_BAD_BLOCK);
+                        pb = -1;
+                    }
+                    tb[i] = pb;
+                }
+            }
+            if (lane == 0) {
+                info[2 * slot] = e0;
+                info[2 * slot + 1] = e1;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ifull0 + 8 * slot);  // release: info and table visible
+            if (idx >= n_items) break;
+            for (int c = 0; c < e1.y; ++c) {
+                const int st = iss % C::kStages;
+                // every consumer warp has released this stage's previous chunk
+                if (iss >= C::kStages &&
+                    !mbar_wait_bounded(empty0 + 8 * st, (uint32_t)((iss / C::kStages) - 1) & 1u, kWaitLimit)) {
+                    if (lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
+                    ok = false;
                     break;
                 }
-            }
-            const int4 e1 = info[2 * slot + 1];
-            if (p_chunk >= e1.y) {  // item exhausted: move on
-                ++p_item;
-                p_chunk = 0;
-                continue;
-            }
-            const int st = iss % C::kStages;
-            if (iss >= C::kStages)  // every warp has released this stage's previous chunk
-                mbar_wait_bounded(empty0 + 8 * st, (uint32_t)((iss / C::kStages) - 1) & 1u, kWaitLimit);
-            if (lane == 0) {
-                const uint32_t bar = full0 + 8 * st;
-                const int pb = tbl[slot * C::kTblCap + p_chunk / kCPB];
-                if (pb < 0) {
-                    mbar_arrive(bar);  // bad table entry: complete the phase without data
-                } else {
-                    const uint32_t dst = base + (uint32_t)(st * C::kStageBytes);
-                    const int y = (p_chunk % kCPB) * kChunkRows;
-                    const int z = pb * a.Hkv + e1.x;
-                    mbar_arrive_expect_tx(bar, C::kStageBytes);
+                if (lane == 0) {
+                    const uint32_t bar = full0 + 8 * st;
+                    const int pb = tb[c / kCPB];
+                    if (pb < 0) {
+                        mbar_arrive(bar);  // bad table entry: complete the phase without data
+                    } else {
+                        const uint32_t dst = base + (uint32_t)(st * C::kStageBytes);
+                        const int y = (c % kCPB) * kChunkRows;
+                        const int z = pb * a.Hkv + e1.x;
+                        mbar_arrive_expect_tx(bar, C::kStageBytes);
 #pragma unroll
-                    for (int sb = 0; sb < C::kSub; ++sb) {
-                        tma_load_3d(dst + sb * C::kBoxBytes, &tmk, sb * 64, y, z, bar, pol);
-                        tma_load_3d(dst + C::kTileBytes + sb * C::kBoxBytes, &tmv, sb * 64, y, z, bar, pol);
+                        for (int sb = 0; sb < C::kSub; ++sb) {
+                            tma_load_3d(dst + sb * C::kBoxBytes, &tmk, sb * 64, y, z, bar, pol);
+                            tma_load_3d(dst + C::kTileBytes + sb * C::kBoxBytes, &tmv, sb * 64, y, z, bar, pol);
+                        }
                     }
                 }
+                ++iss;
             }
-            ++iss;
-            ++p_chunk;
         }
-    };
+        // The CTA's shared memory outlives its copies: wait for the last
+        // kStages chunks issued (one pending phase per stage at most, so the
+        // parities are unambiguous); they have normally landed long ago.
+        for (int k = iss > C::kStages ? iss - C::kStages : 0; k < iss; ++k)
+            mbar_wait_bounded(full0 + 8 * (k % C::kStages), (uint32_t)(k / C::kStages) & 1u, kWaitLimit);
+        // This warp made every claim of the CTA.  The last CTA to get here
+        // resets the counters, so the plan's list can serve the next launch.
+        if (lane == 0) {
+            __threadfence();
+            if (atomicAdd(a.plan_hdr + 2, 1) == (int)gridDim.x - 1) {
+                a.plan_hdr[1] = 0;
+                a.plan_hdr[2] = 0;
+            }
+        }
+        return;
+    }
 
-    // ------------------------------------------------------------ consumers (all warps)
+    // ------------------------------------------------------------ consumer warps
+    // Every consumer warp walks the same sequence of items (slot by slot) and
+    // chunks (stage by stage); warp w computes the item's KV head g0 + w.
     uint32_t qa[C::kKS][2];
-    for (;; ++seq) {
+    int cons = 0;  // chunks consumed by this warp
+    for (int seq = 0;; ++seq) {
         const int slot = seq % C::kSlots;
-        if (warp == 0 && !p_done && seq >= p_claimed) {
-            if (!claim_into_slot(seq)) p_done = true;
-        }
         if (!mbar_wait_bounded(ifull0 + 8 * slot, (uint32_t)(seq / C::kSlots) & 1u, kWaitLimit)) {
             if (lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
             break;
@@ -272,7 +270,6 @@ __global__ void __launch_bounds__(MmaCfg<D, HG>::kThreads, 2)
         bool timed_out = false;
 
         for (int j = 0; j < nchunk; ++j) {
-            if (warp == 0) top_up();
             const int st = cons % C::kStages;
             const uint32_t parity = (uint32_t)(cons / C::kStages) & 1u;
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(full0 + 8 * st, parity, kWaitLimit))) {
@@ -404,26 +401,12 @@ __global__ void __launch_bounds__(MmaCfg<D, HG>::kThreads, 2)
         __syncwarp();
         if (lane == 0) mbar_arrive(iempty0 + 8 * slot);  // this warp is done with the item slot
     }
-    // Drain: warp 0 waits for any copies it issued that were never consumed
-    // (only after a timeout) before the CTA's shared memory is released.
-    if (warp == 0) {
-        for (int k = cons; k < iss; ++k)
-            mbar_wait_bounded(full0 + 8 * (k % C::kStages), (uint32_t)(k / C::kStages) & 1u, kWaitLimit);
-        // Warp 0's lane 0 made every claim of this CTA.  The last CTA to get
-        // here resets the counters, so the plan's list can serve the next launch.
-        if (lane == 0) {
-            __threadfence();
-            if (atomicAdd(a.plan_hdr + 2, 1) == (int)gridDim.x - 1) {
-                a.plan_hdr[1] = 0;
-                a.plan_hdr[2] = 0;
-            }
-        }
-    }
 }
 
+// Grid of the persistent kernel on the current device: SMs x resident CTAs
+// per SM (the shared-memory attribute is set on first use per device).
 template <typename T, int D, int B, int HG>
-cudaError_t launch_decode_mma_t(const DecodeArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
-                                cudaStream_t st) {
+cudaError_t decode_mma_grid(int *grid) {
     using C = MmaCfg<D, HG>;
     static bool configured[64] = {};
     static int grid_for[64] = {};
@@ -444,8 +427,19 @@ cudaError_t launch_decode_mma_t(const DecodeArgs &a, const CUtensorMap &tmk, con
         grid_for[dev] = sms * (per_sm > 0 ? per_sm : 1);
         configured[dev] = true;
     }
+    *grid = grid_for[dev];
+    return cudaSuccess;
+}
+
+template <typename T, int D, int B, int HG>
+cudaError_t launch_decode_mma_t(const DecodeArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                                cudaStream_t st) {
+    using C = MmaCfg<D, HG>;
+    int grid = 0;
+    cudaError_t e = decode_mma_grid<T, D, B, HG>(&grid);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid_for[dev]);
+    cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = st;
