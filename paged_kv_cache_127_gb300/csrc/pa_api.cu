@@ -124,7 +124,7 @@ int32_t check_chunk_dims(const pa_dims *d, int32_t T, int32_t max_q, int32_t *ma
 // Chunk workspace, each part 256-byte aligned:
 //   header    2 ints: work items, claim counter
 //   list      int4 [S * P * R]: (sequence, partition, tokens, row block)
-//   tok       int32 [T]: sequence of each query row
+//   tok       int32 [T]: partitions each query row sees (0: no sequence)
 //   acc, ml   float [T, Hq, P, D] and [T, Hq, P, 2]   (only if P > 1)
 struct ChunkLayout {
     size_t list, tok, acc, ml, total;
@@ -328,7 +328,7 @@ int32_t pa_chunk_attention(const pa_dims *dims, const void *q, const void *k_cac
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     a.plan_hdr = reinterpret_cast<int *>(ws);
     a.plan_list = reinterpret_cast<int4 *>(ws + L.list);
-    a.tok_seq = reinterpret_cast<int32_t *>(ws + L.tok);
+    a.row_parts = reinterpret_cast<int32_t *>(ws + L.tok);
     a.ws_acc = parts > 1 ? reinterpret_cast<float *>(ws + L.acc) : nullptr;
     a.ws_ml = parts > 1 ? reinterpret_cast<float *>(ws + L.ml) : nullptr;
     a.err = error_word();

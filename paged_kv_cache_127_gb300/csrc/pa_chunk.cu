@@ -2,8 +2,9 @@
 // tokens per sequence; the tensor-core partition kernel is in pa_chunk_mma.cuh).
 //
 // The plan (one CTA) checks that query_start is non-decreasing within [0, T],
-// maps every query row to its sequence (-1 where none, or where the sequence
-// is skipped because n_s > context length or n_s > max_query_len), and lists
+// records for every query row how many partitions it sees (0 where the row
+// has no sequence, or where the sequence is skipped because n_s > context
+// length or n_s > max_query_len), and lists
 // the work: on the mma.sync path every (sequence, partition, row block) whose
 // rows see at least one key of the partition, with the partition's token count
 // up to the block's last row position, largest first (a counting sort on the
@@ -42,10 +43,13 @@ __device__ __forceinline__ int umma_steps(int n, int len, int G, int rows_cta, i
 
 __global__ void __launch_bounds__(1024) chunk_plan_kernel(const ChunkArgs a) {
     constexpr int kBins = kUmmaStepBins > kMaxPartitionBlocks + 1 ? kUmmaStepBins : kMaxPartitionBlocks + 1;
-    constexpr int kQsCache = 4096;
+    static_assert(kBins <= 1024, "one bin per thread in the scan");
+    constexpr int kCache = 4096;
     __shared__ int hist[kBins];
     __shared__ int start[kBins];
-    __shared__ int qs_cache[kQsCache];
+    __shared__ int warp_sums[32];
+    __shared__ int qs_cache[kCache + 1];
+    __shared__ int len_cache[kCache];
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int tid = threadIdx.x;
@@ -55,53 +59,57 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const ChunkArgs a) {
     const int maxpb = Pt / B;
     const int G = a.Hq / a.Hkv;
     const int rpb = a.row_warps * 16;
-    for (int i = tid; i < kBins; i += blockDim.x) hist[i] = 0;
-    int my_bad = 0;
-    if (tid == 0) {
-        a.plan_hdr[1] = 0;
-        my_bad = (a.query_start[0] < 0 || a.query_start[a.S] > a.T) ? 1 : 0;
+    // query_start and context_lens are read once, into shared memory when they fit
+    const bool cached = a.S <= kCache;
+    if (cached) {
+        for (int i = tid; i <= a.S; i += blockDim.x) qs_cache[i] = a.query_start[i];
+        for (int i = tid; i < a.S; i += blockDim.x) len_cache[i] = a.context_lens[i];
     }
+    for (int i = tid; i < kBins; i += blockDim.x) hist[i] = 0;
+    if (tid == 0) a.plan_hdr[1] = 0;
+    __syncthreads();
+    const int *qsv = cached ? qs_cache : a.query_start;
+    const int *lenv = cached ? len_cache : a.context_lens;
+    int my_bad = 0;
+    if (tid == 0) my_bad = (qsv[0] < 0 || qsv[a.S] > a.T) ? 1 : 0;
     for (int s = tid; s < a.S; s += blockDim.x)
-        if (a.query_start[s] > a.query_start[s + 1]) my_bad = 1;
+        if (qsv[s] > qsv[s + 1]) my_bad = 1;
     if (__syncthreads_or(my_bad)) {
         if (tid == 0) {
             set_error(a.err, PA_DEVERR_BAD_LEN);
             a.plan_hdr[0] = 0;
         }
-        for (int i = tid; i < a.T; i += blockDim.x) a.tok_seq[i] = -1;
+        for (int i = tid; i < a.T; i += blockDim.x) a.row_parts[i] = 0;
         return;
     }
-    // query row -> sequence (read by the split-K merge; the tcgen05 path has
-    // none): the last s with query_start[s] <= i, if i is inside its range.  The
-    // binary search runs over a shared-memory copy of query_start when it fits.
+    // Partitions each query row sees (read by the split-K merge; the tcgen05
+    // path has none): 0 where the row has no sequence, else pos / Pt + 1 for
+    // the row's position pos.  The row's sequence is the last s with
+    // query_start[s] <= i, if i is inside its range (a binary search).
     if (a.umma_rows == 0) {
-        const bool cached = a.S + 1 <= kQsCache;
-        if (cached)
-            for (int i = tid; i <= a.S; i += blockDim.x) qs_cache[i] = a.query_start[i];
-        __syncthreads();
-        const int *qsv = cached ? qs_cache : a.query_start;
         for (int i = tid; i < a.T; i += blockDim.x) {
             int lo = 0, hi = a.S;  // invariant: query_start[lo] <= i (or lo == 0), answer in [lo, hi)
             while (hi - lo > 1) {
                 const int mid = (lo + hi) >> 1;
                 if (qsv[mid] <= i) lo = mid; else hi = mid;
             }
-            int s = -1;
-            if (a.S > 0 && qsv[lo] <= i && i < qsv[lo + 1]) {
+            int np = 0;
+            if (qsv[lo] <= i && i < qsv[lo + 1]) {
                 const int n = qsv[lo + 1] - qsv[lo];
-                const int len = a.context_lens[lo];
-                if (len >= 0 && len <= cap && n <= len && n <= a.max_query_len) s = lo;
+                const int len = lenv[lo];
+                if (len >= 0 && len <= cap && n <= len && n <= a.max_query_len)
+                    np = (len - n + (i - qsv[lo])) / Pt + 1;
             }
-            a.tok_seq[i] = s;
+            a.row_parts[i] = np;
         }
     }
     if (a.umma_rows > 0) {
         // tcgen05 path: one entry per (sequence, tile group), by step count, longest first
         const int R = a.umma_rows;
         for (int s = tid; s < a.S; s += blockDim.x) {
-            const int raw = a.context_lens[s];
+            const int raw = lenv[s];
             const int len = clamp_len(raw, cap);
-            const int n = a.query_start[s + 1] - a.query_start[s];
+            const int n = qsv[s + 1] - qsv[s];
             if (raw != len || n > len || n > a.max_query_len) {
                 set_error(a.err, PA_DEVERR_BAD_LEN);
                 continue;
@@ -110,19 +118,12 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const ChunkArgs a) {
                 atomicAdd(&hist[min(umma_steps(n, len, G, R, g), kBins - 1)], 1);
         }
         __syncthreads();
-        if (tid == 0) {
-            int acc = 0;
-            for (int z = kBins - 1; z >= 0; --z) {
-                start[z] = acc;
-                acc += hist[z];
-            }
-            a.plan_hdr[0] = acc;
-        }
-        __syncthreads();
+        const int total = scan_bins_desc(hist, start, kBins - 1, kBins, warp_sums);
+        if (tid == 0) a.plan_hdr[0] = total;
         for (int s = tid; s < a.S; s += blockDim.x) {
-            const int raw = a.context_lens[s];
+            const int raw = lenv[s];
             const int len = clamp_len(raw, cap);
-            const int n = a.query_start[s + 1] - a.query_start[s];
+            const int n = qsv[s + 1] - qsv[s];
             if (raw != len || n > len || n > a.max_query_len) continue;
             for (int g = 0; g * R < n * G; ++g) {
                 const int steps = umma_steps(n, len, G, R, g);
@@ -133,9 +134,9 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const ChunkArgs a) {
         return;
     }
     for (int s = tid; s < a.S; s += blockDim.x) {
-        const int raw = a.context_lens[s];
+        const int raw = lenv[s];
         const int len = clamp_len(raw, cap);
-        const int n = a.query_start[s + 1] - a.query_start[s];
+        const int n = qsv[s + 1] - qsv[s];
         if (raw != len || n > len || n > a.max_query_len) {
             set_error(a.err, PA_DEVERR_BAD_LEN);
             continue;
@@ -149,19 +150,13 @@ __global__ void __launch_bounds__(1024) chunk_plan_kernel(const ChunkArgs a) {
             }
     }
     __syncthreads();
-    if (tid == 0) {
-        int acc = 0;
-        for (int z = maxpb; z >= 1; --z) {
-            start[z] = acc;
-            acc += hist[z];
-        }
-        a.plan_hdr[0] = acc * (a.Hkv / a.head_group);  // items: (sequence, partition, row block, head group)
-    }
-    __syncthreads();
+    // bins maxpb .. 1 (a partition's block count), largest first
+    const int total = scan_bins_desc(hist, start, maxpb, maxpb, warp_sums);
+    if (tid == 0) a.plan_hdr[0] = total * (a.Hkv / a.head_group);  // items: (sequence, partition, row block, head group)
     for (int s = tid; s < a.S; s += blockDim.x) {
-        const int raw = a.context_lens[s];
+        const int raw = lenv[s];
         const int len = clamp_len(raw, cap);
-        const int n = a.query_start[s + 1] - a.query_start[s];
+        const int n = qsv[s + 1] - qsv[s];
         if (raw != len || n > len || n > a.max_query_len) continue;
         const int nrb = (n * G + rpb - 1) / rpb;
         for (int rb = 0; rb < nrb; ++rb)
@@ -187,41 +182,61 @@ cudaError_t launch_chunk_plan(const ChunkArgs &a, cudaStream_t st) {
     return cudaLaunchKernelEx(&cfg, chunk_plan_kernel, a);
 }
 
-// One warp per (query row, query head): combine the row's partitions.
+// One warp per (query row, query head): combine the row's partitions.  The
+// plan stored how many the row sees; rows with at most kFast of them load every
+// (m, l) pair and partial sum in one round trip.
 template <int D>
 __global__ void chunk_merge_kernel(const ChunkArgs a) {
     constexpr int kPer = D / 32;
+    constexpr int kFast = 8;
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int gw = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
     if (gw >= a.T * a.Hq) return;
-    const int i = gw / a.Hq;
-    const int s = a.tok_seq[i];
-    if (s < 0) return;
-    const int qs = a.query_start[s];
-    const int n = a.query_start[s + 1] - qs;
-    const int len = clamp_len(a.context_lens[s], a.max_blocks * a.B);
-    const int pos = len - n + (i - qs);
-    const int np = pos / a.partition_size + 1;
-    if (np <= 1) return;  // written in place by the partition kernel
+    const int np = a.row_parts[gw / a.Hq];
+    if (np <= 1) return;  // no sequence, or written in place by the partition kernel
     const size_t r0 = (size_t)gw * a.max_parts;
     const float *ml = a.ws_ml + 2 * r0;
-    const float *acc = a.ws_acc + r0 * D;
-    float M = -INFINITY;
-    for (int p = lane; p < np; p += 32) M = fmaxf(M, ml[2 * p]);
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float L = 0.f;
+    const float *acc = a.ws_acc + r0 * D + lane * kPer;
+    float M = -INFINITY, L = 0.f;
     float o[kPer];
 #pragma unroll
     for (int k = 0; k < kPer; ++k) o[k] = 0.f;
-    if (M != -INFINITY) {
-        for (int p = 0; p < np; ++p) {
-            const float2 w = *reinterpret_cast<const float2 *>(ml + 2 * p);
-            const float wt = ex2(w.x - M);  // 0 for a partition that saw no key
-            L += wt * w.y;
+    if (np <= kFast) {
+        float2 w[kFast];
+        float x[kFast][kPer];
 #pragma unroll
-            for (int k = 0; k < kPer; ++k) o[k] += wt * acc[(size_t)p * D + lane * kPer + k];
+        for (int p = 0; p < kFast; ++p) {
+            if (p < np) {
+                w[p] = *reinterpret_cast<const float2 *>(ml + 2 * p);
+#pragma unroll
+                for (int k = 0; k < kPer; ++k) x[p][k] = acc[(size_t)p * D + k];
+                M = fmaxf(M, w[p].x);
+            }
+        }
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int p = 0; p < kFast; ++p) {
+                if (p < np) {
+                    const float wt = ex2(w[p].x - M);  // 0 for a partition that saw no key
+                    L += wt * w[p].y;
+#pragma unroll
+                    for (int k = 0; k < kPer; ++k) o[k] += wt * x[p][k];
+                }
+            }
+        }
+    } else {
+        for (int p = lane; p < np; p += 32) M = fmaxf(M, ml[2 * p]);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        if (M != -INFINITY) {
+            for (int p = 0; p < np; ++p) {
+                const float2 w = *reinterpret_cast<const float2 *>(ml + 2 * p);
+                const float wt = ex2(w.x - M);
+                L += wt * w.y;
+#pragma unroll
+                for (int k = 0; k < kPer; ++k) o[k] += wt * acc[(size_t)p * D + k];
+            }
         }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;

@@ -159,4 +159,34 @@ __device__ __forceinline__ void set_error(unsigned int *err, unsigned int bit) {
     if (err) atomicOr(err, bit);
 }
 
+// Exclusive scan of hist[hi], hist[hi - 1], ..., hist[hi - nb + 1] (largest
+// bin first) into start[]; returns the total.  Every thread of a 1024-thread block calls it; nb <= 1024.
+__device__ __forceinline__ int scan_bins_desc(const int *hist, int *start, int hi, int nb, int *warp_sums) {
+    const int t = threadIdx.x;
+    const int lane = t & 31, wid = t >> 5;
+    const int v = t < nb ? hist[hi - t] : 0;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += u;
+    }
+    if (lane == 31) warp_sums[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int w = warp_sums[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, w, off);
+            if (lane >= off) w += u;
+        }
+        warp_sums[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    if (t < nb) start[hi - t] = (wid > 0 ? warp_sums[wid - 1] : 0) + incl - v;
+    const int total = warp_sums[31];
+    __syncthreads();
+    return total;
+}
+
 }  // namespace pa

@@ -46,7 +46,7 @@ struct ChunkArgs {
     float *ws_acc;                  // [T, Hq, P, D]
     int *plan_hdr;                  // [0] work items, [1] claim counter
     int4 *plan_list;                // (sequence, partition, tokens, row block), largest first
-    int32_t *tok_seq;               // [T]: sequence of each query row, -1 if none
+    int32_t *row_parts;             // [T]: partitions each query row sees, 0 if the row has no sequence
     unsigned int *err;
     int S, T, Hq, Hkv, D, B, N, max_blocks, partition_size, max_parts, max_query_len;
     int head_group;                 // KV heads per work item

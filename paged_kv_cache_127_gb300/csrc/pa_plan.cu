@@ -12,9 +12,13 @@
 
 namespace pa {
 
+constexpr int kLenCache = 4096;
+
 __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeArgs a) {
     __shared__ int hist[kMaxPartitionBlocks + 1];
     __shared__ int start[kMaxPartitionBlocks + 1];
+    __shared__ int warp_sums[32];
+    __shared__ int len_cache[kLenCache];  // context_lens, read once when they fit
     // Let the decode kernel start its set-up (it waits for this grid before
     // reading anything written here), then wait for the work before this one
     // in the stream: the workspace and context_lens are only touched after it.
@@ -30,9 +34,13 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeArgs a) {
         a.plan_hdr[1] = 0;
         a.plan_hdr[2] = 0;
     }
+    const bool cached = a.S <= kLenCache;
+    if (cached)
+        for (int s = tid; s < a.S; s += blockDim.x) len_cache[s] = a.context_lens[s];
     __syncthreads();
+    const int *lenv = cached ? len_cache : a.context_lens;
     for (int s = tid; s < a.S; s += blockDim.x) {
-        int len = a.context_lens[s];
+        int len = lenv[s];
         if (len < 0 || len > cap) {
             set_error(a.err, PA_DEVERR_BAD_LEN);
             len = len < 0 ? 0 : cap;
@@ -51,17 +59,11 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const DecodeArgs a) {
         }
     }
     __syncthreads();
-    if (tid == 0) {
-        int acc = 0;
-        for (int z = maxpb; z >= 1; --z) {
-            start[z] = acc;
-            acc += hist[z];
-        }
-        a.plan_hdr[0] = acc * (a.Hkv / a.head_group);  // items: (sequence, partition, head group)
-    }
-    __syncthreads();
+    // list positions by block count, largest first
+    const int total = scan_bins_desc(hist, start, maxpb, maxpb, warp_sums);
+    if (tid == 0) a.plan_hdr[0] = total * (a.Hkv / a.head_group);  // items: (sequence, partition, head group)
     for (int s = tid; s < a.S; s += blockDim.x) {
-        int len = a.context_lens[s];
+        int len = lenv[s];
         len = len < 0 ? 0 : (len > cap ? cap : len);
         const int np = (len + Pt - 1) / Pt;
         for (int p = 0; p < np; ++p) {
