@@ -75,7 +75,8 @@ typedef struct pa_dims {
                                  /* W = num_seqs * num_kv_heads / 4 (work items per  */
                                  /* partition), 512 if W >= 256, 256 if W >= 32,     */
                                  /* else 128 (smaller partitions give a small batch  */
-                                 /* enough parallel work)                            */
+                                 /* enough parallel work); pa_chunk_attention takes  */
+                                 /* four times that, at most 2048                    */
     int32_t kv_dtype;            /* pa_dtype of q, k, v, k_cache and v_cache         */
 } pa_dims;
 
@@ -196,9 +197,10 @@ PA_API int32_t pa_decode_noalloc(const pa_dims *dims, const void *q, const void 
  * sequence), walking each tile's whole context (no partitions, no merge).
  *
  * pa_chunk_workspace_bytes -- the scratch it needs: a work list of S * P * R
- * int4 entries after a 256-byte header, a token-to-sequence map of T ints,
- * and, on the mma.sync path with P > 1, the split-K partials T * Hq * P *
- * (D + 2) floats, each part rounded up to 256 bytes; P as for pa_decode,
+ * int4 entries after a 256-byte header, T ints (the partitions each query
+ * row sees), and, on the mma.sync path with P > 1, the split-K partials
+ * T * Hq * P * (D + 2) floats, each part rounded up to 256 bytes; P as for
+ * pa_decode, with the partition size chosen as for pa_chunk_attention,
  * R = ceil(ceil(max_query_len * Hq / Hkv / 16) / W), W = 2 if max_query_len *
  * Hq / Hkv > 16, else 1.  Returns 0 for invalid arguments.
  */

@@ -57,15 +57,26 @@ int32_t effective_partition(const pa_dims *d) {
     return 128;
 }
 
-// Full decode checks; fills max_parts.
-int32_t check_decode_dims(const pa_dims *d, int32_t *max_parts) {
+// partition_size 0 for chunk attention: four times the decode choice, at most
+// 2048 tokens.  A chunk item carries several query rows per KV head, so each
+// key costs more arithmetic and fewer, longer partitions pay: fewer items to
+// set up and fewer partials to merge (measured on 256 sequences x 5 queries,
+// 8B-shaped: 512 tokens 4.54 TB/s, 1024 4.79, 2048 4.99).
+int32_t chunk_partition(const pa_dims *d) {
+    if (d->partition_size > 0) return d->partition_size;
+    const int32_t pt = 4 * effective_partition(d);
+    const int32_t cap = pa::kMaxPartitionBlocks * (d->block_size > 0 ? d->block_size : 1);
+    return pt < 2048 ? (pt < cap ? pt : cap) : (2048 < cap ? 2048 : cap);
+}
+
+// Full decode checks for partitions of pt tokens; fills max_parts.
+int32_t check_decode_dims_pt(const pa_dims *d, int32_t pt, int32_t *max_parts) {
     int32_t rc = check_cache_dims(d);
     if (rc != PA_OK) return rc;
     if (d->num_seqs < 0 || d->num_q_heads <= 0 || d->max_blocks_per_seq <= 0) return PA_ERR_INVALID;
     if (d->num_q_heads % d->num_kv_heads != 0) return PA_ERR_INVALID;
     if (d->partition_size < 0) return PA_ERR_INVALID;
     const int32_t G = d->num_q_heads / d->num_kv_heads;
-    const int32_t pt = effective_partition(d);
     if (pt % d->block_size != 0 || pt / d->block_size > pa::kMaxPartitionBlocks) return PA_ERR_INVALID;
     if (!(d->head_dim == 64 || d->head_dim == 128) || !(d->block_size == 16 || d->block_size == 32) ||
         !(G == 1 || G == 2 || G == 4 || G == 8))
@@ -79,6 +90,11 @@ int32_t check_decode_dims(const pa_dims *d, int32_t *max_parts) {
     if ((int64_t)d->num_seqs * d->num_kv_heads > INT32_MAX) return PA_ERR_INVALID;
     *max_parts = (int32_t)parts;
     return PA_OK;
+}
+
+int32_t check_decode_dims(const pa_dims *d, int32_t *max_parts) {
+    if (!d) return PA_ERR_INVALID;
+    return check_decode_dims_pt(d, effective_partition(d), max_parts);
 }
 
 // Workspace layout, each part 256-byte aligned:
@@ -112,7 +128,8 @@ size_t workspace_bytes_for(const pa_dims *d, int32_t max_parts) {
 // Chunk-attention checks: the decode checks, 16-bit caches only, and a token
 // count and query-length bound whose scratch sizes stay addressable.
 int32_t check_chunk_dims(const pa_dims *d, int32_t T, int32_t max_q, int32_t *max_parts) {
-    int32_t rc = check_decode_dims(d, max_parts);
+    if (!d) return PA_ERR_INVALID;
+    int32_t rc = check_decode_dims_pt(d, chunk_partition(d), max_parts);
     if (rc != PA_OK) return rc;
     if (d->kv_dtype == PA_F32) return PA_ERR_UNSUPPORTED;
     if (T < 0 || max_q < 1 || max_q > (1 << 20)) return PA_ERR_INVALID;
@@ -341,7 +358,7 @@ int32_t pa_chunk_attention(const pa_dims *dims, const void *q, const void *k_cac
     a.B = dims->block_size;
     a.N = dims->num_blocks;
     a.max_blocks = dims->max_blocks_per_seq;
-    a.partition_size = effective_partition(dims);
+    a.partition_size = chunk_partition(dims);
     a.max_parts = parts;
     a.max_query_len = max_query_len;
     a.head_group = pa::decode_head_group(dims->num_kv_heads);

@@ -15,6 +15,7 @@
 // equation).
 #include "pa_device.cuh"
 #include "pa_internal.h"
+#include "pa_merge.cuh"
 
 namespace pa {
 
@@ -182,76 +183,22 @@ cudaError_t launch_chunk_plan(const ChunkArgs &a, cudaStream_t st) {
     return cudaLaunchKernelEx(&cfg, chunk_plan_kernel, a);
 }
 
-// One warp per (query row, query head): combine the row's partitions.  The
-// plan stored how many the row sees; rows with at most kFast of them load every
-// (m, l) pair and partial sum in one round trip.
+// One block per query row (pa_merge.cuh): the plan stored how many
+// partitions the row sees; a row with one was written in place.
 template <int D>
-__global__ void chunk_merge_kernel(const ChunkArgs a) {
-    constexpr int kPer = D / 32;
-    constexpr int kFast = 8;
+__global__ void __launch_bounds__(kMergeWarps * 32, 3) chunk_merge_kernel(const ChunkArgs a) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int gw = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-    const int lane = threadIdx.x & 31;
-    if (gw >= a.T * a.Hq) return;
-    const int np = a.row_parts[gw / a.Hq];
+    const int i = blockIdx.x;
+    const int np = a.row_parts[i];
     if (np <= 1) return;  // no sequence, or written in place by the partition kernel
-    const size_t r0 = (size_t)gw * a.max_parts;
-    const float *ml = a.ws_ml + 2 * r0;
-    const float *acc = a.ws_acc + r0 * D + lane * kPer;
-    float M = -INFINITY, L = 0.f;
-    float o[kPer];
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) o[k] = 0.f;
-    if (np <= kFast) {
-        float2 w[kFast];
-        float x[kFast][kPer];
-#pragma unroll
-        for (int p = 0; p < kFast; ++p) {
-            if (p < np) {
-                w[p] = *reinterpret_cast<const float2 *>(ml + 2 * p);
-#pragma unroll
-                for (int k = 0; k < kPer; ++k) x[p][k] = acc[(size_t)p * D + k];
-                M = fmaxf(M, w[p].x);
-            }
-        }
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int p = 0; p < kFast; ++p) {
-                if (p < np) {
-                    const float wt = ex2(w[p].x - M);  // 0 for a partition that saw no key
-                    L += wt * w[p].y;
-#pragma unroll
-                    for (int k = 0; k < kPer; ++k) o[k] += wt * x[p][k];
-                }
-            }
-        }
-    } else {
-        for (int p = lane; p < np; p += 32) M = fmaxf(M, ml[2 * p]);
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        if (M != -INFINITY) {
-            for (int p = 0; p < np; ++p) {
-                const float2 w = *reinterpret_cast<const float2 *>(ml + 2 * p);
-                const float wt = ex2(w.x - M);
-                L += wt * w.y;
-#pragma unroll
-                for (int k = 0; k < kPer; ++k) o[k] += wt * acc[(size_t)p * D + k];
-            }
-        }
-    }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    float *dst = a.out + (size_t)gw * D + lane * kPer;
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) dst[k] = o[k] * inv;
+    merge_row<D>(i, np, a.Hq, a.max_parts, a.ws_ml, a.ws_acc, a.out);
 }
 
 cudaError_t launch_chunk_merge(const ChunkArgs &a, cudaStream_t st) {
-    const long long warps = (long long)a.T * a.Hq;
-    if (warps == 0) return cudaSuccess;
-    const int per_block = 4;
+    if (a.T == 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((warps + per_block - 1) / per_block));
-    cfg.blockDim = dim3(per_block * 32);
+    cfg.gridDim = dim3((unsigned)a.T);
+    cfg.blockDim = dim3(kMergeWarps * 32);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

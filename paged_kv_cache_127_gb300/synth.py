@@ -235,7 +235,8 @@ def workload(name: str, seed: int = 0) -> Workload:
                         num_seqs=32, lengths=uniform_lengths(rng, 32, 8192, 32768))
     if name == "verify8b":
         ctx = lognormal_lengths(rng, 256, 600, 0.8, 1, 4096 - 5)
-        return Workload(name, "bf16", 32, 8, 128, 16, 512, 1.0, 1.0, q_prescale=1.0 / math.sqrt(128),
+        # 2048-token partitions: what partition_size 0 picks for chunk attention at this batch
+        return Workload(name, "bf16", 32, 8, 128, 16, 2048, 1.0, 1.0, q_prescale=1.0 / math.sqrt(128),
                         num_seqs=256, lengths=ctx + 5, query_len=5)
     if name == "prefill8b":
         ctx = uniform_lengths(rng, 16, 0, 4096 - 512)

@@ -145,6 +145,24 @@ def test_chunk_workspace_bytes(pa):
     assert pa.pa_chunk_workspace_bytes(d, T, 5) == 0
 
 
+def test_chunk_automatic_partition(pa):
+    # partition_size 0: decode takes 512 tokens at W = S * Hkv / 4 >= 256 work
+    # items per partition; chunk attention takes four times that, at most 2048
+    def up(x):
+        return (x + 255) // 256 * 256
+
+    S, Hq, Hkv, D, T = 256, 32, 8, 128, 1280
+    d = pa.make_dims(num_seqs=S, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, block_size=16,
+                     num_blocks=1000, max_blocks_per_seq=256, partition_size=0, kv_dtype="bf16")
+    P = (256 * 16 + 2047) // 2048
+    assert pa.pa_chunk_workspace_bytes(d, T, 5) == 256 + up(S * P * 16) + up(T * 4) + \
+        up(T * Hq * P * D * 4) + up(T * Hq * P * 2 * 4)
+    d.num_seqs = 16                      # W = 32: decode 256, chunk 1024
+    P = (256 * 16 + 1023) // 1024
+    assert pa.pa_chunk_workspace_bytes(d, 80, 5) == 256 + up(16 * P * 16) + up(80 * 4) + \
+        up(80 * Hq * P * D * 4) + up(80 * Hq * P * 2 * 4)
+
+
 def test_chunk_rejects_bad_arguments_on_the_host(pa):
     def status(T=4, max_q=2, ws=None, ws_bytes=0, **over):
         kw = dict(num_seqs=2, num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16, num_blocks=8,
