@@ -49,8 +49,8 @@ FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 126 * 2**20
 KERNEL_SOURCES = ("pa_decode_mma.cuh", "pa_plan.cu", "pa_cache_ops.cu", "pa_tmap.cu", "pa_api.cu",
                   "pa_device.cuh", "pa_internal.h", "pa_mma.cuh")
-CHUNK_SOURCES = ("pa_chunk_mma.cuh", "pa_chunk_umma.cuh", "pa_tcgen05.cuh", "pa_chunk.cu", "pa_tmap.cu", "pa_api.cu",
-                 "pa_device.cuh", "pa_internal.h", "pa_mma.cuh")
+CHUNK_SOURCES = ("pa_chunk_mma.cuh", "pa_chunk_umma.cuh", "pa_tcgen05.cuh", "pa_chunk.cu", "pa_merge.cuh", "pa_tmap.cu",
+                 "pa_api.cu", "pa_device.cuh", "pa_internal.h", "pa_mma.cuh")
 
 
 # --------------------------------------------------------------------------- distributed helpers
