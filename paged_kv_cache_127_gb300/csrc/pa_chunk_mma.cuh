@@ -296,6 +296,16 @@ __global__ void __launch_bounds__(ChunkCfg<D, HG, RW>::kThreads, ChunkCfg<D, HG,
             if (nv > 0 && j * 16 <= wlim) {
                 const uint32_t kst = base + (uint32_t)(st * C::kStageBytes) + (uint32_t)(head * C::kHeadSub);
                 const uint32_t vst = kst + C::kTileBytes;
+                // V fragments first: they do not depend on P, so their shared-memory
+                // latency hides behind S and the softmax instead of stalling P V
+                uint32_t bv[C::kNT / 2][4];
+#pragma unroll
+                for (int ntp = 0; ntp < C::kNT / 2; ++ntp) {
+                    const uint32_t addr = vst + (uint32_t)((ntp >> 2) * C::kBoxBytes) +
+                                          (uint32_t)(((lm & 1) * 8 + lr) * 128) +
+                                          (((uint32_t)(2 * (ntp & 3)) ^ vx) << 4);
+                    ldsm_x4_t(addr, bv[ntp][0], bv[ntp][1], bv[ntp][2], bv[ntp][3]);
+                }
                 // ---- S = Q K^T for 16 tokens (two n-tiles of 8), even / odd k-steps apart
                 float sc[2][2][4];
 #pragma unroll
@@ -385,14 +395,10 @@ __global__ void __launch_bounds__(ChunkCfg<D, HG, RW>::kThreads, ChunkCfg<D, HG,
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const int ntp = 2 * ntq + u;
-                        const uint32_t addr = vst + (uint32_t)((ntp >> 2) * C::kBoxBytes) +
-                                              (uint32_t)(((lm & 1) * 8 + lr) * 128) +
-                                              (((uint32_t)(2 * (ntp & 3)) ^ vx) << 4);
-                        ldsm_x4_t(addr, b[u][0], b[u][1], b[u][2], b[u][3]);
-                        b[u][0] &= mlo;
-                        b[u][1] &= mhi;
-                        b[u][2] &= mlo;
-                        b[u][3] &= mhi;
+                        b[u][0] = bv[ntp][0] & mlo;
+                        b[u][1] = bv[ntp][1] & mhi;
+                        b[u][2] = bv[ntp][2] & mlo;
+                        b[u][3] = bv[ntp][3] & mhi;
                     }
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
