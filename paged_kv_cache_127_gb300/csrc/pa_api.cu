@@ -291,6 +291,9 @@ int32_t decode_call(const pa_dims *dims, const void *q, const void *k_cache, con
     if (e == cudaSuccess)
         e = cache_tensor_map(v_cache, bf16, dims->head_dim, dims->block_size, block_heads, a.head_group, &tmv);
     if (e != cudaSuccess) return PA_ERR_CUDA;
+    e = bf16 ? pa::decode_mma_ctas_bf16(a, &a.ctas) : pa::decode_mma_ctas_f16(a, &a.ctas);
+    if (e != cudaSuccess) return to_status(e);
+    a.early = phase == DecodePhase::kPlanAndRun ? 1 : 0;  // the decode kernel follows its own plan
     if (phase != DecodePhase::kRunOnly) {
         e = pa::launch_decode_plan(a, st);
         if (e != cudaSuccess) return to_status(e);

@@ -7,4 +7,7 @@ cudaError_t launch_decode_mma_bf16(const DecodeArgs &a, const CUtensorMap &tmk, 
                                  cudaStream_t st) {
     return dispatch_decode_mma<__nv_bfloat16>(a, tmk, tmv, st);
 }
+cudaError_t decode_mma_ctas_bf16(const DecodeArgs &a, int *ctas) {
+    return dispatch_decode_mma_grid<__nv_bfloat16>(a, ctas);
+}
 }  // namespace pa

@@ -7,4 +7,7 @@ cudaError_t launch_decode_mma_f16(const DecodeArgs &a, const CUtensorMap &tmk, c
                                  cudaStream_t st) {
     return dispatch_decode_mma<__half>(a, tmk, tmv, st);
 }
+cudaError_t decode_mma_ctas_f16(const DecodeArgs &a, int *ctas) {
+    return dispatch_decode_mma_grid<__half>(a, ctas);
+}
 }  // namespace pa

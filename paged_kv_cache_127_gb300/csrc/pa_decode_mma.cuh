@@ -126,11 +126,14 @@ __global__ void __launch_bounds__(MmaCfg<D, HG>::kThreads, 2)
         prefetch_tmap(&tmv);
     }
     __syncthreads();
-    griddep_wait();  // the plan kernel's work list must be complete (no-op without PDL)
+    // Right after this call's own plan kernel (a.early), everything before the
+    // plan is complete when this grid starts, so the caches, tables and lengths
+    // may be read at once; only the producer waits, for the plan's list, before
+    // its first claim.  Otherwise wait here for the kernel before this one.
+    if (!a.early) griddep_wait();
     // The merge kernel may be scheduled now: it only waits (griddepcontrol.wait)
     // beside this grid, which already fills every SM, and starts on completion.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int n_items = a.plan_hdr[0];
 
     // ---- lane roles in the MMA fragments
     const int g = lane >> 2;         // fragment row = query head within the group (rows 8-15: P_lo)
@@ -146,13 +149,19 @@ __global__ void __launch_bounds__(MmaCfg<D, HG>::kThreads, 2)
     // loads, up to kStages chunks ahead of the consumer warps and across item
     // boundaries; it never consumes, so a claim (an atomic, the list entry and
     // the item's table slice) overlaps the chunks already in the ring instead
-    // of stalling it.  A CTA's first item is list entry blockIdx.x; every later
-    // one is claimed from the counter only when the issue cursor reaches it (a
-    // few chunks before it is consumed).  Claiming any earlier would fix each
-    // CTA's last item while the list still holds bigger ones, and the
-    // largest-first order would no longer bound the tail.
+    // of stalling it.  CTA b's first item is partition 0 of sequence
+    // b / ngroups, head group b % ngroups, for the first min(S, grid / ngroups)
+    // sequences; the plan's list holds every other item, and each is claimed
+    // from the counter only when the issue cursor reaches it (a few chunks
+    // before it is consumed).  Claiming any earlier would fix each CTA's last
+    // item while the list still holds bigger ones, and the largest-first order
+    // would no longer bound the tail.
     if (warp == C::kConsumers) {
         const uint64_t pol = policy_evict_first();
+        const int nstatic = min(a.S, (int)gridDim.x / ngroups) * ngroups;  // items taken without the list
+        const int cap = a.max_blocks * B;
+        bool listed = false;  // the plan's list is complete and visible
+        int n_items = 0;
         int iss = 0;  // chunks issued
         bool ok = true;
         for (int seq = 0; ok; ++seq) {
@@ -163,15 +172,39 @@ __global__ void __launch_bounds__(MmaCfg<D, HG>::kThreads, 2)
                 if (lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
                 break;
             }
-            int idx = 0;
-            if (lane == 0) idx = seq == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(a.plan_hdr + 1, 1);
-            idx = __shfl_sync(0xffffffffu, idx, 0);
+            int4 e = make_int4(0, 0, 0, 0);
+            int g0 = 0;
+            bool have = false;
+            if (seq == 0 && (int)blockIdx.x < nstatic) {
+                const int s = blockIdx.x / ngroups;
+                int len = a.context_lens[s];
+                len = len < 0 ? 0 : (len > cap ? cap : len);  // the plan flags bad lengths
+                if (len > 0) {
+                    e = make_int4(s, 0, min(a.partition_size, len), (len + a.partition_size - 1) / a.partition_size);
+                    g0 = (blockIdx.x % ngroups) * HG;
+                    have = true;
+                }
+            }
+            if (!have) {
+                if (!listed) {
+                    griddep_wait();
+                    n_items = a.plan_hdr[0];
+                    listed = true;
+                }
+                int idx = 0;
+                if (lane == 0) idx = atomicAdd(a.plan_hdr + 1, 1);
+                idx = __shfl_sync(0xffffffffu, idx, 0);
+                if (idx < n_items) {
+                    e = a.plan_list[idx / ngroups];
+                    g0 = (idx % ngroups) * HG;
+                    have = true;
+                }
+            }
             int4 e0 = make_int4(0, 0, 0, 0), e1 = make_int4(0, 0, 0, 0);
             int32_t *tb = tbl + slot * C::kTblCap;
-            if (idx < n_items) {
-                const int4 e = a.plan_list[idx / ngroups];
+            if (have) {
                 e0 = e;
-                e1 = make_int4((idx % ngroups) * HG, (e.z + 15) >> 4, 1, 0);
+                e1 = make_int4(g0, (e.z + 15) >> 4, 1, 0);
                 const int nblk = (e.z + B - 1) / B;
                 const int32_t *row = a.block_tables + (size_t)e.x * a.max_blocks + (size_t)e.y * (a.partition_size / B);
                 for (int i = lane; i < nblk; i += 32) {
@@ -189,7 +222,7 @@ __global__ void __launch_bounds__(MmaCfg<D, HG>::kThreads, 2)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(ifull0 + 8 * slot);  // release: info and table visible
-            if (idx >= n_items) break;
+            if (!have) break;
             for (int c = 0; c < e1.y; ++c) {
                 const int st = iss % C::kStages;
                 // every consumer warp has released this stage's previous chunk
@@ -225,7 +258,9 @@ __global__ void __launch_bounds__(MmaCfg<D, HG>::kThreads, 2)
         for (int k = iss > C::kStages ? iss - C::kStages : 0; k < iss; ++k)
             mbar_wait_bounded(full0 + 8 * (k % C::kStages), (uint32_t)(k / C::kStages) & 1u, kWaitLimit);
         // This warp made every claim of the CTA.  The last CTA to get here
-        // resets the counters, so the plan's list can serve the next launch.
+        // resets the counters, so the plan's list can serve the next launch
+        // (after the plan itself, which resets them first, has completed).
+        if (!listed) griddep_wait();
         if (lane == 0) {
             __threadfence();
             if (atomicAdd(a.plan_hdr + 2, 1) == (int)gridDim.x - 1) {
@@ -471,6 +506,27 @@ cudaError_t dispatch_decode_mma(const DecodeArgs &a, const CUtensorMap &tmk, con
     if (a.D == 64 && a.B == 32) return dispatch_decode_mma_hg<T, 64, 32>(a, tmk, tmv, st);
     if (a.D == 128 && a.B == 16) return dispatch_decode_mma_hg<T, 128, 16>(a, tmk, tmv, st);
     if (a.D == 128 && a.B == 32) return dispatch_decode_mma_hg<T, 128, 32>(a, tmk, tmv, st);
+    return cudaErrorNotSupported;
+}
+
+template <typename T, int D, int B>
+cudaError_t decode_mma_grid_hg(const DecodeArgs &a, int *grid) {
+    switch (a.head_group) {
+#if PA_MMA_HEAD_GROUP >= 8
+        case 8: return decode_mma_grid<T, D, B, 8>(grid);
+#endif
+        case 4: return decode_mma_grid<T, D, B, 4>(grid);
+        case 2: return decode_mma_grid<T, D, B, 2>(grid);
+        default: return decode_mma_grid<T, D, B, 1>(grid);
+    }
+}
+
+template <typename T>
+cudaError_t dispatch_decode_mma_grid(const DecodeArgs &a, int *grid) {
+    if (a.D == 64 && a.B == 16) return decode_mma_grid_hg<T, 64, 16>(a, grid);
+    if (a.D == 64 && a.B == 32) return decode_mma_grid_hg<T, 64, 32>(a, grid);
+    if (a.D == 128 && a.B == 16) return decode_mma_grid_hg<T, 128, 16>(a, grid);
+    if (a.D == 128 && a.B == 32) return decode_mma_grid_hg<T, 128, 32>(a, grid);
     return cudaErrorNotSupported;
 }
 

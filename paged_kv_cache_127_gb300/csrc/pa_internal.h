@@ -31,6 +31,13 @@ struct DecodeArgs {
     // plan once: the work list depends only on the tables and lengths).
     int zero_layers;
     long long out_layer_floats;
+    // Tensor-core path: CTAs of the decode grid, and whether the decode may
+    // start before its predecessor completes (early != 0 only right after this
+    // call's own plan kernel, which lets it start once everything before the
+    // plan is complete).  The first sequences' partition 0 is taken by CTAs
+    // directly, without the plan's list: sequences s < min(S, ctas / groups).
+    int ctas;
+    int early;
 };
 
 // Everything a chunk-attention launch needs (several query tokens per sequence).
@@ -120,6 +127,10 @@ cudaError_t launch_decode_mma_f16(const DecodeArgs &a, const CUtensorMap &tmk, c
                                   cudaStream_t st);
 cudaError_t launch_decode_mma_bf16(const DecodeArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                    cudaStream_t st);
+// CTAs the tensor-core decode launches for these shapes on the current device
+// (a persistent grid: SMs x resident CTAs per SM).
+cudaError_t decode_mma_ctas_f16(const DecodeArgs &a, int *ctas);
+cudaError_t decode_mma_ctas_bf16(const DecodeArgs &a, int *ctas);
 
 // pa_decode with its launches split: kPlanAndRun is pa_decode; kPlanOnly
 // writes the work list (and the zero rows of `zero_layers` outputs spaced
