@@ -73,3 +73,18 @@ def test_reference_arm_runs_the_oracle_on_cpu(monkeypatch):
     assert line["metric"] == bench.METRIC
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+
+
+def test_prefix_cache_mode_bounds_its_repetitions(monkeypatch):
+    # host-only mode: the default --steps (sized for the decode bench) must not
+    # repeat the whole request stream thousands of times
+    sys.path.insert(0, ROOT)
+    import bench
+    for k in ("RANK", "LOCAL_RANK", "WORLD_SIZE"):
+        monkeypatch.delenv(k, raising=False)
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.main(["--prefix-requests", "300", "--steps", "5000", "--warmup", "50", "--no-cpu-baseline"])
+    line = json.loads(buf.getvalue().strip().splitlines()[-1])
+    assert line["steps"] == 5 and line["unit"] == "requests/s" and line["value"] > 0
+    assert line["gpu_launches"] == 0
