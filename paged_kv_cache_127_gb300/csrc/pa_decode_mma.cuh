@@ -151,7 +151,8 @@ __global__ void __launch_bounds__(MmaCfg<D, HG>::kThreads, 2)
     // the item's table slice) overlaps the chunks already in the ring instead
     // of stalling it.  CTA b's first item is partition 0 of sequence
     // b / ngroups, head group b % ngroups, for the first min(S, grid / ngroups)
-    // sequences; the plan's list holds every other item, and each is claimed
+    // sequences (b < nstatic), else list entry b - nstatic; the plan's list
+    // holds every item but the direct ones, and each later item is claimed
     // from the counter only when the issue cursor reaches it (a few chunks
     // before it is consumed).  Claiming any earlier would fix each CTA's last
     // item while the list still holds bigger ones, and the largest-first order
@@ -191,8 +192,11 @@ __global__ void __launch_bounds__(MmaCfg<D, HG>::kThreads, 2)
                     n_items = a.plan_hdr[0];
                     listed = true;
                 }
+                // CTAs past the directly taken items start with list entry
+                // b - nstatic, without an atomic; later claims follow them
                 int idx = 0;
-                if (lane == 0) idx = atomicAdd(a.plan_hdr + 1, 1);
+                if (seq == 0 && (int)blockIdx.x >= nstatic) idx = blockIdx.x - nstatic;
+                else if (lane == 0) idx = (int)gridDim.x - nstatic + atomicAdd(a.plan_hdr + 1, 1);
                 idx = __shfl_sync(0xffffffffu, idx, 0);
                 if (idx < n_items) {
                     e = a.plan_list[idx / ngroups];
