@@ -460,27 +460,24 @@ template <typename T, int D, int B, int HG, int RW>
 cudaError_t launch_chunk_mma_t(const ChunkArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                cudaStream_t st) {
     using C = ChunkCfg<D, HG, RW>;
-    static bool configured[64] = {};
-    static int grid_for[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        e = cudaFuncSetAttribute(chunk_mma_kernel<T, D, B, HG, RW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)C::kSmem);
-        if (e != cudaSuccess) return e;
+    static std::atomic<int> grid_for[kMaxLaunchDevices];
+    int grid = 0;
+    cudaError_t e = per_device_value(grid_for, &grid, [](int dev, int *v) {
+        cudaError_t r = cudaFuncSetAttribute(chunk_mma_kernel<T, D, B, HG, RW>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+        if (r != cudaSuccess) return r;
         int sms = 0, per_sm = 0;
-        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chunk_mma_kernel<T, D, B, HG, RW>, C::kThreads,
+        r = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (r != cudaSuccess) return r;
+        r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, chunk_mma_kernel<T, D, B, HG, RW>, C::kThreads,
                                                           C::kSmem);
-        if (e != cudaSuccess) return e;
-        grid_for[dev] = sms * (per_sm > 0 ? per_sm : 1);
-        configured[dev] = true;
-    }
+        if (r != cudaSuccess) return r;
+        *v = sms * (per_sm > 0 ? per_sm : 1);
+        return cudaSuccess;
+    });
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid_for[dev]);
+    cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = st;

@@ -499,17 +499,14 @@ template <typename T, int D, int B, int MT>
 cudaError_t launch_chunk_umma_t(const ChunkArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                 cudaStream_t st) {
     using C = UmmaCfg<D, MT>;
-    static bool configured[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static std::atomic<int> configured[kMaxLaunchDevices];
+    int one = 0;
+    cudaError_t e = per_device_value(configured, &one, [](int, int *v) {
+        *v = 1;
+        return cudaFuncSetAttribute(chunk_umma_kernel<T, D, B, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)C::kSmem);
+    });
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        e = cudaFuncSetAttribute(chunk_umma_kernel<T, D, B, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)C::kSmem);
-        if (e != cudaSuccess) return e;
-        configured[dev] = true;
-    }
     const int G = a.Hq / a.Hkv;
     const long long rows = (long long)a.max_query_len * G;
     const long long groups = (rows + C::kM * MT - 1) / (C::kM * MT);  // tile groups per sequence, at most

@@ -405,16 +405,14 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, B, G>::kThreads)
 template <typename T, int D, int B, int G>
 cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t st) {
     using C = DecodeCfg<T, D, B, G>;
-    static bool configured[64] = {};  // per device; the attribute call is idempotent
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static std::atomic<int> configured[kMaxLaunchDevices];
+    int one = 0;
+    cudaError_t e = per_device_value(configured, &one, [](int, int *v) {
+        *v = 1;
+        return cudaFuncSetAttribute(decode_partition_kernel<T, D, B, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)C::kSmem);
+    });
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(decode_partition_kernel<T, D, B, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)C::kSmem);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) configured[dev] = true;
-    }
     dim3 grid((unsigned)(a.S * a.Hkv), (unsigned)a.max_parts);
     decode_partition_kernel<T, D, B, G><<<grid, C::kThreads, C::kSmem, st>>>(a);
     return cudaGetLastError();

@@ -447,15 +447,10 @@ __global__ void __launch_bounds__(MmaCfg<D, HG>::kThreads, 2)
 template <typename T, int D, int B, int HG>
 cudaError_t decode_mma_grid(int *grid) {
     using C = MmaCfg<D, HG>;
-    static bool configured[64] = {};
-    static int grid_for[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        e = cudaFuncSetAttribute(decode_mma_kernel<T, D, B, HG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)C::kSmem);
+    static std::atomic<int> grid_for[kMaxLaunchDevices];
+    return per_device_value(grid_for, grid, [](int dev, int *v) {
+        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<T, D, B, HG>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
         if (e != cudaSuccess) return e;
         int sms = 0, per_sm = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -463,11 +458,9 @@ cudaError_t decode_mma_grid(int *grid) {
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_mma_kernel<T, D, B, HG>, C::kThreads,
                                                           C::kSmem);
         if (e != cudaSuccess) return e;
-        grid_for[dev] = sms * (per_sm > 0 ? per_sm : 1);
-        configured[dev] = true;
-    }
-    *grid = grid_for[dev];
-    return cudaSuccess;
+        *v = sms * (per_sm > 0 ? per_sm : 1);
+        return cudaSuccess;
+    });
 }
 
 template <typename T, int D, int B, int HG>

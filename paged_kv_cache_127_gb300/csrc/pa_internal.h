@@ -4,11 +4,33 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <cstdint>
 
 #include "../../include/pa.h"
 
 namespace pa {
+
+// A launch constant of the current device (a grid size; 1 for "attributes
+// set"), computed by compute(dev, &value) on the first launch there and cached.
+// Host threads that race on a first launch compute and store the same value.
+constexpr int kMaxLaunchDevices = 64;
+template <typename Compute>
+cudaError_t per_device_value(std::atomic<int> (&cache)[kMaxLaunchDevices], int *value, Compute compute) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxLaunchDevices) return cudaErrorInvalidDevice;
+    int v = cache[dev].load(std::memory_order_acquire);
+    if (v == 0) {
+        e = compute(dev, &v);
+        if (e != cudaSuccess) return e;
+        cache[dev].store(v, std::memory_order_release);
+    }
+    *value = v;
+    return cudaSuccess;
+}
 
 // Everything a decode launch needs, already validated by the entry point.
 struct DecodeArgs {
