@@ -327,6 +327,19 @@ PA_API int32_t pa_device_errors(uint32_t *flags, int32_t clear);
 /* Library version string, e.g. "pa 0.1.0 sm_103a". */
 PA_API const char *pa_version(void);
 
+/*
+ * pa_selftest_bounded_wait -- a check of the kernels' failure path; the pages
+ * have no counterpart.  Every wait of the library's kernels on an mbarrier
+ * gives up after a bounded number of polls, records PA_DEVERR_TIMEOUT and
+ * returns.  This runs that wait, `limit` polls (1 .. 2^20), on an mbarrier
+ * nothing ever arrives at, in one kernel on `stream`, and writes the outcome
+ * to *status (device uint32): PA_DEVERR_TIMEOUT when the wait gave up, 0 if
+ * it was satisfied.  No fault and no hang: each poll is bounded in time by the
+ * hardware.  Returns PA_OK, PA_ERR_INVALID (null status, limit out of range)
+ * or PA_ERR_CUDA (launch error).
+ */
+PA_API int32_t pa_selftest_bounded_wait(uint32_t limit, uint32_t *status, void *stream);
+
 /* ------------------------------------------------------- host block allocator
  *
  * A pool of N physical blocks of B slots with a FIFO free list, a reference

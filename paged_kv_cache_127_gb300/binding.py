@@ -66,6 +66,7 @@ _SIGNATURES = {
     "pa_step_graph_destroy": (None, [_vp]),
     "pa_device_errors": (_i32, [_vp, _i32]),
     "pa_version": (ctypes.c_char_p, []),
+    "pa_selftest_bounded_wait": (_i32, [ctypes.c_uint32, _vp, _vp]),
     "pa_pool_create": (_vp, [_i32, _i32, _vp]),
     "pa_pool_destroy": (None, [_vp]),
     "pa_seq_create": (_i32, [_vp]),
@@ -427,6 +428,16 @@ def pa_device_errors(clear: bool = True) -> int:
 
 def pa_version() -> str:
     return lib.pa_version().decode()
+
+
+def pa_selftest_bounded_wait(limit, status, stream=None) -> None:
+    """Run the kernels' bounded mbarrier wait on a barrier nothing arrives at;
+    `status` (a one-element uint32/int32 CUDA tensor) receives PA_DEVERR_TIMEOUT
+    when the wait gives up."""
+    if status.numel() < 1 or status.element_size() != 4 or not status.is_cuda:
+        raise ValueError("status must be a 4-byte CUDA tensor")
+    _check(lib.pa_selftest_bounded_wait(int(limit), status.data_ptr(), _stream_ptr(stream, status.device)),
+           "pa_selftest_bounded_wait")
 
 
 # ------------------------------------------------------------------ host allocator
