@@ -95,6 +95,23 @@ def test_refcount_teardown():
     assert (p0 in bm.free) == g["freed_after_b"]
 
 
+
+def test_freed_blocks_rejoin_the_back_of_the_free_list():
+    # the pages leave the choice of free block open ("Growing a request" hands out
+    # P11); the reading taken is a FIFO list: a freed block is handed out again only
+    # after every block that was already free
+    bm = BlockManager(4, 16)
+    a, b = bm.create(), bm.create()
+    bm.append(a, 16)
+    bm.append(b, 16)
+    assert (bm.table(a), bm.table(b)) == ([0], [1])
+    bm.free_seq(a)
+    assert list(bm.free) == [2, 3, 0]
+    c = bm.create()
+    bm.append(c, 48)
+    assert bm.table(c) == [2, 3, 0]
+
+
 def test_out_of_blocks_changes_nothing():
     bm = BlockManager(3, 4)
     a = bm.create()

@@ -74,6 +74,19 @@ def test_waste_below_one_block_and_eta_bound():
             assert bk.eta_paged([L], B) >= bk.eta_paged_lower_bound(L, B)
 
 
+def test_eta_bound_closed_forms():
+    # one-slot blocks waste nothing: the bound is exactly 1
+    for L in (1, 7, 300):
+        assert bk.eta_paged_lower_bound(L, 1) == 1 == bk.eta_paged([L], 1)
+    # a sequence one token into its last block wastes the full B - 1 slots, so
+    # eta = L / (L + B - 1), and L / (L + B - 1) - (1 - (B - 1) / L) = (B - 1)^2 / (L (L + B - 1))
+    for B in (2, 16, 64):
+        for k in (0, 1, 5, 40):
+            L = k * B + 1
+            gap = bk.eta_paged([L], B) - bk.eta_paged_lower_bound(L, B)
+            assert gap == Fraction((B - 1) ** 2, L * (L + B - 1))
+
+
 def test_pool_slots_and_naive_reservation_do_not_fit():
     g = _load("block_tables.json")["pool"]
     assert g["num_blocks"] * g["block_size"] == g["pool_slots"]

@@ -30,6 +30,8 @@ def test_a_repeated_prompt_reuses_its_whole_blocks(case):
     _serve(bm, cache, prompt, 90)
     assert len(cache.match(prompt + [7] * 90)) == case["full_blocks"]
     assert len(cache.match(prompt)) * B == case["tokens"]
+    # the partly filled last prompt block is not cached at all
+    assert cache.cached_blocks() == case["full_blocks"]
 
 
 def test_q5_shared_prompt_block_count():
@@ -80,3 +82,15 @@ def test_lru_leaf_goes_first_and_running_requests_are_protected():
     assert len(cache.match(a)) == 1 and len(cache.match(b)) == 3
     assert cache.evict(10) == 4 and cache.cached_blocks() == 0
     assert bm.num_free() == 40
+
+
+def test_a_lookup_counts_as_a_use():
+    # least recently *used*: a prompt looked up after another one was cached is the newer
+    bm = BlockManager(20, 4)
+    cache = PrefixCache(bm)
+    a, b = list(range(100, 108)), list(range(200, 208))
+    bm.free_seq(_serve(bm, cache, a, 0))
+    bm.free_seq(_serve(bm, cache, b, 0))
+    cache.match(a)
+    assert cache.evict(1) == 1
+    assert len(cache.match(a)) == 2 and len(cache.match(b)) == 1
