@@ -95,6 +95,8 @@ def test_decode_rejects_bad_arguments_on_the_host(pa):
     # needs a workspace but none is given
     assert _decode_status(pa, partition_size=32) == pa.PA_ERR_INVALID
     assert _decode_status(pa) == pa.PA_ERR_INVALID
+    assert _decode_status(pa, num_seqs=0) == pa.PA_OK             # nothing to do
+    assert _decode_status(pa, num_seqs=-1) == pa.PA_ERR_INVALID
     d = pa.make_dims(num_seqs=1, num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
                      num_blocks=8, max_blocks_per_seq=4)
     assert pa.lib.pa_decode(ctypes.byref(d), None, None, None, None, None, 1.0, None, None, 0,

@@ -188,6 +188,31 @@ def _sample(lens, k, rng):
     return np.array(sorted(picks))
 
 
+@pytest.mark.parametrize("dtype", synth.DTYPES)
+@pytest.mark.parametrize("B", [16, 32])
+def test_decode_contexts_that_fill_the_whole_table(gpu, dtype, B):
+    # the longest context a table row allows (max_blocks_per_seq * B tokens, no
+    # spare column) next to shorter ones, with partitions of one block up to one
+    # partition for the whole row
+    torch, pa = gpu
+    rng = synth.make_rng(4242 + B + 17 * synth.DTYPES.index(dtype))
+    Hkv, G, D, mb = 2, 4, 128, 40
+    lens = np.array([mb * B, 1, mb * B - 1, mb * B, B + 3], dtype=np.int32)
+    N = int(synth.blocks_needed(lens, B).sum()) + 2
+    tables, _ = synth.scattered_tables(rng, lens, B, N, shuffle=True, max_blocks=mb)
+    assert tables.shape == (len(lens), mb) and (tables[lens == mb * B] >= 0).all()
+    K = [synth.normal(rng, (int(n), Hkv, D), 1.0, dtype) for n in lens]
+    V = [synth.normal(rng, (int(n), Hkv, D), 1.0, dtype) for n in lens]
+    q = synth.normal(rng, (len(lens), G * Hkv, D), 1.0, dtype)
+    kc, vc = scatter(K, tables, B, N, dtype), scatter(V, tables, B, N, dtype)
+    scale = 1.0 / math.sqrt(D)
+    ref = oracle.decode(q, kc, vc, tables, lens, scale, dtype)
+    for psize in (0, B, 8 * B, mb * B):
+        got = run_decode(torch, pa, dtype, q, kc, vc, tables, lens, scale, psize)
+        assert_attention_close(got, ref)
+    _check_no_device_errors(pa)
+
+
 @pytest.mark.parametrize("name", ["mha7b", "gqa8b_b16", "gqa8b_b32", "long70b"])
 def test_full_size_workloads_on_sampled_sequences(gpu, name):
     """The bench's own step (allocator tables, write then decode) at full size; the
