@@ -190,3 +190,10 @@ def test_context_longer_than_table_is_rejected():
     kc = np.zeros((2, 1, 4, 4), np.float32)
     with pytest.raises(ValueError):
         oracle.decode(q, kc, kc, np.array([[0]], np.int32), np.array([5], np.int32), 1.0, "f32")
+
+
+def test_query_heads_must_be_a_multiple_of_kv_heads():
+    q = np.zeros((1, 3, 4), np.float32)
+    kc = np.zeros((2, 2, 4, 4), np.float32)
+    with pytest.raises(ValueError):
+        oracle.decode(q, kc, kc, np.array([[0]], np.int32), np.array([2], np.int32), 1.0, "f32")

@@ -29,6 +29,19 @@ def test_three_requests_tables_and_free_count():
     assert bm.num_free() == g["free_after"]
 
 
+def test_pool_statistics_of_the_three_requests():
+    # "Where contiguous allocation wastes space": 25, 47 and 12 tokens take 96 slots
+    # in 16-token blocks, 12 of them padding; a fork shares every block of its parent
+    f = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "fragmentation.json")))["cases"][0]
+    g, bm, seqs = _pool_example()
+    st = bm.stats()
+    assert (st["tokens"], st["table_slots"], st["padded_slots"]) == (f["tokens"], f["paged_slots"], f["paged_waste"])
+    assert (st["used"], st["shared"], st["free"]) == (sum(f["blocks"]), 0, g["free_after"])
+    bm.fork(seqs[1])
+    st = bm.stats()
+    assert (st["used"], st["shared"]) == (sum(f["blocks"]), f["blocks"][1])
+
+
 def test_growth_adds_one_block_and_keeps_entries():
     g, bm, seqs = _pool_example()
     s = seqs[g["grow_seq"]]
@@ -110,6 +123,35 @@ def test_freed_blocks_rejoin_the_back_of_the_free_list():
     c = bm.create()
     bm.append(c, 48)
     assert bm.table(c) == [2, 3, 0]
+
+
+def test_appending_nothing_changes_nothing():
+    # zero new tokens write no slot, so even a shared, partly filled last block is
+    # not copied; a negative count is refused
+    bm = BlockManager(8, 16)
+    a = bm.create()
+    bm.append(a, 24)
+    b = bm.fork(a)
+    snap = (bm.table(a), bm.table(b), list(bm.free), list(bm.ref))
+    assert bm.append(b, 0) == ([], [])
+    assert (bm.table(a), bm.table(b), list(bm.free), list(bm.ref)) == snap
+    with pytest.raises(ValueError):
+        bm.append(b, -1)
+    assert (bm.table(a), bm.table(b), list(bm.free), list(bm.ref)) == snap
+
+
+def test_fault_injection_counts_down():
+    # after set_fail_after(2) exactly two more block allocations succeed
+    bm = BlockManager(8, 16)
+    a = bm.create()
+    bm.set_fail_after(2)
+    bm.append(a, 32)
+    with pytest.raises(OutOfBlocks):
+        bm.append(a, 1)
+    assert bm.length(a) == 32 and bm.num_free() == 6
+    bm.set_fail_after(None)
+    bm.append(a, 1)
+    assert bm.num_free() == 5
 
 
 def test_out_of_blocks_changes_nothing():

@@ -29,6 +29,13 @@ def test_slot_mapping_enumerates_every_slot_of_a_table_once():
     assert slots.tolist() == expect
     neg = oracle.slot_mapping(table, B, np.zeros(2, np.int32), np.array([-1, 3], np.int32))
     assert neg.tolist() == [-1, 6 * B + 3]
+    # a position past the table's last block, and a negative position asked of one
+    # table row, are refused
+    two = np.array([[6, 1, 4, 0], [2, 3, 5, 7]], dtype=np.int32)
+    with pytest.raises(ValueError):
+        oracle.slot_mapping(two, B, np.zeros(1, np.int32), np.array([4 * B], np.int32))
+    with pytest.raises(ValueError):
+        oracle.slot(table[0], B, -1)
 
 
 @pytest.mark.parametrize("dtype", synth.DTYPES)
@@ -87,8 +94,9 @@ def test_copy_blocks_copies_whole_blocks_only(dtype):
     others = [b for b in range(N) if b not in (7, 9, 11)]
     assert kc[others].tobytes() == k0[others].tobytes()
     assert vc[others].tobytes() == v0[others].tobytes()
-    with pytest.raises(ValueError):
-        oracle.copy_blocks(kc, vc, np.array([[0, N]]), dtype)
+    for bad in ([0, N], [N, 0], [-1, 0], [0, -1]):
+        with pytest.raises(ValueError):
+            oracle.copy_blocks(kc, vc, np.array([bad]), dtype)
 
 
 @pytest.mark.parametrize("dtype", synth.DTYPES)

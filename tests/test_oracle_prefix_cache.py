@@ -94,3 +94,35 @@ def test_a_lookup_counts_as_a_use():
     cache.match(a)
     assert cache.evict(1) == 1
     assert len(cache.match(a)) == 2 and len(cache.match(b)) == 1
+
+
+def test_insert_refuses_free_and_repeated_blocks():
+    # a cached block holds the K/V of one prefix, and only allocated blocks can be cached
+    bm = BlockManager(8, 4)
+    cache = PrefixCache(bm)
+    s = bm.create()
+    bm.append(s, 8)
+    b0, b1 = bm.table(s)
+    toks = list(range(8))
+    free_block = next(b for b in range(8) if bm.refcount(b) == 0)
+    with pytest.raises(IndexError):
+        cache.insert(toks, [b0, free_block])
+    with pytest.raises(ValueError):
+        cache.insert(toks, [b0, b0])
+    assert cache.cached_blocks() == 0 and (bm.refcount(b0), bm.refcount(b1)) == (1, 1)
+    assert cache.insert(toks, [b0, b1]) == 2 and (bm.refcount(b0), bm.refcount(b1)) == (2, 2)
+
+
+def test_a_sequence_started_from_a_prefix_holds_its_blocks():
+    bm = BlockManager(8, 4)
+    cache = PrefixCache(bm)
+    s = bm.create()
+    bm.append(s, 8)
+    cache.insert(list(range(8)), bm.table(s))
+    bm.free_seq(s)
+    blocks = cache.match(list(range(10)))
+    t = create_from_prefix(bm, blocks)
+    assert bm.length(t) == 8 and [bm.refcount(b) for b in blocks] == [2, 2]
+    assert cache.evict(2) == 0           # held by the new sequence
+    bm.free_seq(t)
+    assert [bm.refcount(b) for b in blocks] == [1, 1] and cache.evict(2) == 2

@@ -99,6 +99,40 @@ MUTANTS = [
      "bookkeeping: fragmentation over tokens"),
     (BK, "private = blocks_for(suffix, block_size)", "private = blocks_for(prompt % block_size + suffix, block_size)",
      "bookkeeping: shared partial block also stored per request"),
+    (BK, '"reduction": Fraction(naive, paged)', '"reduction": Fraction(paged, naive)', "bookkeeping: reduction inverted"),
+    (BK, "naive = max_len * len(lengths)", "naive = max_len * len(lengths) + 1", "bookkeeping: reserved slots off by one"),
+    (BK, "without = per_req_unshared * requests", "without = per_req_unshared * requests - 1",
+     "bookkeeping: unshared total off by one"),
+    (BK, "return Fraction(tokens, slots) if slots else Fraction(1)",
+     "return Fraction(tokens, slots + 1) if slots else Fraction(1)", "bookkeeping: utilisation over one slot too many"),
+    (BK, "return prompt // block_size", "return -(-prompt // block_size)", "bookkeeping: partial block counted as shareable"),
+    # refusals and the less travelled paths (each mutant stays inside its buffers
+    # on the inputs the pins give it)
+    (C, "if (Hq % Hkv != 0 || dtype < 0 || dtype > 2)", "if (dtype < 0 || dtype > 2)",
+     "oracle: query heads not a multiple of KV heads accepted"),
+    (C, "if (positions[t] / B >= max_blocks)\n            return -1;", "if (positions[t] / B > max_blocks)\n            return -1;",
+     "slot mapping: position past the table accepted"),
+    (C, "if (B <= 0 || pos < 0)\n        return -1;", "if (B <= 0)\n        return -1;", "slot: negative position accepted"),
+    (C, "if (n < 0 || n > lens[s])", "if (n < 0)", "chunk: more queries than context accepted"),
+    (BM, "self.seqs[sid].length = p.length", "self.seqs[sid].length = 0", "allocator: fork starts empty"),
+    (BM, "if n < 0:\n            raise ValueError", "if n < -1:\n            raise ValueError", "allocator: negative append accepted"),
+    (BM, "cow = n > 0 and s.length % B != 0", "cow = s.length % B != 0", "allocator: empty append copies on write"),
+    (BM, "shared = sum(1 for r in self.ref if r > 1)", "shared = sum(1 for r in self.ref if r >= 1)",
+     "allocator: used blocks counted as shared"),
+    (BM, "\"padded_slots\": slots - tokens}", "\"padded_slots\": slots}", "allocator: padding counted as all slots"),
+    (BM, "        self.seqs[sid].length = hs.length\n        host.free_seq(hid)\n", "        self.seqs[sid].length = hs.length\n",
+     "swap in: host blocks kept"),
+    (BM, "if len(s.table) > len(host.free)", "if len(s.table) > len(host.free) + 1", "swap out: host pool overdrawn"),
+    (BM, "        if self._fail_budget is not None:\n            self._fail_budget -= 1\n", "",
+     "allocator: injected failure never comes"),
+    (PC, "if len(set(new)) != len(new) or any(b in held for b in new):", "if any(b in held for b in new):",
+     "prefix cache: one block cached under two prefixes"),
+    (PC, "or self.bm.ref[int(b)] < 1 for b in blocks[:m]", "for b in blocks[:m]", "prefix cache: free block cached"),
+    (PC, "self.bm.ref[int(blocks[k - 1])] += 1\n                added += 1", "added += 1",
+     "prefix cache: cache takes no reference"),
+    (PC, "bm.seqs[sid].length = len(blocks) * bm.B", "bm.seqs[sid].length = len(blocks) * bm.B - 1",
+     "prefix cache: sequence from a prefix one token short"),
+    (PC, "    for b in blocks:\n        bm.ref[int(b)] += 1\n", "", "prefix cache: sequence from a prefix takes no references"),
 ]
 
 # Loads the oracle copy given as argv[1] before pytest can put the repository
