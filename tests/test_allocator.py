@@ -127,6 +127,33 @@ def test_bad_ids_and_arguments(pa):
         with pytest.raises(pa.PaError) as e:
             pa.pa_seq_append_batch(p.handle, [s2, s2], 1)
         assert e.value.status == pa.PA_ERR_INVALID
+        with pytest.raises(pa.PaError) as e:
+            pa.pa_seq_append_batch(p.handle, [s2, s], 1)   # s was freed
+        assert e.value.status == pa.PA_ERR_BAD_INDEX
+        assert pa.pa_seq_len(p.handle, s2) == 0 and pa.pa_pool_num_free(p.handle) == 4
+        pa.pa_seq_append(p.handle, s2, 20)
+        with pytest.raises(pa.PaError) as e:
+            pa.pa_pool_export(p.handle, [s2], 1)            # two blocks do not fit one column
+        assert e.value.status == pa.PA_ERR_INVALID
+
+
+def test_batch_counts_a_copy_that_spares_the_next_sharer(pa):
+    # two sequences share a partly filled block and both append in one batch: the
+    # first copies it, after which the second holds it alone and writes in place,
+    # so one free block is enough (the model, appending one after the other, agrees)
+    bm = BlockManager(3, 16)
+    a = bm.create()
+    bm.append(a, 24)
+    b = bm.fork(a)
+    want = [bm.append(a, 1), bm.append(b, 1)]
+    with pa.Pool(3, 16) as p:
+        pa_a = pa.pa_seq_create(p.handle)
+        pa.pa_seq_append(p.handle, pa_a, 24)
+        pa_b = pa.pa_seq_fork(p.handle, pa_a)
+        slots, pairs = pa.pa_seq_append_batch(p.handle, [pa_a, pa_b], 1)
+        assert slots.tolist() == [w[0] for w in want]
+        assert [tuple(x) for x in pairs.tolist()] == want[0][1] + want[1][1]
+        assert pa.pa_pool_num_free(p.handle) == bm.num_free() == 0
 
 
 def _run_stream(pa, seed, num_blocks, B, steps, batch):
@@ -211,12 +238,18 @@ def _run_stream(pa, seed, num_blocks, B, steps, batch):
             assert pa.pa_seq_table(p.handle, s).tolist() == bm.table(s)
             assert pa.pa_seq_len(p.handle, s) == bm.length(s)
         assert pa.pa_pool_num_free(p.handle) == bm.num_free()
+        if live and ops % 50 == 0:
+            width = max(len(bm.table(s)) for s in live) + 2
+            tables, lens = pa.pa_pool_export(p.handle, live, width, pad=-7)
+            assert tables.tolist() == [bm.table(s) + [-7] * (width - len(bm.table(s))) for s in live]
+            assert lens.tolist() == [bm.length(s) for s in live]
     for blk in range(num_blocks):
         assert pa.pa_block_refcount(p.handle, blk) == bm.refcount(blk)
     st = pa.pa_pool_get_stats(p.handle)
     ref = bm.stats()
     for k in ("free", "used", "shared", "cow_copies", "tokens", "table_slots", "padded_slots"):
         assert st[{"free": "free_blocks", "used": "used_blocks", "shared": "shared_blocks"}.get(k, k)] == ref[k]
+    assert st["live_seqs"] == len(bm.seqs) == len(live)
     p.close()
     return ops
 

@@ -116,3 +116,102 @@ def test_a_block_is_cached_under_one_prefix_only(pa):
         assert pa.pa_prefix_evict(c, 5) == model.evict(5) == 2
         assert pa.pa_pool_num_free(p.handle) == bm.num_free() == 8
         pa.pa_prefix_cache_destroy(c)
+
+
+class _Twin:
+    """The C++ pool and cache driven in lockstep with the block manager and cache models."""
+
+    def __init__(self, pa, num_blocks, B):
+        self.pa = pa
+        self.pool = pa.Pool(num_blocks, B)
+        self.cache = pa.pa_prefix_cache_create(self.pool.handle)
+        self.bm = BlockManager(num_blocks, B)
+        self.model = PrefixCache(self.bm)
+
+    def serve(self, toks):
+        """A request: reuse the cached prefix, store the rest; returns (sequence, blocks)."""
+        got = self.pa.pa_prefix_match(self.cache, toks).tolist()
+        assert got == self.model.match(toks)
+        sid = self.pa.pa_seq_create_from_prefix(self.pool.handle, got)
+        assert sid == create_from_prefix(self.bm, got)
+        self.pa.pa_seq_append(self.pool.handle, sid, len(toks) - len(got) * self.bm.B)
+        self.bm.append(sid, len(toks) - len(got) * self.bm.B)
+        blocks = self.pa.pa_seq_table(self.pool.handle, sid).tolist()
+        assert blocks == self.bm.table(sid)
+        return sid, blocks
+
+    def insert(self, toks, blocks):
+        got = self.pa.pa_prefix_insert(self.cache, toks, blocks)
+        assert got == self.model.insert(toks, blocks)
+        return got
+
+    def free(self, sid):
+        self.pa.pa_seq_free(self.pool.handle, sid)
+        self.bm.free_seq(sid)
+
+    def evict(self, n):
+        got = self.pa.pa_prefix_evict(self.cache, n)
+        assert got == self.model.evict(n)
+        return got
+
+    def match(self, toks):
+        got = self.pa.pa_prefix_match(self.cache, toks).tolist()
+        assert got == self.model.match(toks)
+        return got
+
+    def close(self):
+        self.pa.pa_prefix_cache_destroy(self.cache)
+        self.pool.close()
+
+
+def test_reinserting_a_prompt_makes_it_recent(pa):
+    # an insert stamps the prefixes it finds cached as well as the ones it adds
+    t = _Twin(pa, 8, 2)
+    p, q = [1, 1, 2, 2], [7, 7]
+    s, bp = t.serve(p)
+    t.insert(p, bp)
+    t.free(s)
+    s, bq = t.serve(q)
+    t.insert(q, bq)
+    t.free(s)
+    assert t.insert(p, bp) == 0                 # nothing new: only stamps
+    assert t.evict(1) == 1
+    assert t.match(q) == [] and t.match(p) == bp
+    t.close()
+
+
+def test_an_edge_split_keeps_the_stamps_of_its_upper_part(pa):
+    # the shared first block of two prompts keeps the stamp of its last use when the
+    # edge holding it is split, and is evicted after an older, once-held prompt
+    t = _Twin(pa, 10, 2)
+    held, bh = t.serve([5, 5])
+    t.insert([5, 5], bh)
+    s, b1 = t.serve([1, 1, 2, 2])
+    t.insert([1, 1, 2, 2], b1)
+    t.free(s)
+    s, b2 = t.serve([1, 1, 3, 3])                # shares b1[0]; its insert splits the edge
+    assert b2[0] == b1[0]
+    t.insert([1, 1, 3, 3], b2)
+    t.free(s)
+    assert t.evict(2) == 2                      # the two tails; [5, 5] is still held
+    t.free(held)
+    assert t.evict(1) == 1                      # the older prompt goes, the shared block stays
+    assert t.match([5, 5]) == [] and t.match([1, 1]) == [b1[0]]
+    t.close()
+
+
+def test_a_refused_insert_leaves_no_trace(pa):
+    # an insert refused because one of its blocks is cached elsewhere changes nothing:
+    # the same prefix with a proper block is accepted afterwards
+    t = _Twin(pa, 8, 2)
+    sq, bq = t.serve([9, 9])
+    t.insert([9, 9], bq)
+    sa, ba = t.serve([1, 1, 2, 2])
+    with pytest.raises(pa.PaError):
+        pa.pa_prefix_insert(t.cache, [1, 1, 2, 2], [ba[0], bq[0]])
+    with pytest.raises(ValueError):
+        t.model.insert([1, 1, 2, 2], [ba[0], bq[0]])
+    assert t.insert([1, 1, 2, 2], ba) == 2
+    t.free(sq)
+    t.free(sa)
+    t.close()
