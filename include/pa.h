@@ -413,6 +413,21 @@ PA_API int32_t pa_seq_append(pa_pool *pool, int32_t seq, int32_t n_tokens, int64
 PA_API int32_t pa_seq_append_batch(pa_pool *pool, const int32_t *seqs, int32_t n, int32_t tokens_each,
                             int64_t *slots_out, int64_t *cow_pairs_out, int32_t *n_cow);
 
+/*
+ * pa_copy_pairs_check -- host check of copy-on-write pairs before they go to
+ * pa_copy_blocks, which reads its pairs on the device and cannot check them.
+ * A copy-on-write copy goes to a fresh block ("PagedAttention: Virtual Memory
+ * for the KV Cache", "Sharing a prefix and copying a partial block"), so a
+ * valid list has every id in [0, num_blocks), no destination twice, and no
+ * destination that is also a source (several pairs may share a source).
+ *   pairs  host int64 [num_pairs, 2] (src, dst); may be NULL if num_pairs == 0
+ * Returns PA_OK, PA_ERR_BAD_INDEX (an id out of range) or PA_ERR_INVALID (a
+ * repeated destination, a destination that is a source, num_pairs < 0,
+ * num_blocks <= 0, NULL pairs).  The pairs pa_seq_append and
+ * pa_seq_append_batch emit always pass.
+ */
+PA_API int32_t pa_copy_pairs_check(const int64_t *pairs, int32_t num_pairs, int32_t num_blocks);
+
 /* Release a sequence: each of its blocks' counts drops by one; blocks reaching
  * zero go to the back of the free list, in table order. */
 PA_API int32_t pa_seq_free(pa_pool *pool, int32_t seq);

@@ -81,6 +81,7 @@ _SIGNATURES = {
     "pa_block_refcount": (_i32, [_vp, _i32]),
     "pa_pool_get_stats": (_i32, [_vp, _vp]),
     "pa_pool_set_fail_after": (_i32, [_vp, _i32]),
+    "pa_copy_pairs_check": (_i32, [_vp, _i32, _i32]),
     "pa_swap_blocks": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i64, _i64, _vp, _i32, _i32, _vp]),
     "pa_seq_swap_out": (_i32, [_vp, _vp, _i32, _vp, _vp, _vp]),
     "pa_seq_swap_in": (_i32, [_vp, _vp, _i32, _vp, _vp, _vp]),
@@ -543,6 +544,13 @@ def pa_pool_get_stats(pool) -> dict:
 
 def pa_pool_set_fail_after(pool, n) -> None:
     _check(lib.pa_pool_set_fail_after(pool, -1 if n is None else int(n)), "pa_pool_set_fail_after")
+
+
+def pa_copy_pairs_check(pairs, num_blocks: int) -> None:
+    """Raise PaError unless the host (src, dst) pairs are a valid copy-on-write list."""
+    pairs = np.ascontiguousarray(np.asarray(pairs, dtype=np.int64).reshape(-1, 2))
+    _check(lib.pa_copy_pairs_check(_np_ptr(pairs) if pairs.size else None, pairs.shape[0], num_blocks),
+           "pa_copy_pairs_check")
 
 
 def _neg(r: int, what: str) -> int:

@@ -319,6 +319,26 @@ int32_t pa_seq_swap_in(pa_pool *dev, pa_pool *host, int32_t host_seq, int32_t *d
     return PA_OK;
 }
 
+int32_t pa_copy_pairs_check(const int64_t *pairs, int32_t num_pairs, int32_t num_blocks) {
+    if (num_pairs < 0 || num_blocks <= 0 || (num_pairs > 0 && !pairs)) return PA_ERR_INVALID;
+    std::vector<int64_t> dst;
+    try {
+        dst.reserve((size_t)num_pairs);
+    } catch (const std::bad_alloc &) {
+        return PA_ERR_OOM;
+    }
+    for (int32_t i = 0; i < num_pairs; ++i) {
+        const int64_t s = pairs[2 * i], d = pairs[2 * i + 1];
+        if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) return PA_ERR_BAD_INDEX;
+        dst.push_back(d);
+    }
+    std::sort(dst.begin(), dst.end());
+    if (std::adjacent_find(dst.begin(), dst.end()) != dst.end()) return PA_ERR_INVALID;
+    for (int32_t i = 0; i < num_pairs; ++i)
+        if (std::binary_search(dst.begin(), dst.end(), pairs[2 * i])) return PA_ERR_INVALID;
+    return PA_OK;
+}
+
 int32_t pa_pool_set_fail_after(pa_pool *pool, int32_t n) {
     if (!pool) return PA_ERR_INVALID;
     pool->fail_budget = n < 0 ? -1 : n;

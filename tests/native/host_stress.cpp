@@ -224,6 +224,8 @@ void op_batch(World &w, Rng &r) {
     CHECK(rc == PA_OK, "batch append returned %d", rc);
     if (rc != PA_OK) return;
     CHECK(n_cow >= 0 && n_cow <= (int32_t)ids.size(), "batch n_cow %d", n_cow);
+    CHECK(pa_copy_pairs_check(pairs.data(), n_cow, w.N) == PA_OK,
+          "batch copy pairs fail the host check");
     for (size_t k = 0; k < pick.size(); ++k) {
         Seq &s = w.live[pick[k]];
         const std::vector<int32_t> extra = random_tokens(r, each);

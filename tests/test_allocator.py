@@ -137,6 +137,24 @@ def test_bad_ids_and_arguments(pa):
         assert e.value.status == pa.PA_ERR_INVALID
 
 
+def test_copy_pairs_check(pa):
+    # a copy-on-write copy goes to a fresh block: ids in range, destinations distinct
+    # and never a source; several copies may read one source
+    pa.pa_copy_pairs_check([[3, 7], [3, 9], [0, 11]], 12)
+    pa.pa_copy_pairs_check(np.zeros((0, 2), np.int64), 12)
+    for bad, status in (([[3, 7], [4, 7]], pa.PA_ERR_INVALID),     # destination twice
+                        ([[3, 7], [7, 9]], pa.PA_ERR_INVALID),     # a destination is also a source
+                        ([[5, 5]], pa.PA_ERR_INVALID),
+                        ([[3, 12]], pa.PA_ERR_BAD_INDEX),
+                        ([[-1, 2]], pa.PA_ERR_BAD_INDEX)):
+        with pytest.raises(pa.PaError) as e:
+            pa.pa_copy_pairs_check(bad, 12)
+        assert e.value.status == status
+    assert pa.lib.pa_copy_pairs_check(None, 1, 12) == pa.PA_ERR_INVALID
+    assert pa.lib.pa_copy_pairs_check(None, -1, 12) == pa.PA_ERR_INVALID
+    assert pa.lib.pa_copy_pairs_check(None, 0, 0) == pa.PA_ERR_INVALID
+
+
 def test_batch_counts_a_copy_that_spares_the_next_sharer(pa):
     # two sequences share a partly filled block and both append in one batch: the
     # first copies it, after which the second holds it alone and writes in place,
@@ -219,6 +237,7 @@ def _run_stream(pa, seed, num_blocks, B, steps, batch):
             if ok:
                 assert slots.tolist() == want_slots
                 assert [tuple(x) for x in pairs.tolist()] == want_pairs
+                pa.pa_copy_pairs_check(pairs, num_blocks)
         else:
             s = live[int(rng.integers(len(live)))]
             n = int(rng.integers(0, 2 * B + 3))
