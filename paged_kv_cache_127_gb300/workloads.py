@@ -159,6 +159,7 @@ def build_step(name: str, seed: int = 0, values: bool = True, binding=None) -> D
             binding.pa_seq_append(h, s, int(n) - w.query_len)   # the context already cached
             seqs.append(s)
     slots, pairs = binding.pa_seq_append_batch(h, seqs, w.query_len)   # this step's new tokens
+    binding.pa_copy_pairs_check(pairs, N)   # pa_copy_blocks' precondition, on the host copy
     tables, lens = binding.pa_pool_export(h, seqs, max_blocks, -1)
     pool.close()
 
