@@ -271,7 +271,9 @@ PA_API int32_t pa_copy_blocks_layers(const pa_dims *dims, void *k_caches, void *
  *     q        + l * q_layer_stride          [S, Hq, D]
  *     k_new    + l * kv_new_layer_stride     [num_tokens, Hkv, D] (and v_new)
  *     out      + l * out_layer_stride        [S, Hq, D] fp32
- * (strides in bytes; out_layer_stride a multiple of 16); slot_mapping, block_tables, context_lens and the
+ * (strides in bytes; out_layer_stride a multiple of 16; with num_layers > 1
+ * each stride at least one layer's tensor, so that layers do not overlap,
+ * else PA_ERR_INVALID); slot_mapping, block_tables, context_lens and the
  * workspace are shared by all layers (layers run in order).  Arguments are
  * validated as by the two calls; on failure NULL is returned and *status
  * (nullable) holds the pa_status.  Copy-on-write copies, which are rare and

@@ -45,6 +45,17 @@ pa_step_graph *pa_step_graph_create(const pa_dims *dims, int32_t num_layers, voi
     if (!dims || num_layers <= 0 || cache_layer_stride < 0 || q_layer_stride < 0 || kv_new_layer_stride < 0 ||
         out_layer_stride < 0)
         return nullptr;
+    if (num_layers > 1) {
+        // layers must not overlap: each stride covers one layer's tensor (sizes in
+        // double, so that absurd dims cannot overflow before they are rejected)
+        const double eb = dims->kv_dtype == PA_F32 ? 4.0 : 2.0;
+        const double row = (double)dims->num_seqs * dims->num_q_heads * dims->head_dim;
+        const double pool = (double)dims->num_blocks * dims->num_kv_heads * dims->block_size * dims->head_dim * eb;
+        const double kv_new = (double)num_tokens * dims->num_kv_heads * dims->head_dim * eb;
+        if ((double)cache_layer_stride < pool || (double)q_layer_stride < row * eb ||
+            (double)kv_new_layer_stride < kv_new || (double)out_layer_stride < row * 4.0)
+            return nullptr;
+    }
     pa_step_graph *g = new (std::nothrow) pa_step_graph();
     if (!g) return nullptr;
     cudaStream_t st = nullptr;

@@ -182,3 +182,22 @@ def test_chunk_rejects_bad_arguments_on_the_host(pa):
     assert status() == pa.PA_ERR_INVALID                        # no workspace
     assert status(T=0) == pa.PA_OK                              # nothing to do
     assert status(num_seqs=0) == pa.PA_OK
+
+
+def test_step_graph_refuses_overlapping_layers_on_the_host(pa):
+    # with several layers every stride must cover one layer's tensor; these are
+    # refused before any CUDA call
+    S, Hq, Hkv, D, B, N, T = 4, 8, 2, 128, 16, 10, 4
+    d = pa.make_dims(num_seqs=S, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, block_size=B, num_blocks=N,
+                     max_blocks_per_seq=4, kv_dtype="bf16")
+    pool, qb, kvb, ob = N * Hkv * B * D * 2, S * Hq * D * 2, T * Hkv * D * 2, S * Hq * D * 4
+    fake = ctypes.c_void_p(0x10000)
+
+    def status(cache=pool, q=qb, kv=kvb, out=ob, layers=2):
+        st = ctypes.c_int32(-1)
+        g = pa.lib.pa_step_graph_create(ctypes.byref(d), layers, fake, fake, cache, fake, q, fake, fake, kv, fake,
+                                        T, fake, fake, 1.0, fake, out, fake, 1 << 20, ctypes.byref(st))
+        assert g is None
+        return st.value
+    for over in (dict(cache=pool - 16), dict(q=qb - 2), dict(kv=kvb - 2), dict(out=ob - 16), dict(layers=0)):
+        assert status(**over) == pa.PA_ERR_INVALID, over
