@@ -88,3 +88,26 @@ def test_prefix_cache_mode_bounds_its_repetitions(monkeypatch):
     line = json.loads(buf.getvalue().strip().splitlines()[-1])
     assert line["steps"] == 5 and line["unit"] == "requests/s" and line["value"] > 0
     assert line["gpu_launches"] == 0
+
+
+
+def test_profiled_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
+    # roofline.traffic comes from an ncu summary only while the kernel sources hash
+    # to the value recorded in it; any edit to them makes it null
+    sys.path.insert(0, ROOT)
+    import bench
+    fake = tmp_path / "repo"
+    (fake / "profiles").mkdir(parents=True)
+    (fake / "paged_kv_cache_127_gb300" / "csrc").mkdir(parents=True)
+    for name in set(bench.KERNEL_SOURCES):
+        data = open(os.path.join(ROOT, "paged_kv_cache_127_gb300", "csrc", name), "rb").read()
+        (fake / "paged_kv_cache_127_gb300" / "csrc" / name).write_bytes(data)
+    monkeypatch.setattr(bench, "ROOT", str(fake))
+    (fake / "profiles" / "decode_w.md").write_text(
+        f"# decode, workload w\n\ntraffic_bytes_per_launch: 123456 sources: {bench.kernel_source_hash()}\n")
+    assert bench.profiled_traffic("w") == 123456
+    assert bench.profiled_traffic("w", "chunk") is None            # no chunk summary for w
+    assert bench.profiled_traffic("no_such_workload") is None
+    edited = fake / "paged_kv_cache_127_gb300" / "csrc" / bench.KERNEL_SOURCES[0]
+    edited.write_bytes(edited.read_bytes() + b"\n// edited\n")
+    assert bench.profiled_traffic("w") is None
