@@ -111,3 +111,29 @@ def test_profiled_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
     edited = fake / "paged_kv_cache_127_gb300" / "csrc" / bench.KERNEL_SOURCES[0]
     edited.write_bytes(edited.read_bytes() + b"\n// edited\n")
     assert bench.profiled_traffic("w") is None
+
+
+def test_clock_sampler_reports_median_clock_and_throttle_reasons(tmp_path, monkeypatch):
+    # a stand-in nvidia-smi prints three samples in the queried column order
+    # (index, sm, max sm, power, active mask, hw, hw thermal, sw thermal, sw power cap)
+    fake = tmp_path / "nvidia-smi"
+    fake.write_text("#!/bin/bash\n"
+                    "printf '0, 2070, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Not Active\\n'\n"
+                    "printf '0, 1965, 2070, 1390.5, 0x4, Not Active, Not Active, Not Active, Active\\n'\n"
+                    "printf '0, 1800, 2070, 1400.0, 0x8, Active, Not Active, Not Active, Active\\n'\n"
+                    "printf '[N/A], [N/A]\\n'\n"
+                    "exec sleep 30\n")
+    fake.chmod(0o755)
+    monkeypatch.setenv("PATH", f"{tmp_path}:{os.environ['PATH']}")
+    sys.path.insert(0, ROOT)
+    import time
+
+    import bench
+    s = bench.ClockSampler(0).start()
+    for _ in range(100):                      # until the three samples are written
+        time.sleep(0.05)
+        if os.path.exists(s.path) and open(s.path).read().count("\n") >= 4:
+            break
+    got = s.stop()
+    assert got == {"sm_mhz": 1965.0, "sm_max_mhz": 2070.0, "reasons": ["hw_slowdown", "sw_power_cap"], "samples": 3}
+    assert not os.path.exists(s.path)
