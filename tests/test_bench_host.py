@@ -137,3 +137,14 @@ def test_clock_sampler_reports_median_clock_and_throttle_reasons(tmp_path, monke
     got = s.stop()
     assert got == {"sm_mhz": 1965.0, "sm_max_mhz": 2070.0, "reasons": ["hw_slowdown", "sw_power_cap"], "samples": 3}
     assert not os.path.exists(s.path)
+
+
+def test_roofline_peaks_come_from_the_measured_file_else_the_fallback(tmp_path, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.measured_hbm_peak() == (6800.0, "fallback")
+    assert bench.measured_bf16_peak() == (1900.0, "fallback")
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6698.2, "bf16_tflops": 1883.0}))
+    assert bench.measured_hbm_peak() == (6698.2, "measured")
+    assert bench.measured_bf16_peak()[0] == 1883.0
