@@ -439,7 +439,6 @@ def run_chunk(args):
     write of every new token followed by pa_chunk_attention over them."""
     import torch
 
-    import oracle
     from paged_kv_cache_127_gb300 import binding as pa
     from paged_kv_cache_127_gb300 import workloads
 
@@ -535,6 +534,8 @@ def run_chunk(args):
         "roofline": roof, "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
+        import oracle  # the CPU-baseline leg only
+
         rng = np.random.default_rng(7)
         order = rng.permutation(step.num_seqs)
         kc, vc = step.k_cache, step.v_cache
