@@ -42,6 +42,8 @@ def test_length_ranges():
     for name in ("gqa8b_b16", "gqa8b_b32"):
         g = synth.workload(name).lengths
         assert g.min() >= 1 and g.max() <= 4096
+        # the lognormal tail reaches past 2048 (P ~ 6 % a sequence): the clip is at 4096, not lower
+        assert (g > 2048).sum() >= 5
     p = synth.workload("prefix_cow")
     assert p.lengths.shape == (128,) and p.lengths.min() >= 1 and p.lengths.max() <= 512
     assert (p.prefix_len, p.prefix_group, p.pair_count, p.pair_prefix) == (800, 128, 32, 24)
@@ -90,6 +92,14 @@ def test_pool_and_placement():
     assert ids.min() >= 0 and ids.max() < N
     assert all((tables[s, n:] == -1).all() for s, n in enumerate(nb))
     assert used.sum() == demand and used[ids].all()
+    # a seeded permutation of the pool, not the blocks in order: another seed places
+    # them differently, and consecutive table entries are rarely consecutive ids
+    steps = np.concatenate([np.diff(tables[s_, :n]) for s_, n in enumerate(nb)])
+    assert np.mean(steps == 1) < 0.05
+    other, _ = synth.scattered_tables(synth.make_rng(60), lens, 16, N)
+    assert not np.array_equal(other, tables)
+    ordered, _ = synth.scattered_tables(rng, lens, 16, N, shuffle=False)
+    assert ordered[0, :nb[0]].tolist() == list(range(nb[0]))
     with pytest.raises(ValueError):
         synth.scattered_tables(rng, lens, 16, demand - 1)
 
