@@ -164,6 +164,36 @@ def test_partitioned_merge_equals_plain_softmax(psize):
     np.testing.assert_allclose(part, plain, rtol=1e-12, atol=1e-14)
 
 
+@pytest.mark.parametrize("psize", [4, 16])
+def test_partitioned_merge_with_extreme_partition_maxima(psize):
+    # The merge weights e^(m_b - m*) stay finite only when m* is the largest m_b and
+    # every m_b is its own partition's maximum.  Two cases, each against the plain
+    # softmax: every logit near -1000 (a partition maximum started at 0 rather than
+    # -inf underflows every weight to 0), and a +1000 spike in the first partition
+    # only (an m* taken from another partition overflows).
+    rng = synth.make_rng(81)
+    n, D, B = 40, 8, 4
+    q = np.zeros((1, 1, D), np.float32)
+    q[0, 0, 0] = 1.0
+    V = rng.standard_normal((n, 1, D)).astype(np.float32)
+    tables = np.array([[3, 0, 7, 5, 9, 1, 2, 6, 8, 4]], np.int32)
+    lens = np.array([n], np.int32)
+    for spike in (False, True):
+        K = (0.25 * rng.standard_normal((n, 1, D))).astype(np.float32)
+        if spike:
+            K[1, 0, 0] = 1000.0
+        else:
+            K[:, 0, 0] -= np.float32(1000.0)
+        kc = scatter([K], tables, B, 10, "f32", fill=0)
+        vc = scatter([V], tables, B, 10, "f32", fill=0)
+        plain = oracle.decode(q, kc, vc, tables, lens, 1.0, "f32")
+        part = oracle.decode_partitioned(q, kc, vc, tables, lens, 1.0, "f32", psize)
+        assert np.isfinite(plain).all() and np.isfinite(part).all()
+        np.testing.assert_allclose(part, plain, rtol=1e-9, atol=1e-12)
+        if spike:
+            np.testing.assert_allclose(plain[0, 0], V[1, 0], rtol=1e-9, atol=1e-12)
+
+
 def test_empty_context_gives_zeros():
     rng = synth.make_rng(9)
     q, K, V, kc, vc, tables, lens = random_case(rng, "f32", 2, 2, 2, 8, 4, [3, 5])

@@ -140,6 +140,21 @@ def test_appending_nothing_changes_nothing():
     assert (bm.table(a), bm.table(b), list(bm.free), list(bm.ref)) == snap
 
 
+def test_bad_pools_are_refused_and_copies_counted():
+    with pytest.raises(ValueError):
+        BlockManager(0, 16)
+    with pytest.raises(ValueError):
+        BlockManager(4, 16, [0, 1, 1, 2])          # not a permutation of the ids
+    # one copy-on-write ("Sharing a prefix and copying a partial block") is one copy
+    bm = BlockManager(8, 16)
+    a = bm.create()
+    bm.append(a, 24)
+    b = bm.fork(a)
+    bm.append(b, 1)
+    bm.append(b, 1)                                 # b's block is private now: no second copy
+    assert bm.stats()["cow_copies"] == 1
+
+
 def test_fault_injection_counts_down():
     # after set_fail_after(2) exactly two more block allocations succeed
     bm = BlockManager(8, 16)

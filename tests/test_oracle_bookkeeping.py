@@ -74,6 +74,14 @@ def test_waste_below_one_block_and_eta_bound():
             assert bk.eta_paged([L], B) >= bk.eta_paged_lower_bound(L, B)
 
 
+def test_block_count_refuses_negative_sizes():
+    with pytest.raises(ValueError):
+        bk.blocks_for(-1, 16)
+    with pytest.raises(ValueError):
+        bk.blocks_for(5, 0)
+    assert bk.blocks_for(0, 16) == 0
+
+
 def test_eta_bound_closed_forms():
     # one-slot blocks waste nothing: the bound is exactly 1
     for L in (1, 7, 300):

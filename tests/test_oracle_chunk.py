@@ -119,3 +119,5 @@ def test_rejects_inconsistent_query_ranges():
         oracle.chunk_attention(q, kc, vc, tables, lens, np.array([0, 4, 4], np.int32), 1.0, "f32")
     with pytest.raises(ValueError):       # ranges that do not end at T
         oracle.chunk_attention(q, kc, vc, tables, lens, np.array([0, 1, 3], np.int32), 1.0, "f32")
+    with pytest.raises(ValueError):       # ranges that do not start at row 0
+        oracle.chunk_attention(q, kc, vc, tables, lens, np.array([1, 2, 4], np.int32), 1.0, "f32")

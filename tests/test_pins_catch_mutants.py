@@ -133,6 +133,32 @@ MUTANTS = [
     (PC, "bm.seqs[sid].length = len(blocks) * bm.B", "bm.seqs[sid].length = len(blocks) * bm.B - 1",
      "prefix cache: sequence from a prefix one token short"),
     (PC, "    for b in blocks:\n        bm.ref[int(b)] += 1\n", "", "prefix cache: sequence from a prefix takes no references"),
+    # extreme logits, widening edge cases, and more refusals
+    (C, "double m = -INFINITY;\n                for (int i = i0; i < i1; ++i) {",
+     "double m = 0.0;\n                for (int i = i0; i < i1; ++i) {", "partitions: maximum started at 0"),
+    (C, "double mstar = mb[0];", "double mstar = mb[nparts - 1];", "merge: m* from the last partition only"),
+    (C, "double m = z[0];\n            for (int i = 1; i < len; ++i)", "double m = z[len - 1];\n            for (int i = 1; i < len - 1; ++i)",
+     "decode: maximum misses the first and last logits"),
+    (C, "mag = f ? NAN : INFINITY;", "mag = INFINITY;", "f16: NaN widened to infinity"),
+    (C, "return sign ? -mag : mag;", "return mag;", "f16: sign dropped"),
+    (C, "T < 0 || query_start[0] != 0 ||", "T < 0 || query_start[0] < 0 ||", "chunk: ranges not starting at row 0 accepted"),
+    (C, "if (n < 0 || n > lens[s])\n            return -1;", "if (n < 0 || n > lens[s] + 1)\n            return -1;",
+     "chunk: one query more than the context accepted"),
+    (C, "const size_t blk = (size_t)Hkv * B * D * elem_size(dtype);\n    for (int p = 0; p < P; ++p) {\n"
+        "        const int64_t src = pairs[2 * p], dst = pairs[2 * p + 1];\n        if (src < 0 || src >= N",
+     "const size_t blk = (size_t)Hkv * B * D * elem_size(dtype) / 2;\n    for (int p = 0; p < P; ++p) {\n"
+     "        const int64_t src = pairs[2 * p], dst = pairs[2 * p + 1];\n        if (src < 0 || src >= N",
+     "copy_blocks: half of each block"),
+    (BM, "self.free = deque(order)", "self.free = deque(sorted(order))", "allocator: free order ignored"),
+    (BM, "self.cow_copies += 1", "self.cow_copies += 0", "allocator: copies not counted"),
+    (BM, "if num_blocks <= 0 or block_size <= 0:", "if num_blocks < 0 or block_size <= 0:", "allocator: empty pool accepted"),
+    (BM, "if sorted(order) != list(range(num_blocks)):", "if len(order) != num_blocks:",
+     "allocator: free order not checked as a permutation"),
+    (PC, "while k * self.B <= len(tokens):", "while k * self.B < len(tokens):",
+     "prefix cache: a prompt ending on a block boundary loses its last block"),
+    (BK, "if tokens < 0 or block_size <= 0:", "if block_size <= 0:", "bookkeeping: negative token count accepted"),
+    (BK, '"naive_frag": Fraction(naive - tokens, naive)', '"naive_frag": Fraction(naive - tokens, paged)',
+     "bookkeeping: reserved-slot fragmentation over paged slots"),
 ]
 
 # Loads the oracle copy given as argv[1] before pytest can put the repository
