@@ -170,10 +170,39 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- oracle timing
-def time_oracle(step, seq_ids):
+def host_cores() -> int:
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the baseline's record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for key in ("Model name", "CPU part"):
+            m = re.search(rf"^{key}:\s*(.+)$", out, flags=re.M)
+            if m:
+                arch = re.search(r"^Architecture:\s*(.+)$", out, flags=re.M)
+                return f"{m.group(1).strip()} ({arch.group(1).strip() if arch else os.uname().machine})"
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip() + f" ({os.uname().machine})"
+    except OSError:
+        pass
+    return os.uname().machine
+
+
+def time_oracle(step, seq_ids, kc=None, vc=None):
     """Run the fp64 CPU oracle (KV write then decode) for the given sequences; return seconds."""
     import oracle
-    kc, vc = step.k_cache, step.v_cache
+    kc = step.k_cache if kc is None else kc
+    vc = step.v_cache if vc is None else vc
     t0 = time.perf_counter()
     oracle.write_kv(step.k_new[seq_ids], step.v_new[seq_ids], step.slots[seq_ids], kc, vc, step.dtype)
     oracle.decode(step.q[seq_ids], kc, vc, step.tables[seq_ids], step.lens[seq_ids], step.scale, step.dtype)
@@ -199,7 +228,295 @@ def cpu_baseline(step, budget_s: float = 15.0):
             "seconds": secs}
 
 
+# The all-core baseline runs the unchanged oracle in a pool of spawned worker
+# processes, one per host core; each worker maps the step's arrays from files
+# (copy-on-write, so each KV write stays private) and takes sequences from a
+# shared task list.
+_POOL_STEP = None
+_STEP_FIELDS = ("q", "k_new", "v_new", "slots", "tables", "lens", "k_cache", "v_cache")
+
+
+def _pool_init(folder, dtype, scale):
+    global _POOL_STEP
+    import types
+    import oracle
+    oracle._load()
+    arrs = {f: np.load(os.path.join(folder, f + ".npy"), mmap_mode="c") for f in _STEP_FIELDS}
+    _POOL_STEP = types.SimpleNamespace(dtype=dtype, scale=scale, **arrs)
+
+
+def _pool_task(ids):
+    ids = np.asarray(ids)
+    return time_oracle(_POOL_STEP, ids), int(_POOL_STEP.lens[ids].sum())
+
+
+def _pool_ready(_):
+    return _POOL_STEP is not None
+
+
+class OraclePool:
+    """A spawn-started process pool running the oracle over sequences of one step."""
+
+    def __init__(self, step, cores=None):
+        import multiprocessing as mp
+        import tempfile
+        import oracle
+        oracle._load()                       # built once here, not by every worker
+        self.cores = cores or host_cores()
+        self.step = step
+        self.folder = tempfile.mkdtemp(prefix="pa_oracle_pool_")
+        for f in _STEP_FIELDS:
+            np.save(os.path.join(self.folder, f + ".npy"), np.ascontiguousarray(getattr(step, f)))
+        self.pool = mp.get_context("spawn").Pool(self.cores, initializer=_pool_init,
+                                                 initargs=(self.folder, step.dtype, step.scale))
+        assert all(self.pool.map(_pool_ready, range(4 * self.cores), chunksize=1))
+
+    def run(self, tasks):
+        """Run the tasks (arrays of sequence ids); returns (wall seconds, context tokens)."""
+        t0 = time.perf_counter()
+        res = self.pool.map(_pool_task, tasks, chunksize=1)
+        return time.perf_counter() - t0, sum(r[1] for r in res)
+
+    def close(self):
+        import shutil
+        self.pool.close()
+        self.pool.join()
+        shutil.rmtree(self.folder, ignore_errors=True)
+
+
+def oracle_tasks(step, passes: int, per_task: int = 2, seed: int = 99):
+    rng = np.random.default_rng(seed)
+    tasks = []
+    for _ in range(passes):
+        order = rng.permutation(step.num_seqs)
+        tasks += [order[i:i + per_task] for i in range(0, len(order), per_task)]
+    return tasks
+
+
+def cpu_baseline_all_cores(step, single_gbs: float, target_s: float = 8.0):
+    """The unchanged oracle on every host core: whole passes over the step's
+    sequences, as many as fit about target_s seconds at the expected speed-up."""
+    pool = OraclePool(step)
+    try:
+        per_pass_s = step.kv_bytes_logical() / (single_gbs * 1e9) / pool.cores
+        passes = int(max(1, min(200, round(target_s / max(per_pass_s, 1e-6)))))
+        secs, tokens = pool.run(oracle_tasks(step, passes))
+    finally:
+        pool.close()
+    nbytes = tokens * step.kv_bytes_per_token()
+    return {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": pool.cores, "kind": "oracle",
+            "sample": f"{passes} pass(es) over all {step.num_seqs} sequences ({tokens} context tokens), "
+                      f"KV write + fp64 decode, {pool.cores} worker processes, {secs:.1f} s"}
+
+
+# --------------------------------------------------------------------------- GPU timing helpers
+def time_per_call(torch, fn, stream, reps: int, flush=None):
+    """Per-call CUDA-event times (ms) of `fn`, one event pair per call; with
+    `flush`, a buffer larger than L2 is overwritten before each call (outside
+    the pair), so the call starts with cold caches.  Returns (median, min, all)."""
+    pairs = []
+    for _ in range(reps):
+        if flush is not None:
+            flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        pairs.append((e0, e1))
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in pairs]
+    return float(np.median(ms)), float(np.min(ms)), ms
+
+
+def time_back_to_back(torch, fn, stream, n: int):
+    """Mean time (ms) of `fn` over n calls issued back to back between one event pair."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(n):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n
+
+
+def decode_launches(step, partition_size=None) -> int:
+    """Kernels one pa_decode call launches: plan + tensor-core decode (+ merge when
+    a sequence can span partitions) for 16-bit caches; CUDA-core decode (+ merge) for f32."""
+    pt = partition_size or step.partition_size
+    split = step.max_blocks * step.block_size > pt
+    return (1 if step.dtype == "f32" else 2) + (1 if split else 0)
+
+
+def decode_config(step, workload: str, world: int) -> dict:
+    """The workload's description, shared by both arms' JSON lines."""
+    kv_bytes = step.kv_bytes_logical()
+    return {
+        "workload": workload,
+        "num_seqs": step.num_seqs, "num_q_heads": step.num_q_heads, "num_kv_heads": step.num_kv_heads,
+        "head_dim": step.head_dim, "block_size": step.block_size, "partition_size": step.partition_size,
+        "num_blocks": step.num_blocks, "context_tokens": int(step.lens.sum()),
+        "max_context": int(step.lens.max()), "cow_pairs": int(step.pairs.shape[0]),
+        "kv_bytes_per_step": kv_bytes, "kv_bytes_unique_per_step": step.kv_bytes_unique(),
+        "l2": f"inputs larger than L2 ({kv_bytes / 2**20:.0f} MiB of KV read per step vs "
+              f"{L2_BYTES / 2**20:.0f} MiB L2); no flush between steps",
+        "parallelism": f"replicas x{world} (one workload per GPU, no collective on the data path)",
+    }
+
+
 # --------------------------------------------------------------------------- our arm
+SWEEP_WORKLOADS = ("gqa8b_b32", "mha7b", "prefix_cow", "long70b")
+COMPONENT_REPS = 25          # per-call event pairs, each after an L2 flush
+BACK_TO_BACK_CALLS = 200     # pa_decode calls between one event pair
+SWEEP_STEPS = 50
+
+
+class DecodeBuffers:
+    """One decode step's device tensors and its prepared library calls
+    (copy_blocks when the step has pairs, write_kv, decode) on `stream`."""
+
+    def __init__(self, torch, pa, step, device, stream, q, k_new, v_new, slots, tables, lens, pairs, k_cache,
+                 v_cache, extra_pairs=None):
+        self.step, self.dims = step, step.dims(pa)
+        S, Hq, D = step.num_seqs, step.num_q_heads, step.head_dim
+        self.k_cache, self.v_cache = k_cache, v_cache
+        self.out = torch.empty((S, Hq, D), dtype=torch.float32, device=device)
+        ws_bytes = pa.pa_decode_workspace_bytes(self.dims)
+        self.ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device)
+        self.npairs = int(pairs.shape[0])
+        self.copy = (pa.pa_copy_blocks(self.dims, k_cache, v_cache, pairs, stream, prepare=True)
+                     if self.npairs else None)
+        self.write = pa.pa_write_kv(self.dims, k_new, v_new, slots, k_cache, v_cache, stream, prepare=True)
+        self.decode = pa.pa_decode(self.dims, q, k_cache, v_cache, tables, lens, step.scale, self.out, self.ws,
+                                   stream, prepare=True)
+        # copy_blocks timed alone: the step's own pairs, else pairs into blocks no table uses
+        self.copy_alone = self.copy
+        if self.copy is None and extra_pairs is not None and len(extra_pairs):
+            xp = torch.from_numpy(np.ascontiguousarray(extra_pairs, dtype=np.int64)).to(device)
+            self.copy_alone = pa.pa_copy_blocks(self.dims, k_cache, v_cache, xp, stream, prepare=True)
+        self.copy_alone_pairs = self.npairs or (0 if extra_pairs is None else len(extra_pairs))
+        self.launches_per_step = (1 if self.npairs else 0) + 1 + decode_launches(step)
+
+    def step_calls(self):
+        if self.copy is not None:
+            self.copy()
+        self.write()
+        self.decode()
+
+
+def spare_pairs(step, n: int = 32) -> np.ndarray:
+    """n copy pairs from blocks the step's tables use into blocks none uses
+    (destinations distinct and never a source), for timing copy_blocks alone."""
+    B = step.block_size
+    used = set()
+    for s in range(step.num_seqs):
+        nb = -(-int(step.lens[s]) // B)
+        used.update(int(b) for b in step.tables[s, :nb])
+    free = [b for b in range(step.num_blocks) if b not in used]
+    src = sorted(used)[:n]
+    k = min(n, len(free), len(src))
+    return np.array([[src[i], free[i]] for i in range(k)], dtype=np.int64).reshape(-1, 2)
+
+
+def measure_components(torch, bufs: DecodeBuffers, stream, flush):
+    """Fixed-length timings of the step's kernels, independent of --steps."""
+    for _ in range(5):
+        bufs.decode()
+    b2b = time_back_to_back(torch, bufs.decode, stream, BACK_TO_BACK_CALLS)
+    d_med, d_min, _ = time_per_call(torch, bufs.decode, stream, COMPONENT_REPS, flush)
+    w_med, w_min, _ = time_per_call(torch, bufs.write, stream, COMPONENT_REPS, flush)
+    out = {"decode_ms": {"back_to_back": round(b2b, 5), "median": round(d_med, 5), "min": round(d_min, 5),
+                         "calls_back_to_back": BACK_TO_BACK_CALLS, "reps": COMPONENT_REPS},
+           "write_kv_us": {"median": round(w_med * 1e3, 2), "min": round(w_min * 1e3, 2),
+                           "tokens": int(bufs.step.slots.shape[0]), "reps": COMPONENT_REPS}}
+    if bufs.copy_alone is not None:
+        c_med, c_min, _ = time_per_call(torch, bufs.copy_alone, stream, COMPONENT_REPS, flush)
+        out["copy_blocks_us"] = {"median": round(c_med * 1e3, 2), "min": round(c_min * 1e3, 2),
+                                 "pairs": bufs.copy_alone_pairs, "reps": COMPONENT_REPS,
+                                 "pairs_from": "the step's copy-on-write pairs" if bufs.npairs else
+                                               "blocks in use copied into unused blocks"}
+    return out
+
+
+def roofline_of(step, comp, peak, peak_kind, workload):
+    """The decode call against the HBM roofline: distinct KV bytes per call over
+    its back-to-back mean time (and over the median of single calls after an L2 flush)."""
+    kv_unique = step.kv_bytes_unique()
+    dm = comp["decode_ms"]
+    achieved = kv_unique / (dm["back_to_back"] / 1e3) / 1e9
+    return {
+        "bound": "hbm",
+        "kernel": "pa_decode call (plan + tensor-core decode + split-K merge kernels)",
+        "achieved": round(achieved, 1),
+        "achieved_single_call_median": round(kv_unique / (dm["median"] / 1e3) / 1e9, 1),
+        "achieved_logical": round(step.kv_bytes_logical() / (dm["back_to_back"] / 1e3) / 1e9, 1),
+        "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+        "frac": round(achieved / peak, 4),
+        "pct_of_nominal_8tbs": round(100 * achieved / NOMINAL_HBM_GBS, 2),
+        "traffic": profiled_traffic(workload),
+        "bytes": "distinct KV slots read per pa_decode call (2 * Hkv * D * sizeof per token)",
+        "timing": f"mean of {dm['calls_back_to_back']} back-to-back calls between one CUDA event pair on the "
+                  f"launch stream; single-call median/min over {dm['reps']} event pairs, L2 flushed before each",
+    }
+
+
+def timed_steps(torch, fn, stream, n):
+    """Device time (ms) of n steps between one event pair, synchronised on both sides."""
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(n):
+        fn()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1)
+
+
+def sweep_entry(torch, pa, name, rank, device, stream, flush, peak, peak_kind):
+    """Another workload's decode step, with cache, query and new-row values drawn
+    on the device (N(0, std) as the workload states); tables, slots and pairs
+    from the allocator as for the headline."""
+    from paged_kv_cache_127_gb300 import synth, workloads
+    st = workloads.build_step(name, seed=rank, values=False, binding=pa)
+    w = synth.workload(name, rank)
+    kvt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[st.dtype]
+    gen = torch.Generator(device=device)
+    gen.manual_seed(7000 + 31 * rank + SWEEP_WORKLOADS.index(name))
+    S, Hq, Hkv, D, B, N = (st.num_seqs, st.num_q_heads, st.num_kv_heads, st.head_dim, st.block_size,
+                           st.num_blocks)
+    T = int(st.slots.shape[0])
+
+    def rnd(shape, std):
+        t = torch.randn(shape, generator=gen, device=device, dtype=kvt)
+        return t.mul_(std) if std != 1.0 else t
+
+    kc, vc = rnd((N, Hkv, B, D), w.std), rnd((N, Hkv, B, D), w.std)
+    q = rnd((S, Hq, D), w.std * w.q_prescale)
+    kn, vn = rnd((T, Hkv, D), w.std), rnd((T, Hkv, D), w.std)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    bufs = DecodeBuffers(torch, pa, st, device, stream, q, kn, vn, dev(st.slots), dev(st.tables), dev(st.lens),
+                         dev(st.pairs), kc, vc, extra_pairs=spare_pairs(st))
+    for _ in range(5):
+        bufs.step_calls()
+    ms = timed_steps(torch, bufs.step_calls, stream, SWEEP_STEPS) / SWEEP_STEPS
+    comp = measure_components(torch, bufs, stream, flush)
+    torch.cuda.synchronize()
+    assert torch.isfinite(bufs.out).all().item(), f"{name}: non-finite output"
+    entry = {
+        "value": round(st.kv_bytes_logical() / (ms / 1e3) / 1e9, 1), "unit": "GB/s",
+        "ms_per_step": round(ms, 5), "steps": SWEEP_STEPS,
+        "q_tok_per_s_per_layer": round(S / (ms / 1e3), 1),
+        "dtype": st.dtype,
+        **comp,
+        "roofline": roofline_of(st, comp, peak, peak_kind, name),
+        "config": decode_config(st, name, 1),
+        "data": "synthetic: tables, slots and pairs from the allocator; values drawn on the device",
+    }
+    del bufs, kc, vc, q, kn, vn
+    torch.cuda.empty_cache()
+    return entry
+
+
 def run_ours(args):
     import torch
 
@@ -214,22 +531,20 @@ def run_ours(args):
     step = workloads.build_step(args.workload, seed=rank, binding=pa)
     if args.partition_size:
         step.partition_size = args.partition_size
-    dims = step.dims(pa)
     S, Hq, D = step.num_seqs, step.num_q_heads, step.head_dim
-
-    def bf(x):
-        if step.dtype == "bf16":
-            return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
-        return torch.from_numpy(np.ascontiguousarray(x))
+    kvt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[step.dtype]
+    stream = torch.cuda.current_stream(device)
 
     # The step's inputs, packed in one pinned host buffer (for the end-to-end leg,
-    # one host-to-device copy per step) and its device mirror; the device tensors
-    # below are views into the mirror.
+    # one host-to-device copy per step) and two device mirrors of it; the device
+    # tensors are views into the mirrors.
     def as_bytes(x):
         return np.ascontiguousarray(x).view(np.uint8).reshape(-1)
 
     parts = [("q", step.q), ("k", step.k_new), ("v", step.v_new), ("slots", step.slots),
              ("tables", step.tables), ("lens", step.lens), ("pairs", np.ascontiguousarray(step.pairs))]
+    tdt = {"q": kvt, "k": kvt, "v": kvt, "slots": torch.int64, "tables": torch.int32, "lens": torch.int32,
+           "pairs": torch.int64}
     offs, total = {}, 0
     for name, arr in parts:
         offs[name] = total
@@ -238,89 +553,52 @@ def run_ours(args):
     for name, arr in parts:
         b = as_bytes(arr)
         h_in[offs[name]:offs[name] + b.size] = torch.from_numpy(b)
-    # two device mirrors of the inputs and two outputs: the end-to-end leg
-    # double-buffers them so a step's copies overlap its neighbours' compute
-    d_ins = [h_in.to(device), h_in.to(device)]
-    kvt = torch.bfloat16 if step.dtype == "bf16" else (torch.float16 if step.dtype == "f16" else torch.float32)
+    d_ins = [torch.empty(total, dtype=torch.uint8, device=device) for _ in range(2)]
+    for d in d_ins:
+        pa.pa_copy_to_device(d, h_in, stream)
+
+    def host_cache(x):
+        t = torch.from_numpy(np.ascontiguousarray(x))
+        return t.view(torch.int16).view(torch.bfloat16) if step.dtype == "bf16" else t
+
+    d_kc, d_vc = host_cache(step.k_cache).to(device), host_cache(step.v_cache).to(device)
 
     def views(d_in):
-        def view(name, arr, tdtype, shape):
-            n = np.ascontiguousarray(arr).nbytes
-            return d_in[offs[name]:offs[name] + n].view(tdtype).view(shape)
-        return {"q": view("q", step.q, kvt, step.q.shape), "k": view("k", step.k_new, kvt, step.k_new.shape),
-                "v": view("v", step.v_new, kvt, step.v_new.shape),
-                "slots": view("slots", step.slots, torch.int64, step.slots.shape),
-                "tables": view("tables", step.tables, torch.int32, step.tables.shape),
-                "lens": view("lens", step.lens, torch.int32, step.lens.shape),
-                "pairs": view("pairs", step.pairs, torch.int64, step.pairs.shape)}
+        return {name: d_in[offs[name]:offs[name] + np.ascontiguousarray(arr).nbytes].view(tdt[name])
+                .view(np.ascontiguousarray(arr).shape) for name, arr in parts}
 
-    bufs = [views(d) for d in d_ins]
-    h_outs = [torch.empty((S, Hq, D), dtype=torch.float32).pin_memory() for _ in range(2)]
-    d_kc, d_vc = bf(step.k_cache).to(device), bf(step.v_cache).to(device)
-    d_outs = [torch.empty((S, Hq, D), dtype=torch.float32, device=device) for _ in range(2)]
-    d_out = d_outs[0]
-    ws_bytes = pa.pa_decode_workspace_bytes(dims)
-    d_ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=device)
-    stream = torch.cuda.current_stream(device)
-    npairs = int(step.pairs.shape[0])
-    # copy-on-write pairs apply once: after the first step the copies are in place and
-    # re-running them would copy identical bytes; they stay in the step for fidelity.
-    # Launches per step: copy_blocks (if pairs), write_kv, and pa_decode's kernels:
-    # plan + tensor-core decode (+ merge when a sequence can span partitions) for
-    # 16-bit caches; the CUDA-core decode (+ merge) for f32.
-    split = step.max_blocks * step.block_size > (args.partition_size or step.partition_size)
-    decode_launches = (1 if step.dtype == "f32" else 2) + (1 if split else 0)
-    launches_per_step = (1 if npairs else 0) + 1 + decode_launches
-
-    dec_ev = []
-
-    def device_step(record=False, b=0, st=None):
-        st = stream if st is None else st
-        v = bufs[b]
-        if npairs:
-            pa.pa_copy_blocks(dims, d_kc, d_vc, v["pairs"], st)
-        pa.pa_write_kv(dims, v["k"], v["v"], v["slots"], d_kc, d_vc, st)
-        if record:
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(st)
-        pa.pa_decode(dims, v["q"], d_kc, d_vc, v["tables"], v["lens"], step.scale, d_outs[b], d_ws, st)
-        if record:
-            e1.record(st)
-            dec_ev.append((e0, e1))
+    vws = [views(d) for d in d_ins]
+    bufs = [DecodeBuffers(torch, pa, step, device, stream, v["q"], v["k"], v["v"], v["slots"], v["tables"],
+                          v["lens"], v["pairs"], d_kc, d_vc, extra_pairs=spare_pairs(step)) for v in vws]
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
+    peak, peak_kind = measured_hbm_peak()
 
     pa.pa_device_errors(clear=True)
     sampler = ClockSampler(device.index).start() if rank == 0 else None
     for _ in range(args.warmup):
-        device_step()
+        bufs[0].step_calls()
     torch.cuda.synchronize(device)
     assert pa.pa_device_errors(clear=True) == 0, "device error flags set during warm-up"
 
-    # ---- device-resident timing
+    # ---- the timed steps: exactly K steps between one event pair, inputs resident in HBM
     barrier(dist, device)
-    torch.cuda.synchronize(device)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    # the decode call is bracketed by CUDA events on every 8th step (an event pair
-    # on every step would cost the step ~2 % by breaking the overlap of the
-    # programmatically dependent launches)
-    for i in range(args.steps):
-        device_step(record=(i % 8 == 0))
-    t1.record(stream)
-    torch.cuda.synchronize(device)
+    ms_local = timed_steps(torch, bufs[0].step_calls, stream, args.steps)
     barrier(dist, device)
-    ms_local = t0.elapsed_time(t1)
-    dec_ms = float(np.mean([a.elapsed_time(b) for a, b in dec_ev]))
     ms_total = reduce_scalar(dist, ms_local, "max", device)
 
-    # ---- end to end through the binding with host buffers.  Every step copies
-    # all of its inputs host -> device (one packed copy) and its output device ->
-    # host; steps are double-buffered over three streams, so step i's copies
-    # overlap the compute of steps i - 1 and i + 1, and the host collects step
-    # i - 1's result before enqueueing step i + 1.
+    # ---- fixed-length component timings (roofline), independent of --steps
+    comp = measure_components(torch, bufs[0], stream, flush)
+
+    # ---- end to end through the library with host buffers.  Every step copies
+    # all of its inputs host -> device (one packed pa_copy_to_device) and its
+    # output device -> host (pa_copy_to_host); steps are double-buffered over
+    # three streams, so step i's copies overlap the compute of steps i - 1 and
+    # i + 1, and the host collects step i - 1's result before enqueueing i + 1.
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
     s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    h_outs = [torch.empty((S, Hq, D), dtype=torch.float32).pin_memory() for _ in range(2)]
+    h2d = [pa.pa_copy_to_device(d_ins[b], h_in, s_in, prepare=True) for b in range(2)]
+    d2h = [pa.pa_copy_to_host(h_outs[b], bufs[b].out, s_out, prepare=True) for b in range(2)]
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_cmp = [torch.cuda.Event() for _ in range(2)]
     ev_out = [torch.cuda.Event() for _ in range(2)]
@@ -330,17 +608,15 @@ def run_ours(args):
             b = i & 1
             if i >= 2:
                 s_in.wait_event(ev_cmp[b])      # step i - 2 has read input buffer b
-            with torch.cuda.stream(s_in):
-                d_ins[b].copy_(h_in, non_blocking=True)
+            h2d[b]()
             ev_in[b].record(s_in)
             stream.wait_event(ev_in[b])
             if i >= 2:
                 stream.wait_event(ev_out[b])    # step i - 2's output has reached the host
-            device_step(b=b)
+            bufs[b].step_calls()
             ev_cmp[b].record(stream)
             s_out.wait_event(ev_cmp[b])
-            with torch.cuda.stream(s_out):
-                h_outs[b].copy_(d_outs[b], non_blocking=True)
+            d2h[b]()
             ev_out[b].record(s_out)
             if i >= 1:
                 ev_out[b ^ 1].synchronize()     # the host has step i - 1's result
@@ -354,26 +630,27 @@ def run_ours(args):
     e2e_s = time.perf_counter() - w0
     barrier(dist, device)
     e2e_s = reduce_scalar(dist, e2e_s, "max", device)
-    clocks = sampler.stop() if sampler else None
     assert pa.pa_device_errors(clear=True) == 0, "device error flags set during the timed steps"
-    assert torch.isfinite(d_out).all().item()
+    assert torch.isfinite(bufs[0].out).all().item()
+
+    sweeps = {}
+    if rank == 0 and world == 1 and not args.no_sweeps and args.workload == "gqa8b_b16" \
+            and not args.partition_size:
+        del bufs, vws, d_ins, d_kc, d_vc
+        torch.cuda.empty_cache()
+        for name in SWEEP_WORKLOADS:
+            sweeps[name] = sweep_entry(torch, pa, name, rank, device, stream, flush, peak, peak_kind)
+        assert pa.pa_device_errors(clear=True) == 0, "device error flags set during the sweeps"
+    clocks = sampler.stop() if sampler else None
 
     kv_bytes = step.kv_bytes_logical()
     kv_all = reduce_scalar(dist, kv_bytes, "sum", device)
     seqs_all = reduce_scalar(dist, S, "sum", device)
     step_s = ms_total / 1e3 / args.steps
-    h2d = h_in.numel()
-    d2h = h_outs[0].numel() * h_outs[0].element_size()
-
     if rank != 0:
         return None
-    peak, peak_kind = measured_hbm_peak()
-    # The roofline counts KV bytes HBM must deliver: each distinct slot once.  With
-    # prefix sharing the shared blocks are read by many sequences but come from HBM
-    # (then L2) once, so `value` (logical bytes) can exceed the HBM peak.
-    kv_unique = step.kv_bytes_unique()
-    achieved = kv_unique / (dec_ms / 1e3) / 1e9
     value = kv_all / step_s / 1e9
+    launches_per_step = (1 if step.pairs.shape[0] else 0) + 1 + decode_launches(step)
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -387,41 +664,31 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": step.dtype,
         "data": "synthetic (seeded; shapes and length distributions of the workload)",
-        "config": {
-            "workload": args.workload,
-            "num_seqs": S, "num_q_heads": Hq, "num_kv_heads": step.num_kv_heads, "head_dim": D,
-            "block_size": step.block_size, "partition_size": step.partition_size,
-            "num_blocks": step.num_blocks, "context_tokens": int(step.lens.sum()),
-            "max_context": int(step.lens.max()), "cow_pairs": npairs,
-            "kv_bytes_per_step": kv_bytes,
-            "kv_bytes_unique_per_step": kv_unique,
-            "l2": f"inputs larger than L2 ({kv_bytes / 2**20:.0f} MiB of KV read per step vs "
-                  f"{L2_BYTES / 2**20:.0f} MiB L2); no flush",
-            "parallelism": f"replicas x{world} (one workload per GPU, no collective on the data path)",
-        },
+        "config": decode_config(step, args.workload, world),
         "q_tok_per_s_per_layer": round(seqs_all / step_s, 1),
         "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
-        "roofline": {
-            "bound": "hbm",
-            "kernel": "pa_decode (plan + tensor-core decode + split-K merge kernels), CUDA events around each call",
-            "achieved": round(achieved, 1),
-            "achieved_logical": round(kv_bytes / (dec_ms / 1e3) / 1e9, 1),
-            "peak": peak,
-            "peak_kind": peak_kind,
-            "unit": "GB/s",
-            "frac": round(achieved / peak, 4),
-            "traffic": profiled_traffic(args.workload),
-            "decode_ms": round(dec_ms, 5),
-            "bytes": "distinct KV slots read per pa_decode call (2 * Hkv * D * sizeof per token)",
-        },
+        **comp,
+        "roofline": roofline_of(step, comp, peak, peak_kind, args.workload),
         "e2e": {"value": round(kv_all * e2e_steps / e2e_s / 1e9, 1), "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_s * 1e3 / e2e_steps, 5), "steps": e2e_steps},
+                "h2d_bytes_per_step": h_in.numel(),
+                "d2h_bytes_per_step": h_outs[0].numel() * h_outs[0].element_size(),
+                "ms_per_step": round(e2e_s * 1e3 / e2e_steps, 5), "steps": e2e_steps,
+                "copies": "pa_copy_to_device / pa_copy_to_host (cudaMemcpyAsync in the library), pinned host "
+                          "buffers, double-buffered over copy-in / compute / copy-out streams"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
+    if sweeps:
+        line["sweeps"] = sweeps
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = {k: v for k, v in cpu_baseline(step).items() if k != "seconds"}
+        single = {k: v for k, v in cpu_baseline(step).items() if k != "seconds"}
+        try:
+            base = cpu_baseline_all_cores(step, single["value"])
+        except Exception as e:   # the single-thread figure then stands alone
+            base = dict(single, all_cores_unavailable=f"{type(e).__name__}: {e}")
+        base["single_thread"] = single
+        base["cpu_model"] = cpu_model()
+        line["cpu_baseline"] = base
     return line
 
 
@@ -874,54 +1141,116 @@ def run_prefix(args):
 
 
 # --------------------------------------------------------------------------- reference arm
+class _OracleAllocator:
+    """The allocator calls a workload's set-up makes, served by the oracle's
+    block-manager model (the pages' bookkeeping rules in plain Python), so the
+    reference arm builds the same tables, slots and pairs without loading the
+    product library."""
+
+    class Pool:
+        def __init__(self, num_blocks, block_size, order):
+            from oracle.block_manager import BlockManager
+            self.handle = BlockManager(num_blocks, block_size, [int(b) for b in order])
+
+        def close(self):
+            pass
+
+    @staticmethod
+    def pa_seq_create(bm):
+        return bm.create()
+
+    @staticmethod
+    def pa_seq_fork(bm, parent):
+        return bm.fork(parent)
+
+    @staticmethod
+    def pa_seq_append(bm, seq, n):
+        return bm.append(seq, int(n))
+
+    @staticmethod
+    def pa_seq_free(bm, seq):
+        bm.free_seq(seq)
+
+    @staticmethod
+    def pa_seq_append_batch(bm, seqs, n):
+        slots, pairs = [], []
+        for s_ in seqs:
+            sl, pr = bm.append(s_, int(n))
+            slots += sl
+            pairs += pr
+        return (np.array(slots, dtype=np.int64).reshape(len(seqs), int(n)),
+                np.array(pairs, dtype=np.int64).reshape(-1, 2))
+
+    @staticmethod
+    def pa_copy_pairs_check(pairs, num_blocks):
+        dst = [int(d) for d in pairs[:, 1]]
+        if len(set(dst)) != len(dst) or set(dst) & {int(x) for x in pairs[:, 0]} or \
+                any(not 0 <= int(b) < num_blocks for b in pairs.reshape(-1)):
+            raise ValueError("copy pairs violate the copy precondition")
+
+    @staticmethod
+    def pa_pool_export(bm, seqs, max_blocks, pad=-1):
+        tables = np.full((len(seqs), max_blocks), pad, dtype=np.int32)
+        lens = np.zeros(len(seqs), dtype=np.int32)
+        for i, s_ in enumerate(seqs):
+            t = bm.table(s_)
+            tables[i, :len(t)] = t
+            lens[i] = bm.length(s_)
+        return tables, lens
+
+
 def run_reference(args):
-    """Time the CPU oracle on host cores: each step one bounded sample of the workload."""
+    """Time the CPU oracle on every host core: each step is one bounded sample
+    of the workload (the whole batch when it fits), run by a spawned process
+    pool, with tables, slots and pairs from the oracle's own block manager."""
     rank, _, world = dist_env()
     if rank != 0:
         return None
     from paged_kv_cache_127_gb300 import workloads
 
-    try:
-        from paged_kv_cache_127_gb300 import binding as pa
-    except ImportError:
-        from paged_kv_cache_127_gb300 import build as pa_build
-        pa_build.build()
-        from paged_kv_cache_127_gb300 import binding as pa
-    step = workloads.build_step(args.workload, seed=0, binding=pa)
+    step = workloads.build_step(args.workload, seed=0, binding=_OracleAllocator)
+    if args.partition_size:
+        step.partition_size = args.partition_size
     rng = np.random.default_rng(7)
     order = rng.permutation(step.num_seqs)
-    # size each step so that the whole run stays within ~2 minutes
-    calib = time_oracle(step, order[:1])
-    per_seq = max(calib, 1e-4)
-    budget = 120.0 / max(1, args.steps + args.warmup)
-    k = int(max(1, min(step.num_seqs, budget / per_seq)))
-    per_tok = step.kv_bytes_per_token()
-    pos = 0
+    per_seq = max(time_oracle(step, order[:2]) / 2, 1e-4)       # one thread, seconds per sequence
+    pool = OraclePool(step)
+    try:
+        # size each step so that the whole run stays within ~2 minutes
+        budget = 100.0 / max(1, args.steps + args.warmup)
+        k = int(max(1, min(step.num_seqs, budget * pool.cores / per_seq)))
+        per_tok = step.kv_bytes_per_token()
+        pos = 0
 
-    def one():
-        nonlocal pos
-        ids = np.array([order[(pos + i) % step.num_seqs] for i in range(k)])
-        pos += k
-        return time_oracle(step, ids), int(step.lens[ids].sum()) * per_tok
+        def one():
+            nonlocal pos
+            ids = np.array([order[(pos + i) % step.num_seqs] for i in range(k)])
+            pos += k
+            return pool.run([ids[i:i + 2] for i in range(0, k, 2)])
 
-    for _ in range(args.warmup):
-        one()
-    secs, nbytes = 0.0, 0
-    for _ in range(args.steps):
-        s, b = one()
-        secs += s
-        nbytes += b
-    value = nbytes / secs / 1e9
+        for _ in range(args.warmup):
+            one()
+        secs, tokens = 0.0, 0
+        for _ in range(args.steps):
+            s_, t_ = one()
+            secs += s_
+            tokens += t_
+    finally:
+        pool.close()
+    value = tokens * per_tok / secs / 1e9
+    config = decode_config(step, args.workload, world)
+    config["sequences_per_step"] = k
     return {
         "impl": "reference",
         "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs * 1e3 / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded; same workload as the GPU arm)",
-        "config": {"workload": args.workload, "num_seqs": step.num_seqs, "block_size": step.block_size,
-                   "sequences_per_step": k},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{k} sequence(s) per step, KV write + fp64 decode, single thread"},
+        "config": config,
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": pool.cores, "kind": "oracle",
+                         "cpu_model": cpu_model(),
+                         "sample": f"{k} of {step.num_seqs} sequence(s) per step, KV write + fp64 decode, "
+                                   f"{pool.cores} worker processes"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -935,6 +1264,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweeps", action="store_true",
+                    help="skip the other decode workloads in the default gqa8b_b16 run")
     ap.add_argument("--num-seqs", type=int, default=0,
                     help="with --layers: use only the first K sequences of the workload")
     ap.add_argument("--swap-blocks", type=int, default=0,

@@ -15,6 +15,9 @@
  *    row-major and contiguous, and must be 16-byte aligned.  The GPU entry
  *    points allocate no device memory; the split-K scratch of pa_decode is
  *    passed in as `workspace`.
+ *  - GPU calls work on the calling thread's current device: every device
+ *    pointer and the stream of a call must belong to it (the per-device error
+ *    word, fixed scratch and cached tensor maps are the current device's).
  *  - GPU calls are asynchronous on `stream` (a cudaStream_t passed as void*;
  *    NULL is the legacy default stream).  The returned status covers only
  *    what the host can check (dimensions, dtypes, alignment, supported
@@ -145,8 +148,12 @@ PA_API int32_t pa_decode(const pa_dims *dims, const void *q, const void *k_cache
  * It allocates nothing.
  *
  *  - The first call on each device looks up that buffer's device address
- *    (cudaGetSymbolAddress, with the device current) and caches it; make that
- *    first call before any stream capture on the device.
+ *    (cudaGetSymbolAddress, with the device current) and caches it together
+ *    with the id of the current CUDA context; make that first call before any
+ *    stream capture on the device.  After a device reset the new context has
+ *    a new id, and the next call looks the address up again.
+ *  - Like every GPU call here, it works on the current device: the pointers
+ *    and the stream must belong to it.
  *  - Returns PA_ERR_TOO_LARGE, doing nothing, when pa_decode_workspace_bytes
  *    (dims) exceeds PA_NOALLOC_SCRATCH_BYTES; use pa_decode with a workspace
  *    then.  Other statuses as for pa_decode.
@@ -319,6 +326,21 @@ PA_API int32_t pa_swap_blocks(const pa_dims *dims, void *k_cache, void *v_cache,
                               int32_t num_host_blocks, int32_t num_layers, int64_t dev_layer_stride_bytes,
                               int64_t host_layer_stride_bytes, const int64_t *pairs, int32_t num_pairs,
                               int32_t direction, void *stream);
+
+/*
+ * pa_copy_to_device / pa_copy_to_host -- one asynchronous copy of `bytes`
+ * bytes between host memory and device memory of the current device, on
+ * `stream` (cudaMemcpyAsync).  The pages have no counterpart: this is the hop
+ * a serving step makes to bring its inputs (queries, new K/V rows, slots,
+ * block tables, lengths, copy pairs) to the GPU and its output back, offered
+ * here so that a caller holding only host buffers needs nothing but this
+ * library.  The copy overlaps kernels on other streams only when the host
+ * buffer is pinned (page-locked, e.g. cudaHostAlloc); pageable memory makes
+ * it synchronous.  bytes == 0 does nothing.  Returns PA_OK, PA_ERR_INVALID
+ * (a null pointer with bytes > 0) or PA_ERR_CUDA.
+ */
+PA_API int32_t pa_copy_to_device(void *dst_device, const void *src_host, size_t bytes, void *stream);
+PA_API int32_t pa_copy_to_host(void *dst_host, const void *src_device, size_t bytes, void *stream);
 
 /*
  * pa_device_errors -- read (and, if clear != 0, reset) the sticky PA_DEVERR_*

@@ -9,6 +9,7 @@ built -- there is no fallback path.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -65,6 +66,8 @@ _SIGNATURES = {
     "pa_step_graph_launch": (_i32, [_vp, _vp]),
     "pa_step_graph_destroy": (None, [_vp]),
     "pa_device_errors": (_i32, [_vp, _i32]),
+    "pa_copy_to_device": (_i32, [_vp, _vp, _sz, _vp]),
+    "pa_copy_to_host": (_i32, [_vp, _vp, _sz, _vp]),
     "pa_version": (ctypes.c_char_p, []),
     "pa_selftest_bounded_wait": (_i32, [ctypes.c_uint32, _vp, _vp]),
     "pa_pool_create": (_vp, [_i32, _i32, _vp]),
@@ -151,10 +154,47 @@ def _expect(t, name, shape, dtype, device):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _on(device):
+    """Make `device` current for one library call: the library keeps its
+    per-device state (error word, fixed scratch, tensor-map cache) for the
+    current device, and every pointer and the stream of a call must belong to it."""
+    t = _torch()
+    if t.cuda.current_device() == device.index:
+        return contextlib.nullcontext()
+    return t.cuda.device(device)
+
+
 def _stream_ptr(stream, device):
     t = _torch()
     s = t.cuda.current_stream(device) if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
+
+
+class Prepared:
+    """One library call whose arguments were checked and marshalled once, issued
+    again on every call(): for loops that repeat a call on the same buffers and
+    stream (a serving step, a benchmark), where re-checking tensors each time
+    would cost more host time than the kernel takes.  Holds references to the
+    tensors it was prepared with; refresh their contents in place."""
+
+    __slots__ = ("fn", "args", "what", "device", "keep")
+
+    def __init__(self, fn, args, what, device, keep):
+        self.fn, self.args, self.what, self.device, self.keep = fn, args, what, device, keep
+
+    def __call__(self) -> None:
+        with _on(self.device):
+            st = self.fn(*self.args)
+        _check(st, self.what)
+
+
+def _issue(fn, args, what, device, prepare, keep):
+    if prepare:
+        return Prepared(fn, args, what, device, keep)
+    with _on(device):
+        st = fn(*args)
+    _check(st, what)
+    return None
 
 
 def pa_decode_workspace_bytes(dims: pa_dims) -> int:
@@ -162,8 +202,9 @@ def pa_decode_workspace_bytes(dims: pa_dims) -> int:
 
 
 def pa_decode(dims: pa_dims, q, k_cache, v_cache, block_tables, context_lens, scale: float, out,
-              workspace=None, stream=None) -> None:
-    """out[s, h] = softmax(scale * q[s, h] . K_s^T) . V_s over each sequence's paged context."""
+              workspace=None, stream=None, prepare: bool = False):
+    """out[s, h] = softmax(scale * q[s, h] . K_s^T) . V_s over each sequence's paged context.
+    With prepare=True nothing runs: the checked call is returned as a Prepared."""
     t = _torch()
     d, kv = dims, _torch_dtype(dims.kv_dtype)
     dev = q.device
@@ -183,10 +224,10 @@ def pa_decode(dims: pa_dims, q, k_cache, v_cache, block_tables, context_lens, sc
             raise ValueError("workspace must be a contiguous CUDA tensor on the same device")
         ws_bytes = workspace.numel() * workspace.element_size()
         ws_ptr = ctypes.c_void_p(workspace.data_ptr())
-    st = lib.pa_decode(ctypes.byref(dims), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
-                       block_tables.data_ptr(), context_lens.data_ptr(), float(scale), out.data_ptr(),
-                       ws_ptr, ws_bytes, _stream_ptr(stream, dev))
-    _check(st, "pa_decode")
+    args = (ctypes.byref(dims), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+            context_lens.data_ptr(), float(scale), out.data_ptr(), ws_ptr, ws_bytes, _stream_ptr(stream, dev))
+    return _issue(lib.pa_decode, args, "pa_decode", dev, prepare,
+                  (dims, q, k_cache, v_cache, block_tables, context_lens, out, workspace))
 
 
 def pa_decode_noalloc(dims: pa_dims, q, k_cache, v_cache, block_tables, context_lens, scale: float, out,
@@ -209,9 +250,10 @@ def pa_decode_noalloc(dims: pa_dims, q, k_cache, v_cache, block_tables, context_
     _expect(block_tables, "block_tables", (d.num_seqs, d.max_blocks_per_seq), t.int32, dev)
     _expect(context_lens, "context_lens", (d.num_seqs,), t.int32, dev)
     _expect(out, "out", (d.num_seqs, d.num_q_heads, d.head_dim), t.float32, dev)
-    st = lib.pa_decode_noalloc(ctypes.byref(dims), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
-                               block_tables.data_ptr(), context_lens.data_ptr(), float(scale), out.data_ptr(),
-                               _stream_ptr(stream, dev))
+    with _on(dev):
+        st = lib.pa_decode_noalloc(ctypes.byref(dims), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                   block_tables.data_ptr(), context_lens.data_ptr(), float(scale), out.data_ptr(),
+                                   _stream_ptr(stream, dev))
     _check(st, "pa_decode_noalloc")
 
 
@@ -220,9 +262,10 @@ def pa_chunk_workspace_bytes(dims: pa_dims, num_tokens: int, max_query_len: int)
 
 
 def pa_chunk_attention(dims: pa_dims, q, k_cache, v_cache, block_tables, context_lens, query_start, scale: float,
-                       out, max_query_len: int, workspace=None, stream=None) -> None:
+                       out, max_query_len: int, workspace=None, stream=None, prepare: bool = False):
     """Causal paged attention for the last n_s = query_start[s+1] - query_start[s]
-    tokens of each sequence: the query at position pos sees keys 0..pos."""
+    tokens of each sequence: the query at position pos sees keys 0..pos.
+    With prepare=True nothing runs: the checked call is returned as a Prepared."""
     t = _torch()
     d, kv = dims, _torch_dtype(dims.kv_dtype)
     dev = q.device
@@ -244,15 +287,16 @@ def pa_chunk_attention(dims: pa_dims, q, k_cache, v_cache, block_tables, context
             raise ValueError("workspace must be a contiguous CUDA tensor on the same device")
         ws_bytes = workspace.numel() * workspace.element_size()
         ws_ptr = ctypes.c_void_p(workspace.data_ptr())
-    st = lib.pa_chunk_attention(ctypes.byref(dims), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
-                                block_tables.data_ptr(), context_lens.data_ptr(), query_start.data_ptr(), T,
-                                int(max_query_len), float(scale), out.data_ptr(), ws_ptr, ws_bytes,
-                                _stream_ptr(stream, dev))
-    _check(st, "pa_chunk_attention")
+    args = (ctypes.byref(dims), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+            context_lens.data_ptr(), query_start.data_ptr(), T, int(max_query_len), float(scale), out.data_ptr(),
+            ws_ptr, ws_bytes, _stream_ptr(stream, dev))
+    return _issue(lib.pa_chunk_attention, args, "pa_chunk_attention", dev, prepare,
+                  (dims, q, k_cache, v_cache, block_tables, context_lens, query_start, out, workspace))
 
 
-def pa_write_kv(dims: pa_dims, k, v, slot_mapping, k_cache, v_cache, stream=None) -> None:
-    """k_cache[slot // B, h, slot % B] = k[t, h] (and v) for every slot >= 0."""
+def pa_write_kv(dims: pa_dims, k, v, slot_mapping, k_cache, v_cache, stream=None, prepare: bool = False):
+    """k_cache[slot // B, h, slot % B] = k[t, h] (and v) for every slot >= 0.
+    With prepare=True nothing runs: the checked call is returned as a Prepared."""
     t = _torch()
     d, kv = dims, _torch_dtype(dims.kv_dtype)
     dev = k.device
@@ -263,13 +307,14 @@ def pa_write_kv(dims: pa_dims, k, v, slot_mapping, k_cache, v_cache, stream=None
     cache_shape = (d.num_blocks, d.num_kv_heads, d.block_size, d.head_dim)
     _expect(k_cache, "k_cache", cache_shape, kv, dev)
     _expect(v_cache, "v_cache", cache_shape, kv, dev)
-    st = lib.pa_write_kv(ctypes.byref(dims), k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), T,
-                         k_cache.data_ptr(), v_cache.data_ptr(), _stream_ptr(stream, dev))
-    _check(st, "pa_write_kv")
+    args = (ctypes.byref(dims), k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), T, k_cache.data_ptr(),
+            v_cache.data_ptr(), _stream_ptr(stream, dev))
+    return _issue(lib.pa_write_kv, args, "pa_write_kv", dev, prepare, (dims, k, v, slot_mapping, k_cache, v_cache))
 
 
-def pa_copy_blocks(dims: pa_dims, k_cache, v_cache, src_dst_pairs, stream=None) -> None:
-    """Copy whole blocks src -> dst in both caches for each row of src_dst_pairs [P, 2]."""
+def pa_copy_blocks(dims: pa_dims, k_cache, v_cache, src_dst_pairs, stream=None, prepare: bool = False):
+    """Copy whole blocks src -> dst in both caches for each row of src_dst_pairs [P, 2].
+    With prepare=True nothing runs: the checked call is returned as a Prepared."""
     t = _torch()
     d, kv = dims, _torch_dtype(dims.kv_dtype)
     dev = k_cache.device
@@ -278,9 +323,9 @@ def pa_copy_blocks(dims: pa_dims, k_cache, v_cache, src_dst_pairs, stream=None) 
     _expect(k_cache, "k_cache", cache_shape, kv, dev)
     _expect(v_cache, "v_cache", cache_shape, kv, dev)
     _expect(src_dst_pairs, "src_dst_pairs", (P, 2), t.int64, dev)
-    st = lib.pa_copy_blocks(ctypes.byref(dims), k_cache.data_ptr(), v_cache.data_ptr(),
-                            src_dst_pairs.data_ptr(), P, _stream_ptr(stream, dev))
-    _check(st, "pa_copy_blocks")
+    args = (ctypes.byref(dims), k_cache.data_ptr(), v_cache.data_ptr(), src_dst_pairs.data_ptr(), P,
+            _stream_ptr(stream, dev))
+    return _issue(lib.pa_copy_blocks, args, "pa_copy_blocks", dev, prepare, (dims, k_cache, v_cache, src_dst_pairs))
 
 
 def pa_copy_blocks_layers(dims: pa_dims, k_caches, v_caches, src_dst_pairs, stream=None) -> None:
@@ -295,8 +340,9 @@ def pa_copy_blocks_layers(dims: pa_dims, k_caches, v_caches, src_dst_pairs, stre
     _expect(v_caches, "v_caches", pool_shape, kv, dev)
     _expect(src_dst_pairs, "src_dst_pairs", (P, 2), t.int64, dev)
     stride = k_caches.stride(0) * k_caches.element_size()
-    st = lib.pa_copy_blocks_layers(ctypes.byref(dims), k_caches.data_ptr(), v_caches.data_ptr(), L, stride,
-                                   src_dst_pairs.data_ptr(), P, _stream_ptr(stream, dev))
+    with _on(dev):
+        st = lib.pa_copy_blocks_layers(ctypes.byref(dims), k_caches.data_ptr(), v_caches.data_ptr(), L, stride,
+                                       src_dst_pairs.data_ptr(), P, _stream_ptr(stream, dev))
     _check(st, "pa_copy_blocks_layers")
 
 
@@ -332,18 +378,20 @@ class StepGraph:
                       workspace)
         es = k_caches.element_size()
         status = ctypes.c_int32(0)
-        self.handle = lib.pa_step_graph_create(
-            ctypes.byref(dims), L, k_caches.data_ptr(), v_caches.data_ptr(), k_caches.stride(0) * es,
-            q.data_ptr(), q.stride(0) * es, k_new.data_ptr(), v_new.data_ptr(), k_new.stride(0) * es,
-            slot_mapping.data_ptr(), T, block_tables.data_ptr(), context_lens.data_ptr(), float(scale),
-            out.data_ptr(), out.stride(0) * 4, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-            ctypes.byref(status))
+        with _on(dev):
+            self.handle = lib.pa_step_graph_create(
+                ctypes.byref(dims), L, k_caches.data_ptr(), v_caches.data_ptr(), k_caches.stride(0) * es,
+                q.data_ptr(), q.stride(0) * es, k_new.data_ptr(), v_new.data_ptr(), k_new.stride(0) * es,
+                slot_mapping.data_ptr(), T, block_tables.data_ptr(), context_lens.data_ptr(), float(scale),
+                out.data_ptr(), out.stride(0) * 4, workspace.data_ptr(),
+                workspace.numel() * workspace.element_size(), ctypes.byref(status))
         if not self.handle:
             raise PaError(status.value, "pa_step_graph_create")
         self.device = dev
 
     def launch(self, stream=None) -> None:
-        _check(lib.pa_step_graph_launch(self.handle, _stream_ptr(stream, self.device)), "pa_step_graph_launch")
+        with _on(self.device):
+            _check(lib.pa_step_graph_launch(self.handle, _stream_ptr(stream, self.device)), "pa_step_graph_launch")
 
     def close(self) -> None:
         if self.handle:
@@ -393,9 +441,10 @@ def pa_swap_blocks(dims: pa_dims, k_cache, v_cache, host_k, host_v, pairs, direc
     es = k_cache.element_size()
     dstride = k_cache.stride(0) * es if layered else 0
     hstride = host_k.stride(0) * es if layered else 0
-    _check(lib.pa_swap_blocks(ctypes.byref(dims), k_cache.data_ptr(), v_cache.data_ptr(), host_k.data_ptr(),
-                              host_v.data_ptr(), nh, L, dstride, hstride, pairs.data_ptr(), P, int(direction),
-                              _stream_ptr(stream, dev)), "pa_swap_blocks")
+    with _on(dev):
+        _check(lib.pa_swap_blocks(ctypes.byref(dims), k_cache.data_ptr(), v_cache.data_ptr(), host_k.data_ptr(),
+                                  host_v.data_ptr(), nh, L, dstride, hstride, pairs.data_ptr(), P, int(direction),
+                                  _stream_ptr(stream, dev)), "pa_swap_blocks")
 
 
 def _swap_seq(fn, dev_pool, host_pool, seq, name):
@@ -421,7 +470,35 @@ def pa_seq_swap_in(dev_pool, host_pool, host_seq: int):
     return _swap_seq(lib.pa_seq_swap_in, dev_pool, host_pool, host_seq, "pa_seq_swap_in")
 
 
+def _host_device_pair(host, device, what):
+    if host.is_cuda or not device.is_cuda:
+        raise ValueError(f"{what}: expected one host tensor and one CUDA tensor")
+    if not host.is_contiguous() or not device.is_contiguous():
+        raise ValueError(f"{what}: tensors must be contiguous")
+    nbytes = host.numel() * host.element_size()
+    if device.numel() * device.element_size() != nbytes:
+        raise ValueError(f"{what}: byte sizes differ")
+    return nbytes
+
+
+def pa_copy_to_device(dst, src, stream=None, prepare: bool = False):
+    """Copy host tensor `src` into CUDA tensor `dst` (same byte size) on `stream`,
+    asynchronously when `src` is pinned.  prepare=True returns a Prepared."""
+    n = _host_device_pair(src, dst, "pa_copy_to_device")
+    args = (dst.data_ptr(), src.data_ptr(), n, _stream_ptr(stream, dst.device))
+    return _issue(lib.pa_copy_to_device, args, "pa_copy_to_device", dst.device, prepare, (dst, src))
+
+
+def pa_copy_to_host(dst, src, stream=None, prepare: bool = False):
+    """Copy CUDA tensor `src` into host tensor `dst` (same byte size) on `stream`,
+    asynchronously when `dst` is pinned.  prepare=True returns a Prepared."""
+    n = _host_device_pair(dst, src, "pa_copy_to_host")
+    args = (dst.data_ptr(), src.data_ptr(), n, _stream_ptr(stream, src.device))
+    return _issue(lib.pa_copy_to_host, args, "pa_copy_to_host", src.device, prepare, (dst, src))
+
+
 def pa_device_errors(clear: bool = True) -> int:
+    """The current device's sticky PA_DEVERR_* bits (see pa.h); `clear` resets them."""
     flags = ctypes.c_uint32(0)
     _check(lib.pa_device_errors(ctypes.byref(flags), 1 if clear else 0), "pa_device_errors")
     return int(flags.value)
@@ -437,8 +514,9 @@ def pa_selftest_bounded_wait(limit, status, stream=None) -> None:
     when the wait gives up."""
     if status.numel() < 1 or status.element_size() != 4 or not status.is_cuda:
         raise ValueError("status must be a 4-byte CUDA tensor")
-    _check(lib.pa_selftest_bounded_wait(int(limit), status.data_ptr(), _stream_ptr(stream, status.device)),
-           "pa_selftest_bounded_wait")
+    with _on(status.device):
+        rc = lib.pa_selftest_bounded_wait(int(limit), status.data_ptr(), _stream_ptr(stream, status.device))
+    _check(rc, "pa_selftest_bounded_wait")
 
 
 # ------------------------------------------------------------------ host allocator

@@ -17,16 +17,22 @@ __device__ unsigned int g_device_error_word;
 constexpr int kMaxDevices = 64;
 constexpr int kDefaultPartition = 512;
 
+// The error word's device address in the current context, looked up with
+// cudaGetSymbolAddress and cached per device together with the context id, so
+// a context created after a device reset gets a fresh lookup.
 unsigned int *error_word() {
     static std::mutex mu;
+    static unsigned long long ctx_of[kMaxDevices] = {};
     static unsigned int *cache[kMaxDevices] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     std::lock_guard<std::mutex> lock(mu);
-    if (!cache[dev]) {
+    const unsigned long long ctx = pa::current_context_id();
+    if (!cache[dev] || ctx == 0 || ctx != ctx_of[dev]) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_device_error_word) != cudaSuccess) return nullptr;
         cache[dev] = static_cast<unsigned int *>(p);
+        ctx_of[dev] = pa::current_context_id();   // the lookup makes the primary context current
     }
     return cache[dev];
 }
@@ -483,6 +489,24 @@ int32_t pa_swap_blocks(const pa_dims *dims, void *k_cache, void *v_cache, void *
     return to_status(pa::launch_swap_blocks(hk, hv, k_cache, v_cache, pairs, num_pairs, block_bytes, num_layers,
                                             host_layer_stride_bytes, dev_layer_stride_bytes, num_host_blocks,
                                             dims->num_blocks, err, st));
+}
+
+int32_t pa_copy_to_device(void *dst_device, const void *src_host, size_t bytes, void *stream) {
+    if (bytes == 0) return PA_OK;
+    if (!dst_device || !src_host) return PA_ERR_INVALID;
+    return cudaMemcpyAsync(dst_device, src_host, bytes, cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
+int32_t pa_copy_to_host(void *dst_host, const void *src_device, size_t bytes, void *stream) {
+    if (bytes == 0) return PA_OK;
+    if (!dst_host || !src_device) return PA_ERR_INVALID;
+    return cudaMemcpyAsync(dst_host, src_device, bytes, cudaMemcpyDeviceToHost, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
 }
 
 int32_t pa_device_errors(uint32_t *flags, int32_t clear) {

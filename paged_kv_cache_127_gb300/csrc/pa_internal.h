@@ -171,6 +171,12 @@ int32_t decode_call(const pa_dims *dims, const void *q, const void *k_cache, con
 cudaError_t make_cache_tensor_map(CUtensorMap *map, const void *cache, bool bf16, int D, int B,
                                   long long block_heads, int head_group);
 
+// Process-unique id of the calling thread's current CUDA context, or 0 when
+// no context is current or the driver cannot say.  A device reset destroys
+// the primary context; the one created after it has a new id, so addresses
+// cached under the old id are known to be stale.
+unsigned long long current_context_id();
+
 // Chunk attention: work list, tensor-core partition kernel, split-K merge.
 cudaError_t launch_chunk_plan(const ChunkArgs &a, cudaStream_t st);
 cudaError_t launch_chunk_mma_f16(const ChunkArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,

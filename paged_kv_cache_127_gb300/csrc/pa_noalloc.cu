@@ -11,13 +11,15 @@
 // bytes.  Every GPU that loads the library holds it until the process exits.
 // Host code cannot use the array's name as a device address, so the entry
 // point looks up the real device address with cudaGetSymbolAddress the first
-// time it runs on each device (with that device current) and caches it.
+// time it runs on each device (with that device current) and caches it, keyed
+// by the CUDA context so that a device reset leads to a fresh lookup.
 #include <cuda_runtime.h>
 
 #include <cstdint>
 #include <mutex>
 
 #include "../../include/pa.h"
+#include "pa_internal.h"
 
 namespace {
 
@@ -25,17 +27,22 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRA
 
 constexpr int kMaxDevices = 64;
 
-// Device address of g_noalloc_scratch on the current device, looked up once per device.
+// Device address of g_noalloc_scratch in the current context.  It is looked
+// up once per device and cached with the context's id; when the id changes
+// (the device was reset and its primary context rebuilt) it is looked up again.
 void *scratch_for_current_device() {
     static std::mutex mu;
+    static unsigned long long ctx_of[kMaxDevices] = {};
     static void *addr[kMaxDevices] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
+    const unsigned long long ctx = pa::current_context_id();
+    if (!addr[dev] || ctx == 0 || ctx != ctx_of[dev]) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
         addr[dev] = p;
+        ctx_of[dev] = pa::current_context_id();   // the lookup makes the primary context current
     }
     return addr[dev];
 }

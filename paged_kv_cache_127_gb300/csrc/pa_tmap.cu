@@ -28,7 +28,32 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     });
     return fn;
 }
+
+template <class Fn>
+Fn driver_fn(const char *name, unsigned int version) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, version, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        return reinterpret_cast<Fn>(p);
+    return nullptr;
+}
 }  // namespace
+
+unsigned long long current_context_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        get_current = driver_fn<PFN_cuCtxGetCurrent_v4000>("cuCtxGetCurrent", 4000);
+        get_id = driver_fn<PFN_cuCtxGetId_v12000>("cuCtxGetId", 12000);
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    unsigned long long id = 0;
+    return get_id(ctx, &id) == CUDA_SUCCESS ? id : 0;
+}
 
 cudaError_t make_cache_tensor_map(CUtensorMap *map, const void *cache, bool bf16, int D, int B,
                                   long long block_heads, int head_group) {

@@ -53,14 +53,28 @@ def make_rng(seed: int) -> np.random.Generator:
 
 # ---------------------------------------------------------------- dtype helpers
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
-    """Round float32 values to bfloat16 (round to nearest even); return the bits."""
+    """Round float32 values to bfloat16 (round to nearest even); return the bits.
+
+    Works in 32-bit integers, a few million elements at a time: adding 0x7FFF
+    plus the kept part's lowest bit can wrap around only for negative NaN
+    payloads, and every NaN is replaced by the canonical quiet NaN afterwards."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    u = x.view(np.uint32).astype(np.uint64)
-    rounded = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
-    nan = np.isnan(x)
-    if nan.any():
-        rounded[nan] = 0x7FC0
-    return rounded
+    flat = x.reshape(-1)
+    out = np.empty(flat.shape, dtype=np.uint16)
+    step = 1 << 22
+    for i in range(0, flat.size, step):
+        part = flat[i:i + step]
+        u = part.view(np.uint32)
+        r = (u >> np.uint32(16)) & np.uint32(1)
+        r += u
+        r += np.uint32(0x7FFF)
+        r >>= np.uint32(16)
+        o = out[i:i + step]
+        o[:] = r
+        nan = np.isnan(part)
+        if nan.any():
+            o[nan] = 0x7FC0
+    return out.reshape(x.shape)
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:

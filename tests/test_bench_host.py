@@ -1,12 +1,15 @@
 """Host-side pieces of bench.py: the multi-rank timing reduction over gloo
-(world size 2, CPU only) and the CPU-oracle reference arm on the tiny workload."""
+(world size 2, CPU only), the CPU-oracle reference arm on the tiny workload
+(all host cores, its own allocator model, no product library loaded)."""
 import io
 import json
 import os
 import socket
+import subprocess
 import sys
 from contextlib import redirect_stdout
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -71,8 +74,41 @@ def test_reference_arm_runs_the_oracle_on_cpu(monkeypatch):
     line = json.loads(buf.getvalue().strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
     assert line["metric"] == bench.METRIC
-    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == bench.host_cores()
+    assert line["cpu_baseline"]["cpu_model"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+    # the same workload description as the GPU arm prints
+    for key in ("num_q_heads", "num_kv_heads", "head_dim", "block_size", "num_blocks", "context_tokens",
+                "kv_bytes_per_step", "partition_size"):
+        assert key in line["config"]
+
+
+def test_reference_arm_loads_no_product_library():
+    code = ("import sys, io, contextlib; sys.path.insert(0, %r); import bench\n"
+            "with contextlib.redirect_stdout(io.StringIO()):\n"
+            "    bench.main(['--impl', 'reference', '--workload', 'tiny', '--steps', '3', '--warmup', '3'])\n"
+            "maps = open('/proc/self/maps').read()\n"
+            "print('libpa.so' in maps, 'paged_kv_cache_127_gb300.binding' in sys.modules)\n" % ROOT)
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "LOCAL_RANK", "WORLD_SIZE")}
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.split() == ["False", "False"]
+
+
+@pytest.mark.parametrize("name", ["tiny", "mha7b", "gqa8b_b16", "gqa8b_b32", "prefix_cow", "long70b",
+                                  "verify8b", "prefill8b"])
+def test_reference_allocator_builds_the_product_allocator_step(name):
+    # the reference arm's inputs come from the oracle's block manager; they must
+    # be the very tables, lengths, slots and pairs the product allocator makes
+    sys.path.insert(0, ROOT)
+    import bench
+    from paged_kv_cache_127_gb300 import binding as pa
+    from paged_kv_cache_127_gb300 import workloads
+    a = workloads.build_step(name, seed=0, values=False, binding=pa)
+    b = workloads.build_step(name, seed=0, values=False, binding=bench._OracleAllocator)
+    for f in ("tables", "lens", "slots", "pairs", "free_order"):
+        np.testing.assert_array_equal(getattr(a, f), getattr(b, f), err_msg=f)
+    assert a.num_blocks == b.num_blocks and a.max_blocks == b.max_blocks
 
 
 def test_prefix_cache_mode_bounds_its_repetitions(monkeypatch):
