@@ -593,8 +593,13 @@ def run_ours(args):
     # all of its inputs host -> device (one packed pa_copy_to_device) and its
     # output device -> host (pa_copy_to_host); steps are double-buffered over
     # three streams, so step i's copies overlap the compute of steps i - 1 and
-    # i + 1, and the host collects step i - 1's result before enqueueing i + 1.
-    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    # i + 1.  The host orders the buffers: it waits for step i's inputs to land
+    # before it enqueues step i's kernels (the GPU is still busy with step
+    # i - 1 then), and collects step i - 1's result before it reuses that
+    # step's buffers for step i + 1.  So the compute stream carries no
+    # cross-stream waits, and consecutive steps' kernels keep their
+    # programmatic-launch overlap.
+    e2e_steps = max(1, args.e2e_steps)
     s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
     h_outs = [torch.empty((S, Hq, D), dtype=torch.float32).pin_memory() for _ in range(2)]
     h2d = [pa.pa_copy_to_device(d_ins[b], h_in, s_in, prepare=True) for b in range(2)]
@@ -606,13 +611,9 @@ def run_ours(args):
     def e2e_loop(n):
         for i in range(n):
             b = i & 1
-            if i >= 2:
-                s_in.wait_event(ev_cmp[b])      # step i - 2 has read input buffer b
-            h2d[b]()
+            h2d[b]()                            # buffer b's last user, step i - 2, is complete
             ev_in[b].record(s_in)
-            stream.wait_event(ev_in[b])
-            if i >= 2:
-                stream.wait_event(ev_out[b])    # step i - 2's output has reached the host
+            ev_in[b].synchronize()              # step i's inputs are on the device
             bufs[b].step_calls()
             ev_cmp[b].record(stream)
             s_out.wait_event(ev_cmp[b])
@@ -736,39 +737,28 @@ def run_chunk(args):
     umma = n * G >= 64                                # long chunks: the tcgen05 kernel, no split-K merge
     split = step.max_blocks * step.block_size > step.partition_size and not umma
     launches_per_step = 1 + 2 + (1 if split else 0)   # write_kv, plan, chunk kernel, merge
-    ev = []
+    write = pa.pa_write_kv(dims, d_k, d_v, d_slots, d_kc, d_vc, stream, prepare=True)
+    attend = pa.pa_chunk_attention(dims, d_q, d_kc, d_vc, d_tables, d_lens, d_qs, step.scale, d_out, n, ws, stream,
+                                   prepare=True)
 
-    def device_step(record=False):
-        pa.pa_write_kv(dims, d_k, d_v, d_slots, d_kc, d_vc, stream)
-        if record:
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-        pa.pa_chunk_attention(dims, d_q, d_kc, d_vc, d_tables, d_lens, d_qs, step.scale, d_out, n, ws, stream)
-        if record:
-            e1.record(stream)
-            ev.append((e0, e1))
+    def device_step():
+        write()
+        attend()
 
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
     pa.pa_device_errors(clear=True)
     sampler = ClockSampler(device.index).start() if rank == 0 else None
     for _ in range(args.warmup):
         device_step()
     torch.cuda.synchronize(device)
     barrier(dist, device)
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    # the decode call is bracketed by CUDA events on every 8th step (an event pair
-    # on every step would cost the step ~2 % by breaking the overlap of the
-    # programmatically dependent launches)
-    for i in range(args.steps):
-        device_step(record=(i % 8 == 0))
-    t1.record(stream)
-    torch.cuda.synchronize(device)
+    ms = reduce_scalar(dist, timed_steps(torch, device_step, stream, args.steps), "max", device) / args.steps
     barrier(dist, device)
+    call_ms = time_back_to_back(torch, attend, stream, BACK_TO_BACK_CALLS // 4)
+    c_med, c_min, _ = time_per_call(torch, attend, stream, COMPONENT_REPS, flush)
     clocks = sampler.stop() if sampler else None
     assert pa.pa_device_errors(clear=True) == 0, "device error flags set during the timed steps"
     assert torch.isfinite(d_out).all().item()
-    ms = reduce_scalar(dist, t0.elapsed_time(t1), "max", device) / args.steps
-    call_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
     kv = step.kv_bytes_unique()      # every visible KV slot once (the last query sees the whole context)
     flops = step.chunk_flops()
     if rank != 0:
@@ -786,6 +776,9 @@ def run_chunk(args):
                  "kernel": ("pa_chunk_attention (plan + tcgen05 chunk kernel)" if umma else
                             "pa_chunk_attention (plan + mma.sync chunk kernel + split-K merge)"),
                  "call_ms": round(call_ms, 5),
+                 "call_ms_single_median": round(c_med, 5), "call_ms_single_min": round(c_min, 5),
+                 "timing": f"mean of {BACK_TO_BACK_CALLS // 4} back-to-back calls between one CUDA event pair; "
+                           f"single-call median/min over {COMPONENT_REPS} event pairs, L2 flushed before each",
                  "bytes": "distinct visible KV slots per call", "flops": "4 * D * Hq per (query, visible key)"})
     line = {
         "metric": "paged chunk-attention query-tokens/s (KV write + causal attention of every new token)",
@@ -794,6 +787,7 @@ def run_chunk(args):
         "vs_baseline": None, "dtype": step.dtype, "data": "synthetic (seeded)",
         "config": {"workload": args.workload, "num_seqs": step.num_seqs, "query_len": n, "num_q_heads": Hq,
                    "num_kv_heads": step.num_kv_heads, "head_dim": D, "block_size": step.block_size,
+                   "partition_size": step.partition_size,
                    "context_tokens": int(step.lens.sum()), "kv_bytes_unique_per_step": kv,
                    "flops_per_step": flops,
                    "l2": f"{kv / 2**20:.0f} MiB of KV per step vs {L2_BYTES / 2**20:.0f} MiB L2; no flush"},
@@ -1262,7 +1256,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default="gqa8b_b16")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--e2e-steps", type=int, default=200,
+                    help="steps of the end-to-end leg (a fixed count, independent of --steps)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweeps", action="store_true",
                     help="skip the other decode workloads in the default gqa8b_b16 run")

@@ -37,6 +37,17 @@
 //                share one head's tile in shared memory and must not write it.
 // A warp whose rows all end before a chunk skips that chunk's arithmetic.
 //
+// Eight consumer warps (HG 4, RW 2): the CTA is launched as three warpgroups
+// at 168 registers a thread, the most that lets 12 warps fit one SM.  The
+// producer's warpgroup hands all but 40 of its registers to the two consumer
+// warpgroups (setmaxnreg: 8 x 232 + 4 x 40 = 12 x 168); one of its warps
+// produces, the other three exit.  With 232 registers a consumer warp takes
+// two full chunks that its rows see in one step: S for all 32 keys, one row
+// maximum and rescale, then P V for both chunks (the second chunk's V
+// fragments loaded over the first's).  Measured on 256 sequences x 5 query
+// tokens: 5.22 TB/s with 9 warps at 168 registers, 5.79 with the register
+// split, 5.99 with the paired chunks.
+//
 // Finish: a row whose context fits in one partition writes out[] directly;
 // otherwise each partition stores (m, l, acc) and the merge kernel combines
 // the row's partitions 0 .. pos / partition_size.
@@ -68,7 +79,10 @@ struct ChunkCfg {
     static constexpr int kTileBytes = kSub * kBoxBytes;  // K (or V) of a chunk, all HG heads
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kConsumers = HG * RW;              // warp w < HG * RW: head w % HG, row tile w / HG
-    static constexpr int kThreads = (kConsumers + 1) * 32;  // + one producer warp
+    // eight consumer warps: a whole warpgroup around the producer warp, so its
+    // registers can be handed to the consumers (setmaxnreg)
+    static constexpr bool kRegSplit = kConsumers == 8;
+    static constexpr int kThreads = (kConsumers + (kRegSplit ? 4 : 1)) * 32;
     static constexpr int kMinBlocks = RW == 1 ? 2 : 1;
     static constexpr int kStagesRaw = PA_CHUNK_STAGE_BUDGET / kMinBlocks / kStageBytes;
     static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
@@ -152,7 +166,14 @@ __global__ void __launch_bounds__(ChunkCfg<D, HG, RW>::kThreads, ChunkCfg<D, HG,
     // ones are claimed from the counter when the issue cursor reaches them, not
     // earlier, so each CTA's last item is taken as late as possible and the
     // largest-first order bounds the tail.
-    if (warp == C::kConsumers) {
+    if (warp >= C::kConsumers) {
+        if constexpr (C::kRegSplit) {
+            // launched at 168 registers a thread (3 warps per scheduler): the
+            // producer warpgroup gives up all but 40, the two consumer warpgroups
+            // take 232 (8 x 232 + 4 x 40 = 12 x 168); one warp of the group produces
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 40;\n" ::: "memory");
+            if (warp > C::kConsumers) return;
+        }
         const uint64_t pol = policy_evict_first();
         int iss = 0;  // chunks issued
         bool ok = true;
@@ -237,6 +258,7 @@ __global__ void __launch_bounds__(ChunkCfg<D, HG, RW>::kThreads, ChunkCfg<D, HG,
     // ------------------------------------------------------------ consumer warps
     // Every consumer warp walks the same items (slot by slot) and chunks
     // (stage by stage).
+    if constexpr (C::kRegSplit) asm volatile("setmaxnreg.inc.sync.aligned.u32 232;\n" ::: "memory");
     uint32_t qa[C::kKS][4];
     int cons = 0;  // chunks consumed by this warp
     for (int seq = 0;; ++seq) {
@@ -293,6 +315,154 @@ __global__ void __launch_bounds__(ChunkCfg<D, HG, RW>::kThreads, ChunkCfg<D, HG,
                 break;
             }
             const int nv = ctb[j / kCPB] < 0 ? 0 : min(16, ntok - j * 16);
+            // two full chunks that some row of this warp sees: one softmax step over 32 keys
+            const bool pair = C::kRegSplit && j + 1 < nchunk && nv == 16 && ctb[(j + 1) / kCPB] >= 0 && ntok - (j + 1) * 16 >= 16 &&
+                              (j + 1) * 16 <= wlim;
+            if (pair) {
+                const int st2 = (cons + 1) % C::kStages;
+                const uint32_t parity2 = (uint32_t)((cons + 1) / C::kStages) & 1u;
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(full0 + 8 * st2, parity2, kWaitLimit))) {
+                    if (lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
+                    timed_out = true;
+                    break;
+                }
+                const uint32_t kstp[2] = {base + (uint32_t)(st * C::kStageBytes) + (uint32_t)(head * C::kHeadSub),
+                                          base + (uint32_t)(st2 * C::kStageBytes) + (uint32_t)(head * C::kHeadSub)};
+                uint32_t bv[C::kNT / 2][4];
+#pragma unroll
+                for (int ntp = 0; ntp < C::kNT / 2; ++ntp) {
+                    const uint32_t addr = kstp[0] + C::kTileBytes + (uint32_t)((ntp >> 2) * C::kBoxBytes) +
+                                          (uint32_t)(((lm & 1) * 8 + lr) * 128) +
+                                          (((uint32_t)(2 * (ntp & 3)) ^ vx) << 4);
+                    ldsm_x4_t(addr, bv[ntp][0], bv[ntp][1], bv[ntp][2], bv[ntp][3]);
+                }
+                float sc[2][2][2][4];
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh)
+                            sc[c][nt][hh][0] = sc[c][nt][hh][1] = sc[c][nt][hh][2] = sc[c][nt][hh][3] = 0.f;
+#pragma unroll
+                for (int ks2 = 0; ks2 < C::kKS / 2; ++ks2) {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt) {
+                            const uint32_t addr = kstp[c] + (uint32_t)((ks2 >> 1) * C::kBoxBytes) +
+                                                  (uint32_t)((nt * 8 + lr) * 128) +
+                                                  (((uint32_t)(4 * (ks2 & 1)) ^ kx) << 4);
+                            uint32_t b0, b1, b2, b3;
+                            ldsm_x4(addr, b0, b1, b2, b3);
+                            const int k0 = 2 * ks2, k1 = 2 * ks2 + 1;
+                            M::mma(sc[c][nt][0], qa[k0][0], qa[k0][1], qa[k0][2], qa[k0][3], b0, b1);
+                            M::mma(sc[c][nt][1], qa[k1][0], qa[k1][1], qa[k1][2], qa[k1][3], b2, b3);
+                        }
+                    }
+                }
+                // logits of the 32 keys: chunk c, keys c2, c2+1, 8+c2, 9+c2 at [4c .. 4c+3]
+                float x0[8], x1[8];
+                const int koff[4] = {0, 1, 8, 9};
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    x0[4 * c + 0] = (sc[c][0][0][0] + sc[c][0][1][0]) * sl;
+                    x0[4 * c + 1] = (sc[c][0][0][1] + sc[c][0][1][1]) * sl;
+                    x0[4 * c + 2] = (sc[c][1][0][0] + sc[c][1][1][0]) * sl;
+                    x0[4 * c + 3] = (sc[c][1][0][1] + sc[c][1][1][1]) * sl;
+                    x1[4 * c + 0] = (sc[c][0][0][2] + sc[c][0][1][2]) * sl;
+                    x1[4 * c + 1] = (sc[c][0][0][3] + sc[c][0][1][3]) * sl;
+                    x1[4 * c + 2] = (sc[c][1][0][2] + sc[c][1][1][2]) * sl;
+                    x1[4 * c + 3] = (sc[c][1][0][3] + sc[c][1][1][3]) * sl;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int kk = (j + c) * 16 + c2 + koff[i];
+                        if (kk > lim0) x0[4 * c + i] = -INFINITY;
+                        if (kk > lim1) x1[4 * c + i] = -INFINITY;
+                    }
+                }
+                float mx0 = x0[0], mx1 = x1[0];
+#pragma unroll
+                for (int i = 1; i < 8; ++i) {
+                    mx0 = fmaxf(mx0, x0[i]);
+                    mx1 = fmaxf(mx1, x1[i]);
+                }
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                if (__any_sync(0xffffffffu, mx0 > m0 || mx1 > m1)) {
+                    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                    const float al0 = mn0 == -INFINITY ? 1.f : ex2(m0 - mn0);
+                    const float al1 = mn1 == -INFINITY ? 1.f : ex2(m1 - mn1);
+                    l0 *= al0;
+                    l1 *= al1;
+#pragma unroll
+                    for (int nt = 0; nt < C::kNT; ++nt) {
+                        o[nt][0] *= al0;
+                        o[nt][1] *= al0;
+                        o[nt][2] *= al1;
+                        o[nt][3] *= al1;
+                    }
+                    m0 = mn0;
+                    m1 = mn1;
+                }
+                const float mu0 = m0 == -INFINITY ? 0.f : m0;
+                const float mu1 = m1 == -INFINITY ? 0.f : m1;
+                float p0[8], p1[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    p0[i] = ex2(x0[i] - mu0);
+                    p1[i] = ex2(x1[i] - mu1);
+                }
+                l0 += ((p0[0] + p0[1]) + (p0[2] + p0[3])) + ((p0[4] + p0[5]) + (p0[6] + p0[7]));
+                l1 += ((p1[0] + p1[1]) + (p1[2] + p1[3])) + ((p1[4] + p1[5]) + (p1[6] + p1[7]));
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    if (c == 1) {  // the second chunk's V fragments, over the first chunk's
+#pragma unroll
+                        for (int ntp = 0; ntp < C::kNT / 2; ++ntp) {
+                            const uint32_t addr = kstp[1] + C::kTileBytes + (uint32_t)((ntp >> 2) * C::kBoxBytes) +
+                                                  (uint32_t)(((lm & 1) * 8 + lr) * 128) +
+                                                  (((uint32_t)(2 * (ntp & 3)) ^ vx) << 4);
+                            ldsm_x4_t(addr, bv[ntp][0], bv[ntp][1], bv[ntp][2], bv[ntp][3]);
+                        }
+                    }
+                    const uint32_t h0a = M::pack(p0[4 * c], p0[4 * c + 1]), h1a = M::pack(p1[4 * c], p1[4 * c + 1]);
+                    const uint32_t h0b = M::pack(p0[4 * c + 2], p0[4 * c + 3]);
+                    const uint32_t h1b = M::pack(p1[4 * c + 2], p1[4 * c + 3]);
+                    const float2 f0a = M::unpack(h0a), f1a = M::unpack(h1a);
+                    const float2 f0b = M::unpack(h0b), f1b = M::unpack(h1b);
+                    const uint32_t l0a = M::pack(p0[4 * c] - f0a.x, p0[4 * c + 1] - f0a.y);
+                    const uint32_t l1a = M::pack(p1[4 * c] - f1a.x, p1[4 * c + 1] - f1a.y);
+                    const uint32_t l0b = M::pack(p0[4 * c + 2] - f0b.x, p0[4 * c + 3] - f0b.y);
+                    const uint32_t l1b = M::pack(p1[4 * c + 2] - f1b.x, p1[4 * c + 3] - f1b.y);
+#pragma unroll
+                    for (int ntq = 0; ntq < C::kNT / 4; ++ntq) {
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int ntp = 2 * ntq + u;
+                            M::mma(o[4 * ntq + 2 * u], h0a, h1a, h0b, h1b, bv[ntp][0], bv[ntp][1]);
+                            M::mma(o[4 * ntq + 2 * u + 1], h0a, h1a, h0b, h1b, bv[ntp][2], bv[ntp][3]);
+                        }
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int ntp = 2 * ntq + u;
+                            M::mma(o[4 * ntq + 2 * u], l0a, l1a, l0b, l1b, bv[ntp][0], bv[ntp][1]);
+                            M::mma(o[4 * ntq + 2 * u + 1], l0a, l1a, l0b, l1b, bv[ntp][2], bv[ntp][3]);
+                        }
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(empty0 + 8 * st);
+                    mbar_arrive(empty0 + 8 * st2);
+                }
+                cons += 2;
+                ++j;
+                continue;
+            }
             if (nv > 0 && j * 16 <= wlim) {
                 const uint32_t kst = base + (uint32_t)(st * C::kStageBytes) + (uint32_t)(head * C::kHeadSub);
                 const uint32_t vst = kst + C::kTileBytes;
