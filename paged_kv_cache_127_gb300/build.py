@@ -59,10 +59,27 @@ def _run(cmd, verbose):
     return r
 
 
+def _switches():
+    """Build-time kernel switches taken from the environment: PA_DECODE_CUDA_CORE=1
+    builds the 16-bit decode with q.k and p.v on the CUDA cores instead of the
+    tensor cores (an alternative for comparing the two; the default is off)."""
+    flags = []
+    if os.environ.get("PA_DECODE_CUDA_CORE", "0") not in ("", "0"):
+        flags.append("-DPA_DECODE_CUDA_CORE=1")
+    return flags
+
+
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     """Compile and link libpa.so; return its path."""
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
+    extra_flags = [*extra_flags, *_switches()]
+    # a change of switches rebuilds everything
+    stamp = os.path.join(BUILD, "switches.txt")
+    want = " ".join(_switches())
+    have = open(stamp).read() if os.path.exists(stamp) else None
+    if have != want:
+        force = True
     headers = _headers()
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     jobs = []
@@ -86,6 +103,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         tmp = LIBRARY + f".tmp{os.getpid()}"
         _run([nvcc, *ARCH, "-shared", "-cudart", "static", *objects, "-o", tmp], verbose)
         os.replace(tmp, LIBRARY)
+    with open(stamp, "w") as f:
+        f.write(want)
     return LIBRARY
 
 

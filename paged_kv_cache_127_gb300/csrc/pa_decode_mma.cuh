@@ -42,6 +42,8 @@
 #include <cuda.h>
 
 #include <cmath>
+#include <cstring>
+#include <type_traits>
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
@@ -56,6 +58,14 @@ namespace pa {
 // box is one half for the HG heads (HG x 16 rows x 128 bytes, 8 KB at HG = 4),
 // written with the 128-byte swizzle.  Bigger boxes than one head's 2 KB keep
 // the bulk-copy engine at HBM speed.
+// Build-time switch: 1 computes q.k and p.v of the 16-bit decode on the CUDA
+// cores instead of the tensor cores, everything else unchanged (for comparing
+// the two on otherwise identical sources; the build takes it from the
+// environment variable of the same name).
+#ifndef PA_DECODE_CUDA_CORE
+#define PA_DECODE_CUDA_CORE 0
+#endif
+
 #ifndef PA_MMA_STAGE_BUDGET
 #define PA_MMA_STAGE_BUDGET (96 * 1024)
 #endif
@@ -88,6 +98,189 @@ struct MmaCfg {
     static_assert(kHeadSub % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
+
+#if PA_DECODE_CUDA_CORE
+// Build-time alternative (PA_DECODE_CUDA_CORE=1) for a same-sources comparison
+// of the tensor-core choice: the consumer warps compute q.k and p.v with fp32
+// FMAs on the CUDA cores; the producer warp, the stage ring, the work items,
+// the masking and the finish are those of the tensor-core consumer.
+//   q.k   lane (t = lane % 16, half = lane / 16) takes token t of the chunk and
+//         one half of D for each of the G query heads (q read through L1), and
+//         one shuffle adds the two halves;
+//   softmax  per query head over the chunk's 16 tokens (shuffle max / sum);
+//   p.v   lane takes D / 32 consecutive columns of every head and the
+//         weights of each token by shuffle.
+template <typename T>
+__device__ __forceinline__ float2 widen2(uint32_t w) {
+    if constexpr (std::is_same<T, __nv_bfloat16>::value)
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    else {
+        __half2 h;
+        memcpy(&h, &w, 4);
+        return __half22float2(h);
+    }
+}
+
+template <typename T, int D, int B, int HG>
+__device__ __forceinline__ void consumer_cuda_core(const DecodeArgs &a, uint32_t base, uint32_t full0, uint32_t empty0,
+                                                   uint32_t ifull0, uint32_t iempty0, const int4 *info,
+                                                   const int32_t *tbl, int warp, int lane) {
+    using C = MmaCfg<D, HG>;
+    using E = Elem<T>;
+    constexpr int kCPB = B / 16;
+    constexpr int kHalf = D / 2;      // dims of one lane's q.k half
+    constexpr int kPer = D / 32;      // output columns per lane
+    const unsigned full = 0xffffffffu;
+    const int G = a.Hq / a.Hkv;
+    const float sl = a.scale * 1.4426950408889634f;
+    const int t = lane & 15, hf = lane >> 4;
+    const int d0 = kPer * lane;
+    int cons = 0;
+    for (int seq = 0;; ++seq) {
+        const int slot = seq % C::kSlots;
+        if (!mbar_wait_bounded(ifull0 + 8 * slot, (uint32_t)(seq / C::kSlots) & 1u, kWaitLimit)) {
+            if (lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
+            break;
+        }
+        const int4 e0 = info[2 * slot];
+        const int4 e1 = info[2 * slot + 1];
+        if (!e1.z) break;  // no more work
+        const int s = e0.x, p = e0.y, ntok = e0.z, np = e0.w;
+        const int kvh = e1.x + warp;
+        const int nchunk = e1.y;
+        const int32_t *ctb = tbl + slot * C::kTblCap;
+        const T *qb = static_cast<const T *>(a.q) + ((size_t)s * a.Hq + (size_t)kvh * G) * D;
+        float o[8][kPer], m_run[8], l_run[8];
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+            m_run[g] = -INFINITY;
+            l_run[g] = 0.f;
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) o[g][i] = 0.f;
+        }
+        bool timed_out = false;
+        for (int j = 0; j < nchunk; ++j) {
+            const int st = cons % C::kStages;
+            const uint32_t parity = (uint32_t)(cons / C::kStages) & 1u;
+            if (!__all_sync(full, mbar_wait_bounded(full0 + 8 * st, parity, kWaitLimit))) {
+                if (lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
+                timed_out = true;
+                break;
+            }
+            const int nv = ctb[j / kCPB] < 0 ? 0 : min(16, ntok - j * 16);
+            const uint32_t kst = base + (uint32_t)(st * C::kStageBytes) + (uint32_t)(warp * C::kHeadSub);
+            const uint32_t vst = kst + C::kTileBytes;
+            if (nv > 0) {
+                // ---- S = q K^T: token t, half hf of D
+                float sd[8];
+#pragma unroll
+                for (int g = 0; g < 8; ++g) sd[g] = 0.f;
+#pragma unroll
+                for (int c = 0; c < kHalf / 8; ++c) {
+                    const int e = hf * kHalf + 8 * c;  // first element of this 16-byte chunk
+                    const uint32_t addr = kst + (uint32_t)((e / 64) * C::kBoxBytes) + (uint32_t)(t * 128) +
+                                          ((uint32_t)(((e % 64) / 8) ^ (t & 7)) << 4);
+                    float kf[8];
+                    E::unpack(lds128(addr), kf);
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        if (g < G) {
+                            float qf[8];
+                            E::unpack(__ldg(reinterpret_cast<const uint4 *>(qb + (size_t)g * D + e)), qf);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) sd[g] = fmaf(qf[i], kf[i], sd[g]);
+                        }
+                    }
+                }
+                // ---- online softmax per head over the chunk's tokens (lanes t and t + 16 agree)
+                float pw[8];
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    pw[g] = 0.f;
+                    if (g < G) {
+                        const float dot = sd[g] + __shfl_xor_sync(full, sd[g], 16);
+                        const float x = t < nv ? dot * sl : -INFINITY;
+                        float mx = x;
+                        mx = fmaxf(mx, __shfl_xor_sync(full, mx, 1));
+                        mx = fmaxf(mx, __shfl_xor_sync(full, mx, 2));
+                        mx = fmaxf(mx, __shfl_xor_sync(full, mx, 4));
+                        mx = fmaxf(mx, __shfl_xor_sync(full, mx, 8));
+                        if (mx > m_run[g]) {  // the same in every lane
+                            const float al = ex2(m_run[g] - mx);
+                            l_run[g] *= al;
+#pragma unroll
+                            for (int i = 0; i < kPer; ++i) o[g][i] *= al;
+                            m_run[g] = mx;
+                        }
+                        const float pv = ex2(x - m_run[g]);  // 0 past the context
+                        float ps = pv;
+                        ps += __shfl_xor_sync(full, ps, 1);
+                        ps += __shfl_xor_sync(full, ps, 2);
+                        ps += __shfl_xor_sync(full, ps, 4);
+                        ps += __shfl_xor_sync(full, ps, 8);
+                        l_run[g] += ps;
+                        pw[g] = pv;
+                    }
+                }
+                // ---- O += p V: columns d0 .. d0 + kPer of every head; tokens past the context are not read
+#pragma unroll
+                for (int tt = 0; tt < 16; ++tt) {
+                    if (tt < nv) {
+                        const uint32_t vaddr = vst + (uint32_t)((d0 / 64) * C::kBoxBytes) + (uint32_t)(tt * 128) +
+                                               ((uint32_t)(((d0 % 64) / 8) ^ (tt & 7)) << 4) + (uint32_t)((d0 % 8) * 2);
+                        float vf[kPer];
+                        if constexpr (kPer == 4) {
+                            uint32_t w0, w1;
+                            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(w0), "=r"(w1) : "r"(vaddr));
+                            const float2 a0 = widen2<T>(w0), a1 = widen2<T>(w1);
+                            vf[0] = a0.x, vf[1] = a0.y, vf[2] = a1.x, vf[3] = a1.y;
+                        } else {
+                            uint32_t w0;
+                            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w0) : "r"(vaddr));
+                            const float2 a0 = widen2<T>(w0);
+                            vf[0] = a0.x, vf[1] = a0.y;
+                        }
+#pragma unroll
+                        for (int g = 0; g < 8; ++g) {
+                            if (g < G) {
+                                const float pg = __shfl_sync(full, pw[g], tt);
+#pragma unroll
+                                for (int i = 0; i < kPer; ++i) o[g][i] = fmaf(pg, vf[i], o[g][i]);
+                            }
+                        }
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * st);
+            ++cons;
+        }
+        if (timed_out) break;
+        // ---- finish: whole-sequence items write out[], partitions their (m, l, acc)
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+            if (g < G) {
+                const int h = kvh * G + g;
+                if (np == 1) {
+                    const float inv = l_run[g] > 0.f ? 1.f / l_run[g] : 0.f;
+                    float *orow = a.out + ((size_t)s * a.Hq + h) * D + d0;
+#pragma unroll
+                    for (int i = 0; i < kPer; ++i) orow[i] = o[g][i] * inv;
+                } else {
+                    const size_t r = ((size_t)s * a.Hq + h) * a.max_parts + p;
+                    float *acc = a.ws_acc + r * D + d0;
+#pragma unroll
+                    for (int i = 0; i < kPer; ++i) acc[i] = o[g][i];
+                    if (lane == 0) *reinterpret_cast<float2 *>(a.ws_ml + 2 * r) = make_float2(m_run[g], l_run[g]);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(iempty0 + 8 * slot);
+    }
+}
+#endif  // PA_DECODE_CUDA_CORE
 
 template <typename T, int D, int B, int HG>
 __global__ void __launch_bounds__(MmaCfg<D, HG>::kThreads, 2)
@@ -278,6 +471,10 @@ __global__ void __launch_bounds__(MmaCfg<D, HG>::kThreads, 2)
     // ------------------------------------------------------------ consumer warps
     // Every consumer warp walks the same sequence of items (slot by slot) and
     // chunks (stage by stage); warp w computes the item's KV head g0 + w.
+#if PA_DECODE_CUDA_CORE
+    consumer_cuda_core<T, D, B, HG>(a, base, full0, empty0, ifull0, iempty0, info, tbl, warp, lane);
+    return;
+#endif
     uint32_t qa[C::kKS][2];
     int cons = 0;  // chunks consumed by this warp
     for (int seq = 0;; ++seq) {

@@ -206,3 +206,15 @@ def test_step_graph_refuses_overlapping_layers_on_the_host(pa):
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
         assert status() == pa.PA_ERR_CUDA
+
+
+def test_build_switch_of_the_cuda_core_comparison(monkeypatch):
+    # PA_DECODE_CUDA_CORE=1 builds the 16-bit decode with CUDA-core arithmetic
+    # (for comparing it with the tensor-core kernel); unset or 0 is the default build
+    from paged_kv_cache_127_gb300 import build
+    monkeypatch.delenv("PA_DECODE_CUDA_CORE", raising=False)
+    assert build._switches() == []
+    monkeypatch.setenv("PA_DECODE_CUDA_CORE", "0")
+    assert build._switches() == []
+    monkeypatch.setenv("PA_DECODE_CUDA_CORE", "1")
+    assert build._switches() == ["-DPA_DECODE_CUDA_CORE=1"]
