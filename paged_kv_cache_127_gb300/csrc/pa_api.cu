@@ -211,6 +211,40 @@ cudaError_t cache_tensor_map(const void *ptr, bool bf16, int D, int B, long long
     return cudaSuccess;
 }
 
+// The query tensor map of the tcgen05 chunk path, re-encoded only when the
+// queries' pointer or shape changes (per host thread).
+cudaError_t query_tensor_map(const void *q, bool bf16, int D, int Hq, long long T, int G, CUtensorMap *out) {
+    struct Entry {
+        const void *ptr = nullptr;
+        long long T = 0;
+        int D = 0, Hq = 0, G = 0;
+        bool bf16 = false;
+        CUtensorMap map;
+    };
+    thread_local Entry cache[2];
+    thread_local int next = 0;
+    for (auto &e : cache)
+        if (e.ptr == q && e.T == T && e.D == D && e.Hq == Hq && e.G == G && e.bf16 == bf16) {
+            *out = e.map;
+            return cudaSuccess;
+        }
+    Entry &e = cache[next];
+    next = (next + 1) % 2;
+    cudaError_t rc = pa::make_query_tensor_map(&e.map, q, bf16, D, Hq, T, G);
+    if (rc != cudaSuccess) {
+        e.ptr = nullptr;
+        return rc;
+    }
+    e.ptr = q;
+    e.T = T;
+    e.D = D;
+    e.Hq = Hq;
+    e.G = G;
+    e.bf16 = bf16;
+    *out = e.map;
+    return cudaSuccess;
+}
+
 int32_t to_status(cudaError_t e) {
     if (e == cudaSuccess) return PA_OK;
     if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
@@ -388,7 +422,12 @@ int32_t pa_chunk_attention(const pa_dims *dims, const void *q, const void *k_cac
     e = pa::launch_chunk_plan(a, st);
     if (e != cudaSuccess) return to_status(e);
     if (umma) {
-        e = bf16 ? pa::launch_chunk_umma_bf16(a, tmk, tmv, st) : pa::launch_chunk_umma_f16(a, tmk, tmv, st);
+        // the tcgen05 kernel loads its query tiles with TMA as well
+        CUtensorMap tmq;
+        e = query_tensor_map(q, bf16, dims->head_dim, dims->num_q_heads, num_tokens,
+                             dims->num_q_heads / dims->num_kv_heads, &tmq);
+        if (e != cudaSuccess) return PA_ERR_CUDA;
+        e = bf16 ? pa::launch_chunk_umma_bf16(a, tmk, tmv, tmq, st) : pa::launch_chunk_umma_f16(a, tmk, tmv, tmq, st);
         return to_status(e);
     }
     e = bf16 ? pa::launch_chunk_mma_bf16(a, tmk, tmv, st) : pa::launch_chunk_mma_f16(a, tmk, tmv, st);

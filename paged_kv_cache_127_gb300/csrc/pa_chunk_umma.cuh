@@ -107,7 +107,7 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
 template <typename T, int D, int B, int MT>
 __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
     chunk_umma_kernel(const ChunkArgs a, const __grid_constant__ CUtensorMap tmk,
-                      const __grid_constant__ CUtensorMap tmv) {
+                      const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmq) {
     using C = UmmaCfg<D, MT>;
     using M = Mma16<T>;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
@@ -172,13 +172,14 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
                 mbar_init(p_full(u, b), 4);
                 mbar_init(o_done(u, b), 1);
             }
-            mbar_init(q_full(u), 4);
+            mbar_init(q_full(u), 1);
             mbar_init(drain_s(u), 1);
             mbar_init(drain_p(u), 1);
         }
         fence_mbar_init();
         prefetch_tmap(&tmk);
         prefetch_tmap(&tmv);
+        prefetch_tmap(&tmq);
     }
     if (warp == 1) tc::tmem_alloc(smem_addr(tslot), C::kTmemCols);
     tc::fence_before_sync();
@@ -193,6 +194,19 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
         const uint64_t pol = policy_evict_last();  // the other row tiles of this head reread these keys
         const CUtensorMap *map = is_v ? &tmv : &tmk;
         const uint32_t ring = kvb + (is_v ? (uint32_t)C::kTile : 0u);
+        if (!is_v && lane == 0) {
+            // the query tiles first: tile u holds rows r0 + 128 u .., i.e. tokens
+            // (r0 + 128 u) / G .. of the sequence's chunk, G heads each; rows of
+            // tokens past the chunk are never used (their keys are all masked)
+            const uint64_t qpol = policy_evict_first();
+            for (int u = 0; u < tiles; ++u) {
+                mbar_arrive_expect_tx(q_full(u), (uint32_t)C::kQTile);
+#pragma unroll
+                for (int sb = 0; sb < C::kSub; ++sb)
+                    tma_load_3d(qtile(u) + (uint32_t)(sb * C::kQHalf), &tmq, sb * 64, kvh * G, qs + (r0 + C::kM * u) / G,
+                                q_full(u), qpol);
+            }
+        }
         int j = 0;
         for (; j < nch; ++j) {
             const int st = j % C::kStages;
@@ -329,23 +343,6 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
         const int h = kvh * G + R % G;
         const int pos = len - n + t;
         const float sl = a.scale * 1.4426950408889634f;
-        {
-            // Q row -> shared memory, 128-byte swizzle (16-byte chunk c of row r at c ^ (r & 7))
-            const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.q) +
-                                                               ((size_t)(qs + (valid ? t : 0)) * a.Hq + h) * D);
-#pragma unroll
-            for (int c = 0; c < D / 8; ++c) {
-                const uint4 v = valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-                const uint32_t addr =
-                    qtile(u) + (uint32_t)((c >> 3) * C::kQHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4));
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
-                             "r"(v.w)
-                             : "memory");
-            }
-            tc::fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(q_full(u));
-        }
         const uint32_t tl = tbase + ((uint32_t)(wq * 32) << 16);
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
@@ -465,22 +462,50 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
             if (lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
         } else if (__all_sync(0xffffffffu, mbar_wait_bounded(o_done(u, last % kSB), (uint32_t)(last / kSB) & 1u,
                                                               kWaitLimit))) {
-            // ---- epilogue: out = O / l for this row
+            // ---- epilogue: out = O / l.  The tile's S MMAs are complete, so its
+            // Q tile is free: each warp stages its 32 rows there, W columns at a
+            // time (rows of W floats, 16-byte chunks swizzled by row), then
+            // writes whole rows to global memory, lanes_per_row lanes per row,
+            // instead of one 16-byte piece of 32 different rows per store.
             tc::fence_after_sync();
+            tc::fence_async_smem();
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            float *orow = a.out + ((size_t)(qs + (valid ? t : 0)) * a.Hq + h) * D;
+            constexpr int W = D / 2;                       // columns per pass
+            constexpr int kRowBytes = W * 4;               // 256 (D 128) or 128 (D 64)
+            constexpr int kRowsPerPiece = 4096 / kRowBytes;  // rows in one 4 KB piece of the warp's Q slice
+            constexpr int kLanesPerRow = kRowBytes / 16;
+            constexpr int kRowsPerStore = 32 / kLanesPerRow;
+            auto stage = [&](int rr, int c) {  // staging address of 16-byte chunk c of row rr
+                return qtile(u) + (uint32_t)((rr / kRowsPerPiece) * C::kQHalf + wq * 32 * 128) +
+                       (uint32_t)((rr % kRowsPerPiece) * kRowBytes) + ((uint32_t)(c ^ (rr & 7)) << 4);
+            };
 #pragma unroll
-            for (int q = 0; q < D / 32; ++q) {
-                uint32_t ov[32];
-                tc::tmem_ld32(tl + o_col(u) + 32u * q, ov);
-                tc::tmem_wait_ld();
-                if (valid) {
+            for (int pass = 0; pass < 2; ++pass) {
+#pragma unroll
+                for (int q = 0; q < W / 32; ++q) {
+                    uint32_t ov[32];
+                    tc::tmem_ld32(tl + o_col(u) + (uint32_t)(pass * W + 32 * q), ov);
+                    tc::tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; i += 4)
-                        *reinterpret_cast<float4 *>(orow + 32 * q + i) =
-                            make_float4(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv,
-                                        __uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv);
+                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(stage(lane, 8 * q + i / 4)),
+                                     "f"(__uint_as_float(ov[i]) * inv), "f"(__uint_as_float(ov[i + 1]) * inv),
+                                     "f"(__uint_as_float(ov[i + 2]) * inv), "f"(__uint_as_float(ov[i + 3]) * inv)
+                                     : "memory");
                 }
+                __syncwarp();
+#pragma unroll 4
+                for (int i = 0; i < 32 / kRowsPerStore; ++i) {
+                    const int rr = i * kRowsPerStore + lane / kLanesPerRow;  // row of this warp's 32
+                    const int c = lane % kLanesPerRow;
+                    const int Rr = r0 + C::kM * u + 32 * wq + rr;
+                    const int tr = Rr / G;
+                    const float4 v = *reinterpret_cast<const float4 *>(smem_raw + (stage(rr, c) - raw));
+                    if (tr < n)
+                        *reinterpret_cast<float4 *>(a.out + ((size_t)(qs + tr) * a.Hq + kvh * G + Rr % G) * D +
+                                                    pass * W + 4 * c) = v;
+                }
+                __syncwarp();
             }
             tc::fence_before_sync();
         } else if (lane == 0) {
@@ -497,7 +522,7 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
 
 template <typename T, int D, int B, int MT>
 cudaError_t launch_chunk_umma_t(const ChunkArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
-                                cudaStream_t st) {
+                                const CUtensorMap &tmq, cudaStream_t st) {
     using C = UmmaCfg<D, MT>;
     static std::atomic<int> configured[kMaxLaunchDevices];
     int one = 0;
@@ -522,24 +547,24 @@ cudaError_t launch_chunk_umma_t(const ChunkArgs &a, const CUtensorMap &tmk, cons
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, chunk_umma_kernel<T, D, B, MT>, a, tmk, tmv);
+    return cudaLaunchKernelEx(&cfg, chunk_umma_kernel<T, D, B, MT>, a, tmk, tmv, tmq);
 }
 
 // Two tiles per CTA once a sequence can fill them (chunk_umma_rows).
 template <typename T, int D, int B>
 cudaError_t dispatch_chunk_umma_mt(const ChunkArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
-                                   cudaStream_t st) {
-    return a.umma_rows == 256 ? launch_chunk_umma_t<T, D, B, 2>(a, tmk, tmv, st)
-                              : launch_chunk_umma_t<T, D, B, 1>(a, tmk, tmv, st);
+                                   const CUtensorMap &tmq, cudaStream_t st) {
+    return a.umma_rows == 256 ? launch_chunk_umma_t<T, D, B, 2>(a, tmk, tmv, tmq, st)
+                              : launch_chunk_umma_t<T, D, B, 1>(a, tmk, tmv, tmq, st);
 }
 
 template <typename T>
 cudaError_t dispatch_chunk_umma(const ChunkArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
-                                cudaStream_t st) {
-    if (a.D == 64 && a.B == 16) return dispatch_chunk_umma_mt<T, 64, 16>(a, tmk, tmv, st);
-    if (a.D == 64 && a.B == 32) return dispatch_chunk_umma_mt<T, 64, 32>(a, tmk, tmv, st);
-    if (a.D == 128 && a.B == 16) return dispatch_chunk_umma_mt<T, 128, 16>(a, tmk, tmv, st);
-    if (a.D == 128 && a.B == 32) return dispatch_chunk_umma_mt<T, 128, 32>(a, tmk, tmv, st);
+                                const CUtensorMap &tmq, cudaStream_t st) {
+    if (a.D == 64 && a.B == 16) return dispatch_chunk_umma_mt<T, 64, 16>(a, tmk, tmv, tmq, st);
+    if (a.D == 64 && a.B == 32) return dispatch_chunk_umma_mt<T, 64, 32>(a, tmk, tmv, tmq, st);
+    if (a.D == 128 && a.B == 16) return dispatch_chunk_umma_mt<T, 128, 16>(a, tmk, tmv, tmq, st);
+    if (a.D == 128 && a.B == 32) return dispatch_chunk_umma_mt<T, 128, 32>(a, tmk, tmv, tmq, st);
     return cudaErrorNotSupported;
 }
 
