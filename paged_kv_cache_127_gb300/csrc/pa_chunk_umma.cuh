@@ -475,6 +475,8 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
             constexpr int kRowsPerPiece = 4096 / kRowBytes;  // rows in one 4 KB piece of the warp's Q slice
             constexpr int kLanesPerRow = kRowBytes / 16;
             constexpr int kRowsPerStore = 32 / kLanesPerRow;
+            const int lg = __ffs(G) - 1;
+            const int rbase = r0 + C::kM * u + 32 * wq;  // tile row of this warp's first row
             auto stage = [&](int rr, int c) {  // staging address of 16-byte chunk c of row rr
                 return qtile(u) + (uint32_t)((rr / kRowsPerPiece) * C::kQHalf + wq * 32 * 128) +
                        (uint32_t)((rr % kRowsPerPiece) * kRowBytes) + ((uint32_t)(c ^ (rr & 7)) << 4);
@@ -494,16 +496,17 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
                                      : "memory");
                 }
                 __syncwarp();
-#pragma unroll 4
+#pragma unroll
                 for (int i = 0; i < 32 / kRowsPerStore; ++i) {
                     const int rr = i * kRowsPerStore + lane / kLanesPerRow;  // row of this warp's 32
                     const int c = lane % kLanesPerRow;
-                    const int Rr = r0 + C::kM * u + 32 * wq + rr;
-                    const int tr = Rr / G;
+                    const int Rr = rbase + rr;
+                    const int tr = Rr >> lg;  // G is a power of two
                     const float4 v = *reinterpret_cast<const float4 *>(smem_raw + (stage(rr, c) - raw));
                     if (tr < n)
-                        *reinterpret_cast<float4 *>(a.out + ((size_t)(qs + tr) * a.Hq + kvh * G + Rr % G) * D +
-                                                    pass * W + 4 * c) = v;
+                        __stcs(reinterpret_cast<float4 *>(a.out + ((size_t)(qs + tr) * a.Hq + kvh * G + (Rr & (G - 1))) * D +
+                                                          pass * W + 4 * c),
+                               v);
                 }
                 __syncwarp();
             }
