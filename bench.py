@@ -365,7 +365,7 @@ def decode_config(step, workload: str, world: int) -> dict:
 
 
 # --------------------------------------------------------------------------- our arm
-SWEEP_WORKLOADS = ("gqa8b_b32", "mha7b", "prefix_cow", "long70b")
+SWEEP_WORKLOADS = ("gqa8b_b32", "mha7b", "prefix_cow", "long70b", "tiny")
 COMPONENT_REPS = 25          # per-call event pairs, each after an L2 flush
 BACK_TO_BACK_CALLS = 200     # pa_decode calls between one event pair
 SWEEP_STEPS = 50

@@ -218,3 +218,16 @@ def test_build_switch_of_the_cuda_core_comparison(monkeypatch):
     assert build._switches() == []
     monkeypatch.setenv("PA_DECODE_CUDA_CORE", "1")
     assert build._switches() == ["-DPA_DECODE_CUDA_CORE=1"]
+
+
+def test_host_device_copy_calls_refuse_bad_arguments(pa):
+    # checked on the host before any copy: null pointers with bytes > 0, and
+    # nothing to do for zero bytes
+    fake = ctypes.c_void_p(0x10000)
+    assert pa.lib.pa_copy_to_device(None, fake, 16, None) == pa.PA_ERR_INVALID
+    assert pa.lib.pa_copy_to_host(fake, None, 16, None) == pa.PA_ERR_INVALID
+    assert pa.lib.pa_copy_to_device(None, None, 0, None) == pa.PA_OK
+    assert pa.lib.pa_copy_to_host(None, None, 0, None) == pa.PA_OK
+    torch = pytest.importorskip("torch")
+    with pytest.raises(ValueError):     # the binding wants one host and one CUDA tensor
+        pa.pa_copy_to_device(torch.empty(4), torch.empty(4))
