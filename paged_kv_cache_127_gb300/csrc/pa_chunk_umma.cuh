@@ -263,6 +263,11 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
         const int u = warp == 1 ? 0 : 1;
         if (u < tiles) {
             constexpr uint32_t idesc_s = tc::f16_idesc(kBf16, false, C::kM, C::kN);
+            // Descriptors of the tile's Q and of stage 0's K, built once: a step's
+            // operands are these plus compile-time offsets (tc::desc_add), which
+            // keeps the issue loop to the MMAs themselves.
+            const uint64_t qdesc = tc::sw128_desc(qtile(u), 16u, 1024u);
+            const uint64_t kdesc0 = tc::sw128_desc(kvb, 16u, 1024u);
             bool ok = mbar_wait_bounded(q_full(u), 0u, kWaitLimit);
             for (int j = 0; ok && j < nch; ++j) {
                 const int st = j % C::kStages;
@@ -273,14 +278,13 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
                 if (!ok) break;
                 tc::fence_after_sync();
                 if (lane == 0) {
-                    const uint32_t kst = kvb + (uint32_t)(st * C::kStageBytes);
+                    const uint64_t kdesc = tc::desc_add(kdesc0, (uint32_t)(st * C::kStageBytes));
+                    const uint32_t sd = tbase + s_col(u, b);
 #pragma unroll
                     for (int k = 0; k < C::kKS; ++k) {
-                        const uint64_t ad =
-                            tc::sw128_desc(qtile(u) + (uint32_t)((k >> 2) * C::kQHalf) + 32u * (k & 3), 16u, 1024u);
-                        const uint64_t bd =
-                            tc::sw128_desc(kst + (uint32_t)((k >> 2) * C::kHalf) + 32u * (k & 3), 16u, 1024u);
-                        tc::mma_f16_ss(tbase + s_col(u, b), ad, bd, idesc_s, k > 0 ? 1u : 0u);
+                        tc::mma_f16_ss(sd, tc::desc_add(qdesc, (uint32_t)((k >> 2) * C::kQHalf + 32 * (k & 3))),
+                                       tc::desc_add(kdesc, (uint32_t)((k >> 2) * C::kHalf + 32 * (k & 3))), idesc_s,
+                                       k > 0 ? 1u : 0u);
                     }
                     tc::mma_commit(s_full(u, b));
                     tc::mma_commit(k_empty(st));  // the K stage is free once every tile's S MMAs complete
@@ -300,11 +304,12 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
         const int u = warp == 3 ? 0 : 1;
         if (u < tiles) {
             constexpr uint32_t idesc_o = tc::f16_idesc(kBf16, true, C::kM, D);
+            const uint64_t vdesc0 = tc::sw128_desc(kvb + (uint32_t)C::kTile, (uint32_t)C::kHalf, 1024u);
+            const uint32_t od = tbase + o_col(u);
             bool ok = true;
             for (int c = 0; ok && c < nch; ++c) {
                 const int b = c % kSB;
                 const int st = c % C::kStages;
-                const uint32_t vst = kvb + (uint32_t)(st * C::kStageBytes + C::kTile);
                 ok = mbar_wait_bounded(v_full(st), (uint32_t)(c / C::kStages) & 1u, kWaitLimit);
                 // tile 0's softmax zeroes the V rows that must not contribute; tile 0's own
                 // P V is issued after that (its P is published after the zeroing)
@@ -313,14 +318,14 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
                 if (!ok) break;
                 tc::fence_after_sync();
                 if (lane == 0) {
+                    const uint64_t vdesc = tc::desc_add(vdesc0, (uint32_t)(st * C::kStageBytes));
+                    const uint32_t pa0 = tbase + s_col(u, b);
 #pragma unroll
                     for (int part = 0; part < 2; ++part) {
 #pragma unroll
-                        for (int k = 0; k < C::kN / 16; ++k) {
-                            const uint32_t at = tbase + s_col(u, b) + (uint32_t)((C::kN / 2) * part + 8 * k);
-                            const uint64_t bd = tc::sw128_desc(vst + 2048u * k, (uint32_t)C::kHalf, 1024u);
-                            tc::mma_f16_ts(tbase + o_col(u), at, bd, idesc_o, (c > 0 || part > 0 || k > 0) ? 1u : 0u);
-                        }
+                        for (int k = 0; k < C::kN / 16; ++k)
+                            tc::mma_f16_ts(od, pa0 + (uint32_t)((C::kN / 2) * part + 8 * k), tc::desc_add(vdesc, 2048u * k),
+                                           idesc_o, (c > 0 || part > 0 || k > 0) ? 1u : 0u);
                     }
                     tc::mma_commit(o_done(u, b));
                     tc::mma_commit(v_empty(st));

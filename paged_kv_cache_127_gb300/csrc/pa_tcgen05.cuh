@@ -64,6 +64,12 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
     return d;
 }
 
+// The descriptor of the operand `bytes` further on (a multiple of 16): the
+// start-address field holds the shared-memory offset >> 4 in 14 bits, and
+// shared-memory offsets stay below 256 KB, so adding to the descriptor's low
+// word never carries out of the field.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) { return desc + (uint64_t)(bytes >> 4); }
+
 // Instruction descriptor of tcgen05.mma kind::f16 with an f32 accumulator:
 //   bits  4-5   D format (1: f32)
 //   bits  7-9   A format (0: f16, 1: bf16)     bits 10-12  B format
