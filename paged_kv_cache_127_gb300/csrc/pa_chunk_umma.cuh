@@ -61,12 +61,13 @@ namespace pa {
 template <int D, int MT>
 struct UmmaCfg {
     static constexpr int kM = 128;                         // rows per tile (TMEM lanes)
+    static constexpr int kMT = MT;                         // tiles per CTA
     static constexpr int kN = PA_CHUNK_UMMA_KEYS;          // keys per step
     static constexpr int kSB = 128 / kN;                   // S/P buffers per tile
     static constexpr int kBoxes = kN / 16;                 // 16-row TMA boxes per step
     static constexpr int kSub = D / 64;                    // 128-byte halves of a row
     static constexpr int kKS = D / 16;                     // k-steps of S = Q K^T
-    static constexpr int kStages = kN == 64 ? 4 : 8;
+    static constexpr int kStages = kN == 64 ? 3 : 6;
     // warps: 0 K producer, 2 V producer; per tile u an S issuer (warp 1, 4) and a
     // P V issuer (warp 3, 5); then one softmax warpgroup per tile
     static constexpr int kSoftWarp0 = MT == 2 ? 6 : 4;
@@ -76,12 +77,14 @@ struct UmmaCfg {
     static constexpr int kStageBytes = 2 * kTile;
     static constexpr int kQTile = kSub * kM * 128;         // Q of one tile (kSub halves of kM x 128 bytes)
     static constexpr int kQHalf = kM * 128;
+    // two sets of query tiles: a CTA loads the next work item's while its
+    // epilogue stages the finished item's output through the other set
     static constexpr size_t kQOff = 0;
-    static constexpr size_t kKVOff = kQOff + (size_t)MT * kQTile;
+    static constexpr size_t kKVOff = kQOff + (size_t)2 * MT * kQTile;
     static constexpr size_t kBarOff = kKVOff + (size_t)kStages * kStageBytes;
     // k_full, k_empty, v_full, v_empty, v_zeroed [kStages] | per tile: s_full, p_full, o_done [kSB],
-    // q_full, drain_s, drain_p
-    static constexpr int kTileBars = 3 * kSB + 3;
+    // q_full [2], q_free [2], drain_s, drain_p
+    static constexpr int kTileBars = 3 * kSB + 6;
     static constexpr int kNumBars = 5 * kStages + MT * kTileBars;
     static constexpr size_t kMaskOff = kBarOff + 8 * kNumBars;
     static constexpr size_t kSlotOff = kMaskOff + 4 * kStages;
@@ -104,6 +107,40 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
     return p;
 }
 
+// One work item of the tcgen05 path: KV head kvh of the plan's entry (sequence
+// s, tile group), i.e. rows r0 .. r0 + 128 MT - 1 of that head's
+// (query token, query head) rows, and the steps of keys those rows see.
+struct UmmaItem {
+    int s, kvh, r0, qs, n, len, tiles, nch;
+};
+
+// Work index w = entry * Hkv + kvh of the plan's longest-first list; false
+// past the list's end or when the entry has no rows (every role skips it alike).
+template <typename C>
+__device__ __forceinline__ bool umma_item(const ChunkArgs &a, int w, int nwork, UmmaItem &it) {
+    if (w >= nwork) return false;
+    const int4 e = a.plan_list[w / a.Hkv];
+    const int G = a.Hq / a.Hkv;
+    it.s = e.x;
+    it.kvh = w % a.Hkv;
+    it.r0 = e.y * C::kM * C::kMT;
+    it.qs = a.query_start[it.s];
+    it.n = a.query_start[it.s + 1] - it.qs;
+    if (it.n <= 0 || it.r0 >= it.n * G) return false;
+    it.len = a.context_lens[it.s];
+    it.tiles = min(C::kMT, (it.n * G - it.r0 + C::kM - 1) / C::kM);  // tiles with at least one row
+    const int t_last = min(it.n - 1, (it.r0 + C::kM * it.tiles - 1) / G);
+    it.nch = (it.len - it.n + t_last) / C::kN + 1;                // kN-key steps up to the last position
+    return true;
+}
+
+// Persistent: the CTAs take the longest-first list in rounds of gridDim.x
+// items, CTA b the b-th item of even rounds and the b-th from the end of odd
+// ones (a snake, which keeps the CTAs' totals within about one item of each
+// other), and each keeps its TMEM, barriers and K/V ring across its items.
+// Every role walks the same item sequence: the ring's stage and phase follow
+// the count g of steps so far, the S/P buffers and their phases the count c of
+// the tile's own steps, the query-tile sets the count of the tile's items.
 template <typename T, int D, int B, int MT>
 __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
     chunk_umma_kernel(const ChunkArgs a, const __grid_constant__ CUtensorMap tmk,
@@ -119,20 +156,13 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
     const int lane = threadIdx.x & 31;
 
     griddep_wait();  // the plan kernel's list of (sequence, tile group), longest first
-    const int item = blockIdx.x / a.Hkv;
-    if (item >= a.plan_hdr[0]) return;
-    const int4 e = a.plan_list[item];
-    const int s = e.x;
-    const int kvh = blockIdx.x % a.Hkv;
+    const int nwork = a.plan_hdr[0] * a.Hkv;
+    if ((int)blockIdx.x >= nwork) return;
     const int G = a.Hq / a.Hkv;
-    const int r0 = e.y * C::kM * MT;
-    const int qs = a.query_start[s];
-    const int n = a.query_start[s + 1] - qs;
-    if (n <= 0 || r0 >= n * G) return;
-    const int len = a.context_lens[s];
-    const int tiles = min(MT, (n * G - r0 + C::kM - 1) / C::kM);  // tiles with at least one row
-    const int t_last = min(n - 1, (r0 + C::kM * tiles - 1) / G);
-    const int nch = (len - n + t_last) / C::kN + 1;              // kN-key steps up to the last position
+    auto umma_work = [&](int rd) {
+        const int b = (rd & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x;
+        return rd * (int)gridDim.x + b;
+    };
 
     const uint32_t qb = base + (uint32_t)C::kQOff;
     const uint32_t kvb = base + (uint32_t)C::kKVOff;
@@ -149,10 +179,12 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
     auto p_full = [&](int u, int b) { return tbar(u, kSB + b); };
     // P V of a step on buffer b complete: O is up to date and S/P[u][b] may be rewritten
     auto o_done = [&](int u, int b) { return tbar(u, 2 * kSB + b); };
-    auto q_full = [&](int u) { return tbar(u, 3 * kSB); };
-    auto drain_s = [&](int u) { return tbar(u, 3 * kSB + 1); };
-    auto drain_p = [&](int u) { return tbar(u, 3 * kSB + 2); };
-    auto qtile = [&](int u) { return qb + (uint32_t)(u * C::kQTile); };
+    auto q_full = [&](int u, int x) { return tbar(u, 3 * kSB + x); };
+    // the epilogue has finished with query-tile set x of tile u (its staging area)
+    auto q_free = [&](int u, int x) { return tbar(u, 3 * kSB + 2 + x); };
+    auto drain_s = [&](int u) { return tbar(u, 3 * kSB + 4); };
+    auto drain_p = [&](int u) { return tbar(u, 3 * kSB + 5); };
+    auto qtile = [&](int x, int u) { return qb + (uint32_t)((x * MT + u) * C::kQTile); };
     auto s_col = [&](int u, int b) { return (uint32_t)(128 * u + C::kN * b); };
     auto o_col = [&](int u) { return C::kOCol + (uint32_t)(D * u); };
     int *vmask = reinterpret_cast<int *>(basep + C::kMaskOff);
@@ -161,9 +193,9 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kStages; ++i) {
             mbar_init(k_full(i), 1);
-            mbar_init(k_empty(i), tiles);  // one commit per tile's S issuer
-            mbar_init(v_full(i), 1);
-            mbar_init(v_empty(i), tiles);  // one commit per tile's P V issuer
+            mbar_init(k_empty(i), MT);  // one arrival per tile's S issuer (a commit, or a plain
+            mbar_init(v_full(i), 1);    // arrival when the item has no rows in that tile)
+            mbar_init(v_empty(i), MT);  // likewise from each tile's P V issuer
             mbar_init(v_zeroed(i), 4);
         }
         for (int u = 0; u < MT; ++u) {
@@ -172,7 +204,10 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
                 mbar_init(p_full(u, b), 4);
                 mbar_init(o_done(u, b), 1);
             }
-            mbar_init(q_full(u), 1);
+            for (int x = 0; x < 2; ++x) {
+                mbar_init(q_full(u, x), 1);
+                mbar_init(q_free(u, x), 4);
+            }
             mbar_init(drain_s(u), 1);
             mbar_init(drain_p(u), 1);
         }
@@ -190,91 +225,123 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
     if (warp == 0 || warp == 2) {
         // ------------------------------------------------------------ producers: K (warp 0), V (warp 2)
         const bool is_v = warp == 2;
-        const int32_t *row = a.block_tables + (size_t)s * a.max_blocks;
         const uint64_t pol = policy_evict_last();  // the other row tiles of this head reread these keys
+        const uint64_t qpol = policy_evict_first();
         const CUtensorMap *map = is_v ? &tmv : &tmk;
         const uint32_t ring = kvb + (is_v ? (uint32_t)C::kTile : 0u);
-        if (!is_v && lane == 0) {
-            // the query tiles first: tile u holds rows r0 + 128 u .., i.e. tokens
-            // (r0 + 128 u) / G .. of the sequence's chunk, G heads each; rows of
-            // tokens past the chunk are never used (their keys are all masked)
-            const uint64_t qpol = policy_evict_first();
-            for (int u = 0; u < tiles; ++u) {
-                mbar_arrive_expect_tx(q_full(u), (uint32_t)C::kQTile);
+        int g = 0;                  // ring steps issued
+        int ku[MT];                 // items of each tile so far (query-tile sets)
 #pragma unroll
-                for (int sb = 0; sb < C::kSub; ++sb)
-                    tma_load_3d(qtile(u) + (uint32_t)(sb * C::kQHalf), &tmq, sb * 64, kvh * G, qs + (r0 + C::kM * u) / G,
-                                q_full(u), qpol);
-            }
-        }
-        int j = 0;
-        for (; j < nch; ++j) {
-            const int st = j % C::kStages;
-            if (j >= C::kStages &&
-                !mbar_wait_bounded(is_v ? v_empty(st) : k_empty(st), (uint32_t)((j / C::kStages) - 1) & 1u,
-                                   kWaitLimit)) {
-                if (lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
-                break;
-            }
-            if (lane == 0) {
-                int mask = 0, blk[C::kBoxes];
+        for (int u = 0; u < MT; ++u) ku[u] = 0;
+        bool ok = true;
+        for (int rd = 0; ok && rd * (int)gridDim.x < nwork; ++rd) {
+            UmmaItem it;
+            if (!umma_item<C>(a, umma_work(rd), nwork, it)) continue;
+            const int32_t *row = a.block_tables + (size_t)it.s * a.max_blocks;
+            if (!is_v) {
+                // the query tiles first: tile u holds rows r0 + 128 u .., i.e. tokens
+                // (r0 + 128 u) / G .. of the sequence's chunk, G heads each; rows of
+                // tokens past the chunk are never used (their keys are all masked).
+                // Set x is free once the epilogue of the tile's item before last is done.
+                for (int u = 0; ok && u < it.tiles; ++u) {
+                    const int x = ku[u] & 1;
+                    if (ku[u] >= 2) ok = mbar_wait_bounded(q_free(u, x), (uint32_t)((ku[u] >> 1) - 1) & 1u, kWaitLimit);
+                    if (ok && lane == 0) {
+                        mbar_arrive_expect_tx(q_full(u, x), (uint32_t)C::kQTile);
 #pragma unroll
-                for (int i = 0; i < C::kBoxes; ++i) {
-                    const int tok = j * C::kN + 16 * i;
-                    blk[i] = -1;
-                    if (tok < len) {
-                        const int pbk = row[tok / B];
-                        if (pbk >= 0 && pbk < a.N) {
-                            blk[i] = pbk;
-                            mask |= 1 << i;
-                        } else if (!is_v) {
-                            set_error(a.err, PA_DEVERR_BAD_BLOCK);
+                        for (int sb = 0; sb < C::kSub; ++sb)
+                            tma_load_3d(qtile(x, u) + (uint32_t)(sb * C::kQHalf), &tmq, sb * 64, it.kvh * G,
+                                        it.qs + (it.r0 + C::kM * u) / G, q_full(u, x), qpol);
+                    }
+                    ++ku[u];
+                }
+                __syncwarp();
+                if (!ok) break;
+            }
+            for (int j = 0; j < it.nch; ++j, ++g) {
+                const int st = g % C::kStages;
+                if (g >= C::kStages &&
+                    !mbar_wait_bounded(is_v ? v_empty(st) : k_empty(st), (uint32_t)((g / C::kStages) - 1) & 1u,
+                                       kWaitLimit)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    int mask = 0, blk[C::kBoxes];
+#pragma unroll
+                    for (int i = 0; i < C::kBoxes; ++i) {
+                        const int tok = j * C::kN + 16 * i;
+                        blk[i] = -1;
+                        if (tok < it.len) {
+                            const int pbk = row[tok / B];
+                            if (pbk >= 0 && pbk < a.N) {
+                                blk[i] = pbk;
+                                mask |= 1 << i;
+                            } else if (!is_v) {
+                                set_error(a.err, PA_DEVERR_BAD_BLOCK);
+                            }
+                        }
+                    }
+                    if (is_v) vmask[st] = mask;  // read by the softmax after v_full (released with v_empty)
+                    const uint32_t bar = is_v ? v_full(st) : k_full(st);
+                    const uint32_t bytes = (uint32_t)__popc(mask) * C::kSub * 2048u;
+                    if (bytes == 0) {
+                        mbar_arrive(bar);
+                    } else {
+                        mbar_arrive_expect_tx(bar, bytes);
+                        const uint32_t dst = ring + (uint32_t)(st * C::kStageBytes);
+#pragma unroll
+                        for (int i = 0; i < C::kBoxes; ++i) {
+                            if (!(mask >> i & 1)) continue;
+                            const int y = (j * C::kN + 16 * i) % B;
+                            const int z = blk[i] * a.Hkv + it.kvh;
+#pragma unroll
+                            for (int sb = 0; sb < C::kSub; ++sb)
+                                tma_load_3d(dst + (uint32_t)(sb * C::kHalf + i * 2048), map, sb * 64, y, z, bar, pol);
                         }
                     }
                 }
-                if (is_v) vmask[st] = mask;  // read by the softmax after v_full (released with v_empty)
-                const uint32_t bar = is_v ? v_full(st) : k_full(st);
-                const uint32_t bytes = (uint32_t)__popc(mask) * C::kSub * 2048u;
-                if (bytes == 0) {
-                    mbar_arrive(bar);
-                } else {
-                    mbar_arrive_expect_tx(bar, bytes);
-                    const uint32_t dst = ring + (uint32_t)(st * C::kStageBytes);
-#pragma unroll
-                    for (int i = 0; i < C::kBoxes; ++i) {
-                        if (!(mask >> i & 1)) continue;
-                        const int y = (j * C::kN + 16 * i) % B;
-                        const int z = blk[i] * a.Hkv + kvh;
-#pragma unroll
-                        for (int sb = 0; sb < C::kSub; ++sb)
-                            tma_load_3d(dst + (uint32_t)(sb * C::kHalf + i * 2048), map, sb * 64, y, z, bar, pol);
-                    }
-                }
+                __syncwarp();
             }
-            __syncwarp();
         }
+        if (!ok && lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
         // copies still in flight must land before the CTA's shared memory is released
-        for (int k = max(0, j - C::kStages); k < j; ++k)
+        for (int k = max(0, g - C::kStages); k < g; ++k)
             mbar_wait_bounded(is_v ? v_full(k % C::kStages) : k_full(k % C::kStages), (uint32_t)(k / C::kStages) & 1u,
                               kWaitLimit);
     } else if (warp == 1 || (MT == 2 && warp == 4)) {
         // ------------------------------------------------------------ S = Q K^T issuer of tile u
         // One issuer per tile: a tile waits for its own P V, not the other tile's.
         const int u = warp == 1 ? 0 : 1;
-        if (u < tiles) {
-            constexpr uint32_t idesc_s = tc::f16_idesc(kBf16, false, C::kM, C::kN);
-            // Descriptors of the tile's Q and of stage 0's K, built once: a step's
-            // operands are these plus compile-time offsets (tc::desc_add), which
-            // keeps the issue loop to the MMAs themselves.
-            const uint64_t qdesc = tc::sw128_desc(qtile(u), 16u, 1024u);
-            const uint64_t kdesc0 = tc::sw128_desc(kvb, 16u, 1024u);
-            bool ok = mbar_wait_bounded(q_full(u), 0u, kWaitLimit);
-            for (int j = 0; ok && j < nch; ++j) {
-                const int st = j % C::kStages;
-                const int b = j % kSB;
-                ok = mbar_wait_bounded(k_full(st), (uint32_t)(j / C::kStages) & 1u, kWaitLimit);
-                // S/P[u][b] is free once the P V of step j - kSB has read P from it
-                if (ok && j >= kSB) ok = mbar_wait_bounded(o_done(u, b), (uint32_t)((j / kSB) - 1) & 1u, kWaitLimit);
+        constexpr uint32_t idesc_s = tc::f16_idesc(kBf16, false, C::kM, C::kN);
+        // Descriptors built once: a step's operands are these plus compile-time
+        // offsets (tc::desc_add), which keeps the issue loop to the MMAs themselves.
+        const uint64_t kdesc0 = tc::sw128_desc(kvb, 16u, 1024u);
+        int g = 0, c = 0, ku = 0;  // ring steps, this tile's steps, this tile's items
+        bool ok = true;
+        for (int rd = 0; ok && rd * (int)gridDim.x < nwork; ++rd) {
+            UmmaItem it;
+            if (!umma_item<C>(a, umma_work(rd), nwork, it)) continue;
+            if (u >= it.tiles) {
+                // no rows in this tile: release each K stage as it lands
+                for (int j = 0; ok && j < it.nch; ++j, ++g) {
+                    const int st = g % C::kStages;
+                    ok = mbar_wait_bounded(k_full(st), (uint32_t)(g / C::kStages) & 1u, kWaitLimit);
+                    if (ok && lane == 0) mbar_arrive(k_empty(st));
+                    __syncwarp();
+                }
+                continue;
+            }
+            const int x = ku & 1;
+            ok = mbar_wait_bounded(q_full(u, x), (uint32_t)(ku >> 1) & 1u, kWaitLimit);
+            ++ku;
+            const uint64_t qdesc = tc::sw128_desc(qtile(x, u), 16u, 1024u);
+            for (int j = 0; ok && j < it.nch; ++j, ++g, ++c) {
+                const int st = g % C::kStages;
+                const int b = c % kSB;
+                ok = mbar_wait_bounded(k_full(st), (uint32_t)(g / C::kStages) & 1u, kWaitLimit);
+                // S/P[u][b] is free once the P V of this tile's step c - kSB has read P from it
+                if (ok && c >= kSB) ok = mbar_wait_bounded(o_done(u, b), (uint32_t)((c / kSB) - 1) & 1u, kWaitLimit);
                 if (!ok) break;
                 tc::fence_after_sync();
                 if (lane == 0) {
@@ -291,29 +358,44 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
                 }
                 __syncwarp();
             }
-            if (!ok && lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
-            // every MMA issued by this thread has completed before TMEM is freed
-            if (lane == 0) tc::mma_commit(drain_s(u));
-            __syncwarp();
-            mbar_wait_bounded(drain_s(u), 0u, kWaitLimit);
         }
+        if (!ok && lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
+        // every MMA issued by this thread has completed before TMEM is freed
+        if (lane == 0) tc::mma_commit(drain_s(u));
+        __syncwarp();
+        mbar_wait_bounded(drain_s(u), 0u, kWaitLimit);
     } else if (warp == 3 || (MT == 2 && warp == 5)) {
         // ------------------------------------------------------------ O += P V issuer of tile u
         // Threads of their own: issuing S MMAs may block while the tensor pipe is
-        // busy, and must not hold back a P V whose P is ready.
+        // busy, and must not hold back a P V whose P is ready.  An item's first
+        // P V overwrites O: its P is published after the softmax warps have read
+        // the previous item's O out in their epilogue.
         const int u = warp == 3 ? 0 : 1;
-        if (u < tiles) {
-            constexpr uint32_t idesc_o = tc::f16_idesc(kBf16, true, C::kM, D);
-            const uint64_t vdesc0 = tc::sw128_desc(kvb + (uint32_t)C::kTile, (uint32_t)C::kHalf, 1024u);
-            const uint32_t od = tbase + o_col(u);
-            bool ok = true;
-            for (int c = 0; ok && c < nch; ++c) {
+        constexpr uint32_t idesc_o = tc::f16_idesc(kBf16, true, C::kM, D);
+        const uint64_t vdesc0 = tc::sw128_desc(kvb + (uint32_t)C::kTile, (uint32_t)C::kHalf, 1024u);
+        const uint32_t od = tbase + o_col(u);
+        int g = 0, c = 0;
+        bool ok = true;
+        for (int rd = 0; ok && rd * (int)gridDim.x < nwork; ++rd) {
+            UmmaItem it;
+            if (!umma_item<C>(a, umma_work(rd), nwork, it)) continue;
+            if (u >= it.tiles) {
+                // no rows in this tile: release each V stage as it lands
+                for (int j = 0; ok && j < it.nch; ++j, ++g) {
+                    const int st = g % C::kStages;
+                    ok = mbar_wait_bounded(v_full(st), (uint32_t)(g / C::kStages) & 1u, kWaitLimit);
+                    if (ok && lane == 0) mbar_arrive(v_empty(st));
+                    __syncwarp();
+                }
+                continue;
+            }
+            for (int j = 0; ok && j < it.nch; ++j, ++g, ++c) {
                 const int b = c % kSB;
-                const int st = c % C::kStages;
-                ok = mbar_wait_bounded(v_full(st), (uint32_t)(c / C::kStages) & 1u, kWaitLimit);
+                const int st = g % C::kStages;
+                ok = mbar_wait_bounded(v_full(st), (uint32_t)(g / C::kStages) & 1u, kWaitLimit);
                 // tile 0's softmax zeroes the V rows that must not contribute; tile 0's own
                 // P V is issued after that (its P is published after the zeroing)
-                if (ok && u > 0) ok = mbar_wait_bounded(v_zeroed(st), (uint32_t)(c / C::kStages) & 1u, kWaitLimit);
+                if (ok && u > 0) ok = mbar_wait_bounded(v_zeroed(st), (uint32_t)(g / C::kStages) & 1u, kWaitLimit);
                 if (ok) ok = mbar_wait_bounded(p_full(u, b), (uint32_t)(c / kSB) & 1u, kWaitLimit);
                 if (!ok) break;
                 tc::fence_after_sync();
@@ -325,150 +407,160 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
 #pragma unroll
                         for (int k = 0; k < C::kN / 16; ++k)
                             tc::mma_f16_ts(od, pa0 + (uint32_t)((C::kN / 2) * part + 8 * k), tc::desc_add(vdesc, 2048u * k),
-                                           idesc_o, (c > 0 || part > 0 || k > 0) ? 1u : 0u);
+                                           idesc_o, (j > 0 || part > 0 || k > 0) ? 1u : 0u);
                     }
                     tc::mma_commit(o_done(u, b));
                     tc::mma_commit(v_empty(st));
                 }
                 __syncwarp();
             }
-            if (!ok && lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
-            if (lane == 0) tc::mma_commit(drain_p(u));
-            __syncwarp();
-            mbar_wait_bounded(drain_p(u), 0u, kWaitLimit);
         }
-    } else if (warp >= C::kSoftWarp0 && (warp - C::kSoftWarp0) / 4 < tiles) {
+        if (!ok && lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
+        if (lane == 0) tc::mma_commit(drain_p(u));
+        __syncwarp();
+        mbar_wait_bounded(drain_p(u), 0u, kWaitLimit);
+    } else if (warp >= C::kSoftWarp0) {
         // ------------------------------------------------------------ softmax (one row per thread)
         const int u = (warp - C::kSoftWarp0) / 4;  // tile of this warpgroup
         const int wq = warp & 3;                 // TMEM lanes 32 * wq .. 32 * wq + 31
         const int r = 32 * wq + lane;            // row within the tile
-        const int R = r0 + C::kM * u + r;
-        const int t = R / G;
-        const bool valid = t < n;
-        const int h = kvh * G + R % G;
-        const int pos = len - n + t;
         const float sl = a.scale * 1.4426950408889634f;
         const uint32_t tl = tbase + ((uint32_t)(wq * 32) << 16);
-        float m_used = -INFINITY, l = 0.f;
+        int g = 0, c = 0, ku = 0;
         bool ok = true;
-        for (int j = 0; j < nch; ++j) {
-            const int b = j % kSB;
-            const int st = j % C::kStages;
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(s_full(u, b), (uint32_t)(j / kSB) & 1u, kWaitLimit));
-            if (!ok) break;
-            tc::fence_after_sync();
-            uint32_t sv[C::kN / 32][32];
-#pragma unroll
-            for (int q = 0; q < C::kN / 32; ++q) tc::tmem_ld32(tl + s_col(u, b) + 32u * q, sv[q]);
-            tc::tmem_wait_ld();
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(v_full(st), (uint32_t)(j / C::kStages) & 1u, kWaitLimit));
-            if (!ok) break;
-            const int mask = vmask[st];
-            const int lim = valid ? pos - j * C::kN : -1;  // last visible key of this step
-            // raw logits; the softmax scale is folded into the exponent's FFMA
-            float f[C::kN];
-#pragma unroll
-            for (int c = 0; c < C::kN; ++c) f[c] = __uint_as_float(sv[c >> 5][c & 31]);
-            float mul = sl;
-            if (!(sl > 0.f)) {
-                // a non-positive scale: scale first, mask to -inf
-#pragma unroll
-                for (int c = 0; c < C::kN; ++c) f[c] = (c <= lim && (mask >> (c >> 4) & 1)) ? f[c] * sl : -INFINITY;
-                mul = 1.f;
-            } else if (!(__all_sync(0xffffffffu, lim >= C::kN - 1) && mask == (1 << C::kBoxes) - 1)) {
-                // a step on the diagonal, past the context or over a block not loaded
-#pragma unroll
-                for (int c = 0; c < C::kN; ++c)
-                    if (!(c <= lim && (mask >> (c >> 4) & 1))) f[c] = -INFINITY;
+        for (int rd = 0; ok && rd * (int)gridDim.x < nwork; ++rd) {
+            UmmaItem it;
+            if (!umma_item<C>(a, umma_work(rd), nwork, it)) continue;
+            if (u >= it.tiles) {
+                g += it.nch;
+                continue;
             }
-            // row maximum as 8 independent chains (a single 64-long chain of
-            // dependent max operations would sit on the critical path)
-            float mx[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mx[i] = f[i];
-#pragma unroll
-            for (int c = 8; c < C::kN; ++c) mx[c & 7] = fmaxf(mx[c & 7], f[c]);
-            const float mr = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-            const float mc = mr * mul;  // -inf when nothing is visible
-            const bool need = mc > m_used + 8.f;
-            const float alpha = (need && j > 0) ? ex2(m_used - mc) : 1.f;
-            if (need) m_used = mc;
-            const float mu = m_used == -INFINITY ? 0.f : m_used;
-            // P = exp2(x - m) split into P_hi + P_lo, in registers before waiting,
-            // two keys per packed f32x2 operation; the row sum in 4 pair accumulators
-            uint32_t hw[C::kN / 2], lw[C::kN / 2];
-            uint64_t ls[4] = {0ull, 0ull, 0ull, 0ull};
-            const uint64_t mul2 = tc::f2(mul, mul), nmu2 = tc::f2(-mu, -mu);
-#pragma unroll
-            for (int v = 0; v < C::kN / 2; ++v) {
-                const float2 xa = tc::f2split(tc::fma2(tc::f2(f[2 * v], f[2 * v + 1]), mul2, nmu2));
-                const float p0 = ex2(xa.x), p1 = ex2(xa.y);
-                const uint64_t pp = tc::f2(p0, p1);
-                ls[v & 3] = tc::add2(ls[v & 3], pp);
-                hw[v] = M::pack(p0, p1);
-                const float2 hf = M::unpack(hw[v]);
-                const float2 d = tc::f2split(tc::sub2(pp, tc::f2(hf.x, hf.y)));
-                lw[v] = M::pack(d.x, d.y);
-            }
-            const float2 s01 = tc::f2split(tc::add2(ls[0], ls[1])), s23 = tc::f2split(tc::add2(ls[2], ls[3]));
-            l = l * alpha + ((s01.x + s01.y) + (s23.x + s23.y));
-            // O may be rescaled only once the P V of step j - 1 has landed in it
-            const bool rescale = j > 0 && __any_sync(0xffffffffu, need);
-            if (rescale) {
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait_bounded(o_done(u, (j - 1) % kSB), (uint32_t)((j - 1) / kSB) & 1u, kWaitLimit));
+            const int x = ku & 1;
+            ++ku;
+            const int n = it.n, len = it.len, nch = it.nch;
+            const int R = it.r0 + C::kM * u + r;
+            const int t = R / G;
+            const bool valid = t < n;
+            const int pos = len - n + t;
+            float m_used = -INFINITY, l = 0.f;
+            for (int j = 0; j < nch; ++j, ++g, ++c) {
+                const int b = c % kSB;
+                const int st = g % C::kStages;
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(s_full(u, b), (uint32_t)(c / kSB) & 1u, kWaitLimit));
                 if (!ok) break;
                 tc::fence_after_sync();
-#pragma unroll 1
-                for (int q = 0; q < D / 16; ++q) {
-                    uint32_t ov[16];
-                    tc::tmem_ld16(tl + o_col(u) + 16u * q, ov);
-                    tc::tmem_wait_ld();
+                uint32_t sv[C::kN / 32][32];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                    tc::tmem_st16(tl + o_col(u) + 16u * q, ov);
+                for (int q = 0; q < C::kN / 32; ++q) tc::tmem_ld32(tl + s_col(u, b) + 32u * q, sv[q]);
+                tc::tmem_wait_ld();
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(v_full(st), (uint32_t)(g / C::kStages) & 1u, kWaitLimit));
+                if (!ok) break;
+                const int mask = vmask[st];
+                const int lim = valid ? pos - j * C::kN : -1;  // last visible key of this step
+                // raw logits; the softmax scale is folded into the exponent's FFMA
+                float f[C::kN];
+#pragma unroll
+                for (int cc = 0; cc < C::kN; ++cc) f[cc] = __uint_as_float(sv[cc >> 5][cc & 31]);
+                float mul = sl;
+                if (!(sl > 0.f)) {
+                    // a non-positive scale: scale first, mask to -inf
+#pragma unroll
+                    for (int cc = 0; cc < C::kN; ++cc)
+                        f[cc] = (cc <= lim && (mask >> (cc >> 4) & 1)) ? f[cc] * sl : -INFINITY;
+                    mul = 1.f;
+                } else if (!(__all_sync(0xffffffffu, lim >= C::kN - 1) && mask == (1 << C::kBoxes) - 1)) {
+                    // a step on the diagonal, past the context or over a block not loaded
+#pragma unroll
+                    for (int cc = 0; cc < C::kN; ++cc)
+                        if (!(cc <= lim && (mask >> (cc >> 4) & 1))) f[cc] = -INFINITY;
+                }
+                // row maximum as 8 independent chains (a single 64-long chain of
+                // dependent max operations would sit on the critical path)
+                float mx[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx[i] = f[i];
+#pragma unroll
+                for (int cc = 8; cc < C::kN; ++cc) mx[cc & 7] = fmaxf(mx[cc & 7], f[cc]);
+                const float mr = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                const float mc = mr * mul;  // -inf when nothing is visible
+                const bool need = mc > m_used + 8.f;
+                const float alpha = (need && j > 0) ? ex2(m_used - mc) : 1.f;
+                if (need) m_used = mc;
+                const float mu = m_used == -INFINITY ? 0.f : m_used;
+                // P = exp2(x - m) split into P_hi + P_lo, in registers before waiting,
+                // two keys per packed f32x2 operation; the row sum in 4 pair accumulators
+                uint32_t hw[C::kN / 2], lw[C::kN / 2];
+                uint64_t ls[4] = {0ull, 0ull, 0ull, 0ull};
+                const uint64_t mul2 = tc::f2(mul, mul), nmu2 = tc::f2(-mu, -mu);
+#pragma unroll
+                for (int v = 0; v < C::kN / 2; ++v) {
+                    const float2 xa = tc::f2split(tc::fma2(tc::f2(f[2 * v], f[2 * v + 1]), mul2, nmu2));
+                    const float p0 = ex2(xa.x), p1 = ex2(xa.y);
+                    const uint64_t pp = tc::f2(p0, p1);
+                    ls[v & 3] = tc::add2(ls[v & 3], pp);
+                    hw[v] = M::pack(p0, p1);
+                    const float2 hf = M::unpack(hw[v]);
+                    const float2 d = tc::f2split(tc::sub2(pp, tc::f2(hf.x, hf.y)));
+                    lw[v] = M::pack(d.x, d.y);
+                }
+                const float2 s01 = tc::f2split(tc::add2(ls[0], ls[1])), s23 = tc::f2split(tc::add2(ls[2], ls[3]));
+                l = l * alpha + ((s01.x + s01.y) + (s23.x + s23.y));
+                // O may be rescaled only once the P V of step j - 1 has landed in it
+                const bool rescale = j > 0 && __any_sync(0xffffffffu, need);
+                if (rescale) {
+                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_done(u, (c - 1) % kSB),
+                                                                    (uint32_t)((c - 1) / kSB) & 1u, kWaitLimit));
+                    if (!ok) break;
+                    tc::fence_after_sync();
+#pragma unroll 1
+                    for (int q = 0; q < D / 16; ++q) {
+                        uint32_t ov[16];
+                        tc::tmem_ld16(tl + o_col(u) + 16u * q, ov);
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                        tc::tmem_st16(tl + o_col(u) + 16u * q, ov);
+                    }
+                    tc::tmem_wait_st();
+                }
+                // P into TMEM over this step's S (already read): P_hi, then P_lo
+                if constexpr (C::kN == 64) {
+                    tc::tmem_st32(tl + s_col(u, b), hw);
+                    tc::tmem_st32(tl + s_col(u, b) + 32u, lw);
+                } else {
+                    tc::tmem_st16(tl + s_col(u, b), hw);
+                    tc::tmem_st16(tl + s_col(u, b) + 16u, lw);
                 }
                 tc::tmem_wait_st();
-            }
-            // P into TMEM over this step's S (already read): P_hi, then P_lo
-            if constexpr (C::kN == 64) {
-                tc::tmem_st32(tl + s_col(u, b), hw);
-                tc::tmem_st32(tl + s_col(u, b) + 32u, lw);
-            } else {
-                tc::tmem_st16(tl + s_col(u, b), hw);
-                tc::tmem_st16(tl + s_col(u, b) + 16u, lw);
-            }
-            tc::tmem_wait_st();
-            // V rows of keys that were not loaded or lie past the context hold
-            // anything: tile 0's warpgroup zeroes them (row r < kN of this step's
-            // V, whole 128-byte rows) before it publishes its P and v_zeroed, which
-            // the other tile's P V issuer waits for.
-            if (u == 0 && r < C::kN && (j * C::kN + r >= len || !(mask >> (r >> 4) & 1))) {
-                const uint32_t vrow = kvb + (uint32_t)(st * C::kStageBytes + C::kTile + r * 128);
+                // V rows of keys that were not loaded or lie past the context hold
+                // anything: tile 0's warpgroup zeroes them (row r < kN of this step's
+                // V, whole 128-byte rows) before it publishes its P and v_zeroed, which
+                // the other tile's P V issuer waits for.
+                if (u == 0 && r < C::kN && (j * C::kN + r >= len || !(mask >> (r >> 4) & 1))) {
+                    const uint32_t vrow = kvb + (uint32_t)(st * C::kStageBytes + C::kTile + r * 128);
 #pragma unroll
-                for (int sb = 0; sb < C::kSub; ++sb)
+                    for (int sb = 0; sb < C::kSub; ++sb)
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vrow + sb * C::kHalf + c * 16),
-                                     "r"(0u)
-                                     : "memory");
+                        for (int cc = 0; cc < 8; ++cc)
+                            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vrow + sb * C::kHalf + cc * 16),
+                                         "r"(0u)
+                                         : "memory");
+                }
+                tc::fence_async_smem();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(p_full(u, b));
+                    if (u == 0) mbar_arrive(v_zeroed(st));
+                }
             }
-            tc::fence_async_smem();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(p_full(u, b));
-                if (u == 0) mbar_arrive(v_zeroed(st));
-            }
-        }
-        const int last = nch - 1;
-        if (!ok) {
-            if (lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
-        } else if (__all_sync(0xffffffffu, mbar_wait_bounded(o_done(u, last % kSB), (uint32_t)(last / kSB) & 1u,
-                                                              kWaitLimit))) {
-            // ---- epilogue: out = O / l.  The tile's S MMAs are complete, so its
-            // Q tile is free: each warp stages its 32 rows there, W columns at a
+            if (!ok) break;
+            const int last = c - 1;  // this tile's last step of the item
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_done(u, last % kSB), (uint32_t)(last / kSB) & 1u, kWaitLimit));
+            if (!ok) break;
+            // ---- epilogue: out = O / l.  The item's S MMAs are complete, so its
+            // query tile is free: each warp stages its 32 rows there, W columns at a
             // time (rows of W floats, 16-byte chunks swizzled by row), then
             // writes whole rows to global memory, lanes_per_row lanes per row,
             // instead of one 16-byte piece of 32 different rows per store.
@@ -481,10 +573,11 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
             constexpr int kLanesPerRow = kRowBytes / 16;
             constexpr int kRowsPerStore = 32 / kLanesPerRow;
             const int lg = __ffs(G) - 1;
-            const int rbase = r0 + C::kM * u + 32 * wq;  // tile row of this warp's first row
-            auto stage = [&](int rr, int c) {  // staging address of 16-byte chunk c of row rr
-                return qtile(u) + (uint32_t)((rr / kRowsPerPiece) * C::kQHalf + wq * 32 * 128) +
-                       (uint32_t)((rr % kRowsPerPiece) * kRowBytes) + ((uint32_t)(c ^ (rr & 7)) << 4);
+            const int rbase = it.r0 + C::kM * u + 32 * wq;  // tile row of this warp's first row
+            const uint32_t qt = qtile(x, u);
+            auto stage = [&](int rr, int cc) {  // staging address of 16-byte chunk cc of row rr
+                return qt + (uint32_t)((rr / kRowsPerPiece) * C::kQHalf + wq * 32 * 128) +
+                       (uint32_t)((rr % kRowsPerPiece) * kRowBytes) + ((uint32_t)(cc ^ (rr & 7)) << 4);
             };
 #pragma unroll
             for (int pass = 0; pass < 2; ++pass) {
@@ -504,21 +597,24 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 32 / kRowsPerStore; ++i) {
                     const int rr = i * kRowsPerStore + lane / kLanesPerRow;  // row of this warp's 32
-                    const int c = lane % kLanesPerRow;
+                    const int cc = lane % kLanesPerRow;
                     const int Rr = rbase + rr;
                     const int tr = Rr >> lg;  // G is a power of two
-                    const float4 v = *reinterpret_cast<const float4 *>(smem_raw + (stage(rr, c) - raw));
+                    const float4 v = *reinterpret_cast<const float4 *>(smem_raw + (stage(rr, cc) - raw));
                     if (tr < n)
-                        __stcs(reinterpret_cast<float4 *>(a.out + ((size_t)(qs + tr) * a.Hq + kvh * G + (Rr & (G - 1))) * D +
-                                                          pass * W + 4 * c),
+                        __stcs(reinterpret_cast<float4 *>(a.out + ((size_t)(it.qs + tr) * a.Hq + it.kvh * G +
+                                                                   (Rr & (G - 1))) * D + pass * W + 4 * cc),
                                v);
                 }
                 __syncwarp();
             }
+            // the query-tile set may be reloaded (async proxy) after these generic-proxy reads
+            tc::fence_async_smem();
             tc::fence_before_sync();
-        } else if (lane == 0) {
-            set_error(a.err, PA_DEVERR_TIMEOUT);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_free(u, x));
         }
+        if (!ok && lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -532,21 +628,24 @@ template <typename T, int D, int B, int MT>
 cudaError_t launch_chunk_umma_t(const ChunkArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
                                 const CUtensorMap &tmq, cudaStream_t st) {
     using C = UmmaCfg<D, MT>;
-    static std::atomic<int> configured[kMaxLaunchDevices];
-    int one = 0;
-    cudaError_t e = per_device_value(configured, &one, [](int, int *v) {
-        *v = 1;
-        return cudaFuncSetAttribute(chunk_umma_kernel<T, D, B, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)C::kSmem);
+    static std::atomic<int> sms_of[kMaxLaunchDevices];
+    int sms = 0;
+    cudaError_t e = per_device_value(sms_of, &sms, [](int dev, int *v) {
+        cudaError_t r = cudaFuncSetAttribute(chunk_umma_kernel<T, D, B, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)C::kSmem);
+        if (r != cudaSuccess) return r;
+        return cudaDeviceGetAttribute(v, cudaDevAttrMultiProcessorCount, dev);
     });
     if (e != cudaSuccess) return e;
     const int G = a.Hq / a.Hkv;
     const long long rows = (long long)a.max_query_len * G;
     const long long groups = (rows + C::kM * MT - 1) / (C::kM * MT);  // tile groups per sequence, at most
-    const long long ctas = groups * a.S * a.Hkv;                       // one per list entry and KV head
-    if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const long long work = groups * a.S * a.Hkv;                       // list entries x KV heads, at most
+    if (work > 0x7fffffffLL) return cudaErrorInvalidValue;
+    // persistent: one CTA per SM (the shared memory admits no second one)
+    const long long ctas = work < sms ? work : sms;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.gridDim = dim3((unsigned)(ctas > 0 ? ctas : 1));
     cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = st;
