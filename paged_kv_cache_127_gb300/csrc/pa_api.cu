@@ -245,6 +245,37 @@ cudaError_t query_tensor_map(const void *q, bool bf16, int D, int Hq, long long 
     return cudaSuccess;
 }
 
+// The output tensor map of the tcgen05 chunk path, likewise cached.
+cudaError_t output_tensor_map(float *o, int D, int Hq, long long T, int G, CUtensorMap *out) {
+    struct Entry {
+        const float *ptr = nullptr;
+        long long T = 0;
+        int D = 0, Hq = 0, G = 0;
+        CUtensorMap map;
+    };
+    thread_local Entry cache[2];
+    thread_local int next = 0;
+    for (auto &e : cache)
+        if (e.ptr == o && e.T == T && e.D == D && e.Hq == Hq && e.G == G) {
+            *out = e.map;
+            return cudaSuccess;
+        }
+    Entry &e = cache[next];
+    next = (next + 1) % 2;
+    cudaError_t rc = pa::make_output_tensor_map(&e.map, o, D, Hq, T, G);
+    if (rc != cudaSuccess) {
+        e.ptr = nullptr;
+        return rc;
+    }
+    e.ptr = o;
+    e.T = T;
+    e.D = D;
+    e.Hq = Hq;
+    e.G = G;
+    *out = e.map;
+    return cudaSuccess;
+}
+
 int32_t to_status(cudaError_t e) {
     if (e == cudaSuccess) return PA_OK;
     if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
@@ -422,12 +453,16 @@ int32_t pa_chunk_attention(const pa_dims *dims, const void *q, const void *k_cac
     e = pa::launch_chunk_plan(a, st);
     if (e != cudaSuccess) return to_status(e);
     if (umma) {
-        // the tcgen05 kernel loads its query tiles with TMA as well
-        CUtensorMap tmq;
+        // the tcgen05 kernel loads its query tiles and stores its output with TMA as well
+        CUtensorMap tmq, tmo;
         e = query_tensor_map(q, bf16, dims->head_dim, dims->num_q_heads, num_tokens,
                              dims->num_q_heads / dims->num_kv_heads, &tmq);
+        if (e == cudaSuccess)
+            e = output_tensor_map(out, dims->head_dim, dims->num_q_heads, num_tokens,
+                                  dims->num_q_heads / dims->num_kv_heads, &tmo);
         if (e != cudaSuccess) return PA_ERR_CUDA;
-        e = bf16 ? pa::launch_chunk_umma_bf16(a, tmk, tmv, tmq, st) : pa::launch_chunk_umma_f16(a, tmk, tmv, tmq, st);
+        e = bf16 ? pa::launch_chunk_umma_bf16(a, tmk, tmv, tmq, tmo, st)
+                 : pa::launch_chunk_umma_f16(a, tmk, tmv, tmq, tmo, st);
         return to_status(e);
     }
     e = bf16 ? pa::launch_chunk_mma_bf16(a, tmk, tmv, st) : pa::launch_chunk_mma_f16(a, tmk, tmv, st);

@@ -9,7 +9,7 @@ cudaError_t launch_chunk_mma_f16(const ChunkArgs &a, const CUtensorMap &tmk, con
     return dispatch_chunk_mma<__half>(a, tmk, tmv, st);
 }
 cudaError_t launch_chunk_umma_f16(const ChunkArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
-                                  const CUtensorMap &tmq, cudaStream_t st) {
-    return dispatch_chunk_umma<__half>(a, tmk, tmv, tmq, st);
+                                  const CUtensorMap &tmq, const CUtensorMap &tmo, cudaStream_t st) {
+    return dispatch_chunk_umma<__half>(a, tmk, tmv, tmq, tmo, st);
 }
 }  // namespace pa

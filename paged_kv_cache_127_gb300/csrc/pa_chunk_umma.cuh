@@ -99,12 +99,34 @@ struct UmmaCfg {
     static_assert(kOCol + MT * D <= kTmemCols, "TMEM budget");
     static_assert(kKVOff % 1024 == 0, "swizzle atoms 1024-byte aligned");
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
+    static_assert(kQTile % 16384 == 0, "query tile holds whole 16 KB output boxes");
 };
 
 __device__ __forceinline__ uint64_t policy_evict_last() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
     return p;
+}
+
+// TMA store of one box from shared memory (bulk-group completion), and the
+// waits on this thread's stores: until at most N are still reading shared
+// memory, and until all have completed.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int x, int y, int z, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%1, %2, %3}], [%4], %5;" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(x), "r"(y), "r"(z), "r"(src), "l"(policy)
+        : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Barrier over the 128 threads of one softmax warpgroup (ids 1 and 2; 0 is __syncthreads).
+__device__ __forceinline__ void warpgroup_sync(int id) {
+    asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
 }
 
 // One work item of the tcgen05 path: KV head kvh of the plan's entry (sequence
@@ -144,7 +166,8 @@ __device__ __forceinline__ bool umma_item(const ChunkArgs &a, int w, int nwork, 
 template <typename T, int D, int B, int MT>
 __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
     chunk_umma_kernel(const ChunkArgs a, const __grid_constant__ CUtensorMap tmk,
-                      const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmq) {
+                      const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmq,
+                      const __grid_constant__ CUtensorMap tmo) {
     using C = UmmaCfg<D, MT>;
     using M = Mma16<T>;
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
@@ -215,6 +238,7 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
         prefetch_tmap(&tmk);
         prefetch_tmap(&tmv);
         prefetch_tmap(&tmq);
+        prefetch_tmap(&tmo);
     }
     if (warp == 1) tc::tmem_alloc(smem_addr(tslot), C::kTmemCols);
     tc::fence_before_sync();
@@ -559,54 +583,89 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
             const int last = c - 1;  // this tile's last step of the item
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_done(u, last % kSB), (uint32_t)(last / kSB) & 1u, kWaitLimit));
             if (!ok) break;
-            // ---- epilogue: out = O / l.  The item's S MMAs are complete, so its
-            // query tile is free: each warp stages its 32 rows there, W columns at a
-            // time (rows of W floats, 16-byte chunks swizzled by row), then
-            // writes whole rows to global memory, lanes_per_row lanes per row,
-            // instead of one 16-byte piece of 32 different rows per store.
+            // ---- epilogue: out = O / l, staged through the item's query tile (its S
+            // MMAs are complete, so it is free).
             tc::fence_after_sync();
             tc::fence_async_smem();
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            constexpr int W = D / 2;                       // columns per pass
-            constexpr int kRowBytes = W * 4;               // 256 (D 128) or 128 (D 64)
-            constexpr int kRowsPerPiece = 4096 / kRowBytes;  // rows in one 4 KB piece of the warp's Q slice
-            constexpr int kLanesPerRow = kRowBytes / 16;
-            constexpr int kRowsPerStore = 32 / kLanesPerRow;
-            const int lg = __ffs(G) - 1;
-            const int rbase = it.r0 + C::kM * u + 32 * wq;  // tile row of this warp's first row
             const uint32_t qt = qtile(x, u);
-            auto stage = [&](int rr, int cc) {  // staging address of 16-byte chunk cc of row rr
-                return qt + (uint32_t)((rr / kRowsPerPiece) * C::kQHalf + wq * 32 * 128) +
-                       (uint32_t)((rr % kRowsPerPiece) * kRowBytes) + ((uint32_t)(cc ^ (rr & 7)) << 4);
-            };
+            if (it.r0 + C::kM * (u + 1) <= n * G) {
+                // A tile whose 128 rows all belong to the chunk: 32-column blocks, each
+                // staged as one TMA box (rows in (token, head) order, 128-byte
+                // swizzle) and stored by one thread while the warpgroup moves on;
+                // consecutive blocks take turns in the query tile's 16 KB parts.
+                constexpr int kParts = C::kQTile / 16384;  // 2 (D 128) or 1 (D 64)
+                const bool issuer = wq == 0 && lane == 0;
+                const uint64_t spol = policy_evict_first();
 #pragma unroll
-            for (int pass = 0; pass < 2; ++pass) {
-#pragma unroll
-                for (int q = 0; q < W / 32; ++q) {
+                for (int cb = 0; cb < D / 32; ++cb) {
+                    const uint32_t half = qt + (uint32_t)((cb % kParts) * 16384);
+                    if (cb >= kParts) {
+                        if (issuer) bulk_wait_read<kParts - 1>();  // the store of block cb - kParts has read this part
+                        warpgroup_sync(1 + u);
+                    }
                     uint32_t ov[32];
-                    tc::tmem_ld32(tl + o_col(u) + (uint32_t)(pass * W + 32 * q), ov);
+                    tc::tmem_ld32(tl + o_col(u) + (uint32_t)(32 * cb), ov);
                     tc::tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; i += 4)
-                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(stage(lane, 8 * q + i / 4)),
-                                     "f"(__uint_as_float(ov[i]) * inv), "f"(__uint_as_float(ov[i + 1]) * inv),
-                                     "f"(__uint_as_float(ov[i + 2]) * inv), "f"(__uint_as_float(ov[i + 3]) * inv)
+                    for (int i = 0; i < 8; ++i)
+                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(half + (uint32_t)(r * 128) +
+                                                                                      ((uint32_t)(i ^ (r & 7)) << 4)),
+                                     "f"(__uint_as_float(ov[4 * i]) * inv), "f"(__uint_as_float(ov[4 * i + 1]) * inv),
+                                     "f"(__uint_as_float(ov[4 * i + 2]) * inv), "f"(__uint_as_float(ov[4 * i + 3]) * inv)
                                      : "memory");
+                    tc::fence_async_smem();
+                    warpgroup_sync(1 + u);
+                    if (issuer) tma_store_3d(&tmo, half, 32 * cb, it.kvh * G, it.qs + (it.r0 + C::kM * u) / G, spol);
                 }
-                __syncwarp();
+                if (issuer) bulk_wait_read<0>();
+                warpgroup_sync(1 + u);
+            } else {
+                // A tile with rows past the chunk: each warp stages its 32 rows, W
+                // columns at a time (rows of W floats, 16-byte chunks swizzled by row),
+                // then writes whole rows of the chunk's tokens to global memory,
+                // lanes_per_row lanes per row, instead of one 16-byte piece of 32
+                // different rows per store.
+                constexpr int W = D / 2;                       // columns per pass
+                constexpr int kRowBytes = W * 4;               // 256 (D 128) or 128 (D 64)
+                constexpr int kRowsPerPiece = 4096 / kRowBytes;  // rows in one 4 KB piece of the warp's Q slice
+                constexpr int kLanesPerRow = kRowBytes / 16;
+                constexpr int kRowsPerStore = 32 / kLanesPerRow;
+                const int lg = __ffs(G) - 1;
+                const int rbase = it.r0 + C::kM * u + 32 * wq;  // tile row of this warp's first row
+                auto stage = [&](int rr, int cc) {  // staging address of 16-byte chunk cc of row rr
+                    return qt + (uint32_t)((rr / kRowsPerPiece) * C::kQHalf + wq * 32 * 128) +
+                           (uint32_t)((rr % kRowsPerPiece) * kRowBytes) + ((uint32_t)(cc ^ (rr & 7)) << 4);
+                };
 #pragma unroll
-                for (int i = 0; i < 32 / kRowsPerStore; ++i) {
-                    const int rr = i * kRowsPerStore + lane / kLanesPerRow;  // row of this warp's 32
-                    const int cc = lane % kLanesPerRow;
-                    const int Rr = rbase + rr;
-                    const int tr = Rr >> lg;  // G is a power of two
-                    const float4 v = *reinterpret_cast<const float4 *>(smem_raw + (stage(rr, cc) - raw));
-                    if (tr < n)
-                        __stcs(reinterpret_cast<float4 *>(a.out + ((size_t)(it.qs + tr) * a.Hq + it.kvh * G +
-                                                                   (Rr & (G - 1))) * D + pass * W + 4 * cc),
-                               v);
+                for (int pass = 0; pass < 2; ++pass) {
+#pragma unroll
+                    for (int q = 0; q < W / 32; ++q) {
+                        uint32_t ov[32];
+                        tc::tmem_ld32(tl + o_col(u) + (uint32_t)(pass * W + 32 * q), ov);
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(stage(lane, 8 * q + i / 4)),
+                                         "f"(__uint_as_float(ov[i]) * inv), "f"(__uint_as_float(ov[i + 1]) * inv),
+                                         "f"(__uint_as_float(ov[i + 2]) * inv), "f"(__uint_as_float(ov[i + 3]) * inv)
+                                         : "memory");
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 32 / kRowsPerStore; ++i) {
+                        const int rr = i * kRowsPerStore + lane / kLanesPerRow;  // row of this warp's 32
+                        const int cc = lane % kLanesPerRow;
+                        const int Rr = rbase + rr;
+                        const int tr = Rr >> lg;  // G is a power of two
+                        const float4 v = *reinterpret_cast<const float4 *>(smem_raw + (stage(rr, cc) - raw));
+                        if (tr < n)
+                            __stcs(reinterpret_cast<float4 *>(a.out + ((size_t)(it.qs + tr) * a.Hq + it.kvh * G +
+                                                                       (Rr & (G - 1))) * D + pass * W + 4 * cc),
+                                   v);
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
             }
             // the query-tile set may be reloaded (async proxy) after these generic-proxy reads
             tc::fence_async_smem();
@@ -615,6 +674,7 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
             if (lane == 0) mbar_arrive(q_free(u, x));
         }
         if (!ok && lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
+        if (wq == 0 && lane == 0) bulk_wait_all();  // this thread's output stores have completed
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -626,7 +686,7 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
 
 template <typename T, int D, int B, int MT>
 cudaError_t launch_chunk_umma_t(const ChunkArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
-                                const CUtensorMap &tmq, cudaStream_t st) {
+                                const CUtensorMap &tmq, const CUtensorMap &tmo, cudaStream_t st) {
     using C = UmmaCfg<D, MT>;
     static std::atomic<int> sms_of[kMaxLaunchDevices];
     int sms = 0;
@@ -654,24 +714,24 @@ cudaError_t launch_chunk_umma_t(const ChunkArgs &a, const CUtensorMap &tmk, cons
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, chunk_umma_kernel<T, D, B, MT>, a, tmk, tmv, tmq);
+    return cudaLaunchKernelEx(&cfg, chunk_umma_kernel<T, D, B, MT>, a, tmk, tmv, tmq, tmo);
 }
 
 // Two tiles per CTA once a sequence can fill them (chunk_umma_rows).
 template <typename T, int D, int B>
 cudaError_t dispatch_chunk_umma_mt(const ChunkArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
-                                   const CUtensorMap &tmq, cudaStream_t st) {
-    return a.umma_rows == 256 ? launch_chunk_umma_t<T, D, B, 2>(a, tmk, tmv, tmq, st)
-                              : launch_chunk_umma_t<T, D, B, 1>(a, tmk, tmv, tmq, st);
+                                   const CUtensorMap &tmq, const CUtensorMap &tmo, cudaStream_t st) {
+    return a.umma_rows == 256 ? launch_chunk_umma_t<T, D, B, 2>(a, tmk, tmv, tmq, tmo, st)
+                              : launch_chunk_umma_t<T, D, B, 1>(a, tmk, tmv, tmq, tmo, st);
 }
 
 template <typename T>
 cudaError_t dispatch_chunk_umma(const ChunkArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
-                                const CUtensorMap &tmq, cudaStream_t st) {
-    if (a.D == 64 && a.B == 16) return dispatch_chunk_umma_mt<T, 64, 16>(a, tmk, tmv, tmq, st);
-    if (a.D == 64 && a.B == 32) return dispatch_chunk_umma_mt<T, 64, 32>(a, tmk, tmv, tmq, st);
-    if (a.D == 128 && a.B == 16) return dispatch_chunk_umma_mt<T, 128, 16>(a, tmk, tmv, tmq, st);
-    if (a.D == 128 && a.B == 32) return dispatch_chunk_umma_mt<T, 128, 32>(a, tmk, tmv, tmq, st);
+                                const CUtensorMap &tmq, const CUtensorMap &tmo, cudaStream_t st) {
+    if (a.D == 64 && a.B == 16) return dispatch_chunk_umma_mt<T, 64, 16>(a, tmk, tmv, tmq, tmo, st);
+    if (a.D == 64 && a.B == 32) return dispatch_chunk_umma_mt<T, 64, 32>(a, tmk, tmv, tmq, tmo, st);
+    if (a.D == 128 && a.B == 16) return dispatch_chunk_umma_mt<T, 128, 16>(a, tmk, tmv, tmq, tmo, st);
+    if (a.D == 128 && a.B == 32) return dispatch_chunk_umma_mt<T, 128, 32>(a, tmk, tmv, tmq, tmo, st);
     return cudaErrorNotSupported;
 }
 

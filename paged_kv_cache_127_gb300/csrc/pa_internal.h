@@ -176,6 +176,7 @@ cudaError_t make_cache_tensor_map(CUtensorMap *map, const void *cache, bool bf16
 // 128 (query token, query head) rows of one tcgen05 tile of a KV head, the
 // left or right half of D, landing with the 128-byte swizzle.
 cudaError_t make_query_tensor_map(CUtensorMap *map, const void *q, bool bf16, int D, int Hq, long long T, int G);
+cudaError_t make_output_tensor_map(CUtensorMap *map, float *out, int D, int Hq, long long T, int G);
 
 // Process-unique id of the calling thread's current CUDA context, or 0 when
 // no context is current or the driver cannot say.  A device reset destroys
@@ -193,9 +194,9 @@ cudaError_t launch_chunk_merge(const ChunkArgs &a, cudaStream_t st);
 // tcgen05 path: one CTA per (128-row tile, KV head, sequence); tensor maps with
 // one (block, head) per box (make_cache_tensor_map with head_group 1).
 cudaError_t launch_chunk_umma_f16(const ChunkArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
-                                  const CUtensorMap &tmq, cudaStream_t st);
+                                  const CUtensorMap &tmq, const CUtensorMap &tmo, cudaStream_t st);
 cudaError_t launch_chunk_umma_bf16(const ChunkArgs &a, const CUtensorMap &tmk, const CUtensorMap &tmv,
-                                   const CUtensorMap &tmq, cudaStream_t st);
+                                   const CUtensorMap &tmq, const CUtensorMap &tmo, cudaStream_t st);
 
 cudaError_t launch_write_kv(const void *k, const void *v, const int64_t *slots, int T, int Hkv,
                             int row_bytes, int B, int N, void *k_cache, void *v_cache,

@@ -84,4 +84,20 @@ cudaError_t make_query_tensor_map(CUtensorMap *map, const void *q, bool bf16, in
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// The fp32 output [T, Hq, D] of the tcgen05 chunk path, for TMA stores: a box
+// is 32 columns (128 bytes, 128-byte swizzle) x G heads x 128 / G tokens, the
+// 128 rows of one query tile in (token, head) order.
+cudaError_t make_output_tensor_map(CUtensorMap *map, float *out, int D, int Hq, long long T, int G) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)T};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)Hq * D * 4};
+    const cuuint32_t box[3] = {32u, (cuuint32_t)G, (cuuint32_t)(128 / G)};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, out, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace pa
