@@ -261,7 +261,8 @@ PA_API int32_t pa_copy_blocks(const pa_dims *dims, void *k_cache, void *v_cache,
  * multi-layer pool [L, N, Hkv, B, D]; the block manager's ids are the same in
  * every layer).  layer_stride_bytes must be a multiple of 16 and at least one
  * pool (N * Hkv * B * D elements) when num_layers > 1.  One launch for all
- * layers.  Same preconditions and errors as pa_copy_blocks.
+ * layers, so num_layers is at most 32767 (PA_ERR_INVALID above).  Same
+ * preconditions and errors as pa_copy_blocks.
  */
 PA_API int32_t pa_copy_blocks_layers(const pa_dims *dims, void *k_caches, void *v_caches, int32_t num_layers,
                                      int64_t layer_stride_bytes, const int64_t *src_dst_pairs, int32_t num_pairs,
@@ -315,6 +316,7 @@ PA_API void pa_step_graph_destroy(pa_step_graph *graph);
  *                     block pairs[i][0] to host block pairs[i][1]; PA_SWAP_IN
  *                     copies host block pairs[i][0] to device block pairs[i][1]
  *   strides           bytes between layers (used when num_layers > 1)
+ *   num_layers        at most 32767 (PA_ERR_INVALID above)
  * One kernel moves every pair of every layer, K and V, with the GPU reading
  * and writing host memory directly; bit-exact.  Ids outside the pools are
  * skipped and flagged (PA_DEVERR_BAD_PAIR).  Destinations must be distinct.

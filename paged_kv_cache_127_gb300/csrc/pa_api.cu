@@ -497,12 +497,16 @@ int32_t pa_copy_blocks(const pa_dims *dims, void *k_cache, void *v_cache, const 
     return pa_copy_blocks_layers(dims, k_cache, v_cache, 1, layer_bytes, src_dst_pairs, num_pairs, stream);
 }
 
+// Layers one copy or swap launch covers: its grid has 2 * num_layers rows (K and V).
+constexpr int32_t kMaxCopyLayers = 32767;
+
 int32_t pa_copy_blocks_layers(const pa_dims *dims, void *k_caches, void *v_caches, int32_t num_layers,
                               int64_t layer_stride_bytes, const int64_t *src_dst_pairs, int32_t num_pairs,
                               void *stream) {
     int32_t rc = check_cache_dims(dims);
     if (rc != PA_OK) return rc;
-    if (num_pairs < 0 || num_layers < 0 || num_layers > 32768) return PA_ERR_INVALID;
+    // the copy grid's y extent is 2 * num_layers, at most 65535
+    if (num_pairs < 0 || num_layers < 0 || num_layers > kMaxCopyLayers) return PA_ERR_INVALID;
     if (num_pairs == 0 || num_layers == 0) return PA_OK;
     const int64_t block_bytes =
         (int64_t)dims->num_kv_heads * dims->block_size * dims->head_dim * elem_bytes(dims->kv_dtype);
@@ -538,7 +542,7 @@ int32_t pa_swap_blocks(const pa_dims *dims, void *k_cache, void *v_cache, void *
                        void *stream) {
     int32_t rc = check_cache_dims(dims);
     if (rc != PA_OK) return rc;
-    if (num_pairs < 0 || num_layers < 0 || num_layers > 32768 || num_host_blocks <= 0 ||
+    if (num_pairs < 0 || num_layers < 0 || num_layers > kMaxCopyLayers || num_host_blocks <= 0 ||
         (direction != PA_SWAP_OUT && direction != PA_SWAP_IN))
         return PA_ERR_INVALID;
     if (num_pairs == 0 || num_layers == 0) return PA_OK;

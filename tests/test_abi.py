@@ -231,3 +231,18 @@ def test_host_device_copy_calls_refuse_bad_arguments(pa):
     torch = pytest.importorskip("torch")
     with pytest.raises(ValueError):     # the binding wants one host and one CUDA tensor
         pa.pa_copy_to_device(torch.empty(4), torch.empty(4))
+
+
+def test_layer_copies_refuse_more_layers_than_one_launch_covers(pa):
+    # one launch moves K and V of every layer: its grid has 2 * num_layers rows,
+    # at most 65535, so 32768 layers are refused on the host (not left to fail
+    # at launch); refused before any pointer is used
+    d = pa.make_dims(num_seqs=1, num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16, num_blocks=10,
+                     max_blocks_per_seq=4, kv_dtype="bf16")
+    fake = ctypes.c_void_p(0x10000)
+    pool = 10 * 2 * 16 * 128 * 2
+    for layers in (32768, 1 << 30):
+        assert pa.lib.pa_copy_blocks_layers(ctypes.byref(d), fake, fake, layers, pool, fake, 1, None) == \
+            pa.PA_ERR_INVALID
+        assert pa.lib.pa_swap_blocks(ctypes.byref(d), fake, fake, fake, fake, 10, layers, pool, pool, fake, 1,
+                                     pa.PA_SWAP_OUT, None) == pa.PA_ERR_INVALID
