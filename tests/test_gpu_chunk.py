@@ -218,3 +218,25 @@ def test_chunk_bad_block_entry_is_flagged_and_skipped(gpu, path, nq):
             w = softmax(0.1 * (K[vis, h // G] @ q64[t, h]))
             want[t, h] = w @ V[vis, h // G]
     assert_attention_close(got[nq:], want)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_chunk_persistent_ctas_over_mixed_tiles(gpu, dtype):
+    # The tcgen05 kernel is persistent: each CTA walks several work items and
+    # keeps its TMEM, barriers and rings across them.  96 sequences with chunk
+    # lengths cycling through 96, 64, 33, 80, 0 and 70 tokens (G = 4, so 384,
+    # 256, 132, 320, 0 and 280 rows, two 128-row tiles per item) give 512 work
+    # items for at most one CTA per SM: items with two full tiles, a full and a
+    # partly filled tile, one tile (the second tile's roles skip the item), and
+    # sequences with no item, mixed within each CTA's sequence of items.
+    torch, pa = gpu
+    rng = synth.make_rng(3300 + (dtype == "bf16"))
+    Hq, Hkv, D, B = 16, 4, 128, 16
+    nq = [96, 64, 33, 80, 0, 70] * 16
+    lens = [n + int(x) for n, x in zip(nq, rng.integers(1, 300, len(nq)))]
+    q, kc, vc, tables, lens, qs = chunk_case(rng, dtype, Hq, Hkv, D, B, lens, nq)
+    scale = 1.0 / math.sqrt(D)
+    ref = oracle.chunk_attention(q, kc, vc, tables, lens, qs, scale, dtype)
+    got = run_chunk(torch, pa, dtype, q, kc, vc, tables, lens, qs, scale)
+    assert_attention_close(got, ref)
+    assert pa.pa_device_errors(clear=True) == 0
