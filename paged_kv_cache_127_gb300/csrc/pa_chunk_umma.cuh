@@ -7,12 +7,15 @@
 // "KV Cache Fundamentals" and "Block Table and Logical-to-Physical Mapping"),
 // for chunks whose (query token, query head) rows fill 128-row tiles.
 //
-// Work: one CTA per (MT 128-row tiles, KV head, sequence), taken from the plan
-// kernel's list, longest first (so the longest CTAs do not form the tail); the
-// rows of a KV head are r = t * G + gq.  The CTA walks the visible context in steps of
-// PA_CHUNK_UMMA_KEYS keys, with no split across CTAs (a tile has enough rows to keep the tensor
-// cores busy), so there is no merge.  MT = 2 tiles share every K/V load and
-// give the softmax two warpgroups.  Warp roles:
+// Work: a work item is (MT 128-row tiles, KV head, sequence); the rows of a
+// KV head are r = t * G + gq.  The item's CTA walks the visible context in
+// steps of PA_CHUNK_UMMA_KEYS keys, with no split across CTAs (a tile has
+// enough rows to keep the tensor cores busy), so there is no merge.  MT = 2
+// tiles share every K/V load and give the softmax two warpgroups.  The kernel
+// is persistent, one CTA per SM: the CTAs take the plan's longest-first list
+// in snake order and keep TMEM, barriers and rings from item to item; the next
+// item's query tiles (a second set) and first S overlap the finished item's
+// epilogue, whose output leaves by TMA stores.  Warp roles:
 //   warps 0, 2   producers of K and of V: 16-row TMA boxes (one KV head, both
 //                128-byte halves of D) into two 3-stage rings, so that a K
 //                stage is refilled as soon as its S MMAs complete, well before
