@@ -131,6 +131,19 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 __device__ __forceinline__ void warpgroup_sync(int id) {
     asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
 }
+// The same barrier, returning whether `pred` holds in all 128 threads.
+__device__ __forceinline__ bool warpgroup_all(int id, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, %2, 128, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id)
+        : "memory");
+    return r != 0;
+}
 
 // One work item of the tcgen05 path: KV head kvh of the plan's entry (sequence
 // s, tile group), i.e. rows r0 .. r0 + 128 MT - 1 of that head's
@@ -582,9 +595,14 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
                     if (u == 0) mbar_arrive(v_zeroed(st));
                 }
             }
-            if (!ok) break;
             const int last = c - 1;  // this tile's last step of the item
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_done(u, last % kSB), (uint32_t)(last / kSB) & 1u, kWaitLimit));
+            if (ok)
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait_bounded(o_done(u, last % kSB), (uint32_t)(last / kSB) & 1u, kWaitLimit));
+            // One decision for the warpgroup: every warp reaches this barrier (all
+            // its waits above are bounded), so the epilogue's barriers below are
+            // entered by all four warps or by none.
+            ok = warpgroup_all(1 + u, ok);
             if (!ok) break;
             // ---- epilogue: out = O / l, staged through the item's query tile (its S
             // MMAs are complete, so it is free).
