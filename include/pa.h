@@ -199,9 +199,10 @@ PA_API int32_t pa_decode_noalloc(const pa_dims *dims, const void *q, const void 
  *
  * Two kernels serve it: while max_query_len * Hq / Hkv (query rows per KV
  * head) is below 64, a persistent mma.sync kernel over context partitions
- * with a split-K merge; from 64 rows on, a tcgen05 kernel with 128-row tiles
- * whose accumulators live in tensor memory, one CTA per (tile, KV head,
- * sequence), walking each tile's whole context (no partitions, no merge).
+ * with a split-K merge; from 64 rows on, a persistent tcgen05 kernel with
+ * 128-row tiles whose accumulators live in tensor memory, one CTA per SM
+ * taking work items (tiles, KV head, sequence) longest first, each walking
+ * its tiles' whole context (no partitions, no merge).
  *
  * pa_chunk_workspace_bytes -- the scratch it needs: a work list of S * P * R
  * int4 entries after a 256-byte header, T ints (the partitions each query
