@@ -86,12 +86,14 @@ struct UmmaCfg {
     static constexpr size_t kKVOff = kQOff + (size_t)2 * MT * kQTile;
     static constexpr size_t kBarOff = kKVOff + (size_t)kStages * kStageBytes;
     // k_full, k_empty, v_full, v_empty, v_zeroed [kStages] | per tile: s_full, p_full, o_done [kSB],
-    // q_full [2], q_free [2], drain_s, drain_p
-    static constexpr int kTileBars = 3 * kSB + 6;
+    // q_full [2], q_free [2], drain_s, drain_p, item_ready [2]
+    static constexpr int kTileBars = 3 * kSB + 8;
     static constexpr int kNumBars = 5 * kStages + MT * kTileBars;
     static constexpr size_t kMaskOff = kBarOff + 8 * kNumBars;
     static constexpr size_t kSlotOff = kMaskOff + 4 * kStages;
-    static constexpr size_t kSmem = kSlotOff + 16 + 1024;  // + alignment slack
+    // published work items: per tile and query-tile set, 16 ints (UmmaSlot)
+    static constexpr size_t kItemOff = kSlotOff + 16;
+    static constexpr size_t kSmem = kItemOff + (size_t)MT * 2 * 64 + 1024;  // + alignment slack
     static constexpr uint32_t kTmemCols = 256 * MT;
     static constexpr uint32_t kOCol = 128 * MT;            // S[u][b] at 128 u + kN b; O[u] at kOCol + D u
     // P[u][b] aliases S[u][b]: P_hi in its first kN / 2 columns, P_lo in the next
@@ -151,6 +153,12 @@ __device__ __forceinline__ bool warpgroup_all(int id, bool pred) {
 struct UmmaItem {
     int s, kvh, r0, qs, n, len, tiles, nch;
 };
+// A work item as the K producer publishes it to a tile's roles: the item, the
+// ring step at which its first step falls, and an end mark (no more items).
+struct UmmaSlot {
+    UmmaItem it;
+    int g0, end;
+};
 
 // Work index w = entry * Hkv + kvh of the plan's longest-first list; false
 // past the list's end or when the entry has no rows (every role skips it alike).
@@ -172,13 +180,15 @@ __device__ __forceinline__ bool umma_item(const ChunkArgs &a, int w, int nwork, 
     return true;
 }
 
-// Persistent: the CTAs take the longest-first list in rounds of gridDim.x
-// items, CTA b the b-th item of even rounds and the b-th from the end of odd
-// ones (a snake, which keeps the CTAs' totals within about one item of each
-// other), and each keeps its TMEM, barriers and K/V ring across its items.
-// Every role walks the same item sequence: the ring's stage and phase follow
-// the count g of steps so far, the S/P buffers and their phases the count c of
-// the tile's own steps, the query-tile sets the count of the tile's items.
+// Persistent: each CTA's K producer claims the entries of the plan's
+// longest-first list one at a time (an atomic counter, so an SM takes the next
+// longest item as soon as it is ready for one) and publishes each to the roles
+// of every tile, through a shared-memory slot per tile and query-tile set; the
+// CTA keeps its TMEM, barriers and K/V ring across items.
+// Every tile's roles see every item, and those of a tile without rows in it
+// only release its ring stages.  The ring's stage and phase follow the count g
+// of steps so far, the S/P buffers and their phases the count c of the tile's
+// own steps, the slots and query-tile sets the count of items published.
 template <typename T, int D, int B, int MT>
 __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
     chunk_umma_kernel(const ChunkArgs a, const __grid_constant__ CUtensorMap tmk,
@@ -198,10 +208,6 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
     const int nwork = a.plan_hdr[0] * a.Hkv;
     if ((int)blockIdx.x >= nwork) return;
     const int G = a.Hq / a.Hkv;
-    auto umma_work = [&](int rd) {
-        const int b = (rd & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x;
-        return rd * (int)gridDim.x + b;
-    };
 
     const uint32_t qb = base + (uint32_t)C::kQOff;
     const uint32_t kvb = base + (uint32_t)C::kKVOff;
@@ -223,6 +229,16 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
     auto q_free = [&](int u, int x) { return tbar(u, 3 * kSB + 2 + x); };
     auto drain_s = [&](int u) { return tbar(u, 3 * kSB + 4); };
     auto drain_p = [&](int u) { return tbar(u, 3 * kSB + 5); };
+    // the K producer has published tile u's next item in slot x
+    auto item_ready = [&](int u, int x) { return tbar(u, 3 * kSB + 6 + x); };
+    UmmaSlot *slots = reinterpret_cast<UmmaSlot *>(basep + C::kItemOff);
+    auto slot = [&](int u, int x) -> UmmaSlot & { return slots[2 * u + x]; };
+    // wait for tile u's k-th published item (slot k & 1) and read it
+    auto take = [&](int u, int k, UmmaSlot &out) {
+        const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(item_ready(u, k & 1), (uint32_t)(k >> 1) & 1u, kWaitLimit));
+        if (got) out = slot(u, k & 1);
+        return got;
+    };
     auto qtile = [&](int x, int u) { return qb + (uint32_t)((x * MT + u) * C::kQTile); };
     auto s_col = [&](int u, int b) { return (uint32_t)(128 * u + C::kN * b); };
     auto o_col = [&](int u) { return C::kOCol + (uint32_t)(D * u); };
@@ -245,7 +261,8 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
             }
             for (int x = 0; x < 2; ++x) {
                 mbar_init(q_full(u, x), 1);
-                mbar_init(q_free(u, x), 4);
+                mbar_init(q_free(u, x), 4 + 2);  // the softmax warps, and both MMA issuers once they have read the slot
+                mbar_init(item_ready(u, x), 1);
             }
             mbar_init(drain_s(u), 1);
             mbar_init(drain_p(u), 1);
@@ -270,34 +287,61 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
         const CUtensorMap *map = is_v ? &tmv : &tmk;
         const uint32_t ring = kvb + (is_v ? (uint32_t)C::kTile : 0u);
         int g = 0;                  // ring steps issued
-        int ku[MT];                 // items of each tile so far (query-tile sets)
+        int ku[MT];                 // items published to each tile so far (query-tile sets)
 #pragma unroll
         for (int u = 0; u < MT; ++u) ku[u] = 0;
+        int k0 = 0;                 // V producer: tile 0's items taken so far
         bool ok = true;
-        for (int rd = 0; ok && rd * (int)gridDim.x < nwork; ++rd) {
+        for (;;) {
             UmmaItem it;
-            if (!umma_item<C>(a, umma_work(rd), nwork, it)) continue;
-            const int32_t *row = a.block_tables + (size_t)it.s * a.max_blocks;
             if (!is_v) {
-                // the query tiles first: tile u holds rows r0 + 128 u .., i.e. tokens
-                // (r0 + 128 u) / G .. of the sequence's chunk, G heads each; rows of
-                // tokens past the chunk are never used (their keys are all masked).
-                // Set x is free once the epilogue of the tile's item before last is done.
-                for (int u = 0; ok && u < it.tiles; ++u) {
+                // claim the next entry of the longest-first list (skipping entries
+                // without rows); past its end, publish the end mark to every tile
+                bool have = false;
+                while (!have) {
+                    int w = 0;
+                    if (lane == 0) w = atomicAdd(&a.plan_hdr[1], 1);
+                    w = __shfl_sync(0xffffffffu, w, 0);
+                    if (w >= nwork) break;
+                    have = umma_item<C>(a, w, nwork, it);
+                }
+                // every tile's roles see every item (a tile without rows in it releases
+                // its ring stages); slot x of tile u is free once the tile's roles are
+                // done with the item before last
+                for (int u = 0; ok && u < MT; ++u) {
                     const int x = ku[u] & 1;
                     if (ku[u] >= 2) ok = mbar_wait_bounded(q_free(u, x), (uint32_t)((ku[u] >> 1) - 1) & 1u, kWaitLimit);
                     if (ok && lane == 0) {
-                        mbar_arrive_expect_tx(q_full(u, x), (uint32_t)C::kQTile);
+                        UmmaSlot &sl = slot(u, x);
+                        if (have) sl.it = it;
+                        sl.g0 = g;
+                        sl.end = have ? 0 : 1;
+                        mbar_arrive(item_ready(u, x));
+                        if (have && u >= it.tiles) {
+                            mbar_arrive(q_full(u, x));  // no query tile: keep the set's phases in step
+                        } else if (have) {
+                            // the query tile: tile u holds rows r0 + 128 u .., i.e. tokens
+                            // (r0 + 128 u) / G .. of the sequence's chunk, G heads each; rows
+                            // of tokens past the chunk are never used (their keys are all masked)
+                            mbar_arrive_expect_tx(q_full(u, x), (uint32_t)C::kQTile);
 #pragma unroll
-                        for (int sb = 0; sb < C::kSub; ++sb)
-                            tma_load_3d(qtile(x, u) + (uint32_t)(sb * C::kQHalf), &tmq, sb * 64, it.kvh * G,
-                                        it.qs + (it.r0 + C::kM * u) / G, q_full(u, x), qpol);
+                            for (int sb = 0; sb < C::kSub; ++sb)
+                                tma_load_3d(qtile(x, u) + (uint32_t)(sb * C::kQHalf), &tmq, sb * 64, it.kvh * G,
+                                            it.qs + (it.r0 + C::kM * u) / G, q_full(u, x), qpol);
+                        }
                     }
                     ++ku[u];
                 }
                 __syncwarp();
-                if (!ok) break;
+                if (!ok || !have) break;
+            } else {
+                // the V producer follows tile 0's items (tile 0 has rows in every item)
+                UmmaSlot sl;
+                ok = take(0, k0++, sl);
+                if (!ok || sl.end) break;
+                it = sl.it;
             }
+            const int32_t *row = a.block_tables + (size_t)it.s * a.max_blocks;
             for (int j = 0; j < it.nch; ++j, ++g) {
                 const int st = g % C::kStages;
                 if (g >= C::kStages &&
@@ -343,6 +387,7 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
                 }
                 __syncwarp();
             }
+            if (!ok) break;
         }
         if (!ok && lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
         // copies still in flight must land before the CTA's shared memory is released
@@ -359,9 +404,15 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
         const uint64_t kdesc0 = tc::sw128_desc(kvb, 16u, 1024u);
         int g = 0, c = 0, ku = 0;  // ring steps, this tile's steps, this tile's items
         bool ok = true;
-        for (int rd = 0; ok && rd * (int)gridDim.x < nwork; ++rd) {
-            UmmaItem it;
-            if (!umma_item<C>(a, umma_work(rd), nwork, it)) continue;
+        for (;;) {
+            UmmaSlot sl;
+            ok = take(u, ku, sl);
+            if (!ok || sl.end) break;
+            const UmmaItem it = sl.it;
+            const int x = ku & 1;
+            const uint32_t qpar = (uint32_t)(ku >> 1) & 1u;
+            ++ku;
+            if (lane == 0) mbar_arrive(q_free(u, x));  // done with the slot
             if (u >= it.tiles) {
                 // no rows in this tile: release each K stage as it lands
                 for (int j = 0; ok && j < it.nch; ++j, ++g) {
@@ -370,11 +421,10 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
                     if (ok && lane == 0) mbar_arrive(k_empty(st));
                     __syncwarp();
                 }
+                if (!ok) break;
                 continue;
             }
-            const int x = ku & 1;
-            ok = mbar_wait_bounded(q_full(u, x), (uint32_t)(ku >> 1) & 1u, kWaitLimit);
-            ++ku;
+            ok = mbar_wait_bounded(q_full(u, x), qpar, kWaitLimit);
             const uint64_t qdesc = tc::sw128_desc(qtile(x, u), 16u, 1024u);
             for (int j = 0; ok && j < it.nch; ++j, ++g, ++c) {
                 const int st = g % C::kStages;
@@ -398,6 +448,7 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
                 }
                 __syncwarp();
             }
+            if (!ok) break;
         }
         if (!ok && lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
         // every MMA issued by this thread has completed before TMEM is freed
@@ -414,11 +465,15 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
         constexpr uint32_t idesc_o = tc::f16_idesc(kBf16, true, C::kM, D);
         const uint64_t vdesc0 = tc::sw128_desc(kvb + (uint32_t)C::kTile, (uint32_t)C::kHalf, 1024u);
         const uint32_t od = tbase + o_col(u);
-        int g = 0, c = 0;
+        int g = 0, c = 0, ku = 0;
         bool ok = true;
-        for (int rd = 0; ok && rd * (int)gridDim.x < nwork; ++rd) {
-            UmmaItem it;
-            if (!umma_item<C>(a, umma_work(rd), nwork, it)) continue;
+        for (;;) {
+            UmmaSlot sl;
+            ok = take(u, ku, sl);
+            if (!ok || sl.end) break;
+            const UmmaItem it = sl.it;
+            if (lane == 0) mbar_arrive(q_free(u, ku & 1));  // done with the slot
+            ++ku;
             if (u >= it.tiles) {
                 // no rows in this tile: release each V stage as it lands
                 for (int j = 0; ok && j < it.nch; ++j, ++g) {
@@ -427,6 +482,7 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
                     if (ok && lane == 0) mbar_arrive(v_empty(st));
                     __syncwarp();
                 }
+                if (!ok) break;
                 continue;
             }
             for (int j = 0; ok && j < it.nch; ++j, ++g, ++c) {
@@ -454,6 +510,7 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
                 }
                 __syncwarp();
             }
+            if (!ok) break;
         }
         if (!ok && lane == 0) set_error(a.err, PA_DEVERR_TIMEOUT);
         if (lane == 0) tc::mma_commit(drain_p(u));
@@ -468,15 +525,20 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
         const uint32_t tl = tbase + ((uint32_t)(wq * 32) << 16);
         int g = 0, c = 0, ku = 0;
         bool ok = true;
-        for (int rd = 0; ok && rd * (int)gridDim.x < nwork; ++rd) {
-            UmmaItem it;
-            if (!umma_item<C>(a, umma_work(rd), nwork, it)) continue;
-            if (u >= it.tiles) {
-                g += it.nch;
-                continue;
-            }
+        for (;;) {
+            UmmaSlot item;
+            ok = take(u, ku, item);
+            if (!ok || item.end) break;
+            const UmmaItem it = item.it;
             const int x = ku & 1;
             ++ku;
+            if (u >= it.tiles) {
+                // no rows in this tile: only the ring's step count moves on
+                g += it.nch;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(q_free(u, x));
+                continue;
+            }
             const int n = it.n, len = it.len, nch = it.nch;
             const int R = it.r0 + C::kM * u + r;
             const int t = R / G;
