@@ -12,10 +12,10 @@
 // steps of PA_CHUNK_UMMA_KEYS keys, with no split across CTAs (a tile has
 // enough rows to keep the tensor cores busy), so there is no merge.  MT = 2
 // tiles share every K/V load and give the softmax two warpgroups.  The kernel
-// is persistent, one CTA per SM: the CTAs take the plan's longest-first list
-// in snake order and keep TMEM, barriers and rings from item to item; the next
-// item's query tiles (a second set) and first S overlap the finished item's
-// epilogue, whose output leaves by TMA stores.  Warp roles:
+// is persistent, one CTA per SM: each CTA claims items from the plan's
+// longest-first list one at a time and keeps TMEM, barriers and rings from
+// item to item; the next item's query tiles (a second set) and first S overlap
+// the finished item's epilogue, whose output leaves by TMA stores.  Warp roles:
 //   warps 0, 2   producers of K and of V: 16-row TMA boxes (one KV head, both
 //                128-byte halves of D) into two 3-stage rings, so that a K
 //                stage is refilled as soon as its S MMAs complete, well before
