@@ -153,11 +153,11 @@ __device__ __forceinline__ bool warpgroup_all(int id, bool pred) {
 struct UmmaItem {
     int s, kvh, r0, qs, n, len, tiles, nch;
 };
-// A work item as the K producer publishes it to a tile's roles: the item, the
-// ring step at which its first step falls, and an end mark (no more items).
+// A work item as the K producer publishes it to a tile's roles, or the end
+// mark (no more items).
 struct UmmaSlot {
     UmmaItem it;
-    int g0, end;
+    int end;
 };
 
 // Work index w = entry * Hkv + kvh of the plan's longest-first list; false
@@ -314,7 +314,6 @@ __global__ void __launch_bounds__(UmmaCfg<D, MT>::kThreads, 1)
                     if (ok && lane == 0) {
                         UmmaSlot &sl = slot(u, x);
                         if (have) sl.it = it;
-                        sl.g0 = g;
                         sl.end = have ? 0 : 1;
                         mbar_arrive(item_ready(u, x));
                         if (have && u >= it.tiles) {
